@@ -1,0 +1,205 @@
+"""Seeded synthetic inputs for the verify-and-recover step.
+
+This module only draws random numbers in the shapes of the pages' workloads;
+it holds none of the method's arithmetic (no softmax, acceptance, residual or
+top-f).  Both the CUDA path and the CPU oracle read the tensors it returns.
+
+Workloads (vocabulary sizes stand in for the Llama-3 and Qwen3 families that
+"tanishqkumar/ssd" (sourcepulse summary, "Highlighted Details") supports; k,
+f, batch and temperature follow the README bench commands quoted on the
+Chinese README translation page, "基准测试" section):
+
+  tiny      B=1,   k=4, f=2, V=1000,   fp32, Z~N(0,2), D=Z+N(0,0.5), T=1
+  llama_sd  B=1,   k=6,      V=128256, bf16, Z~N(0,3)+5 peaks(+8), D=Z+N(0,1)
+  ssd_fork  B=1,   k=7, f=3, V=128256, bf16, as llama_sd, D has k+1 rows
+  qwen_b64  B=64,  k=5, f=3, V=151936, bf16, D=Z+N(0,sigma_b),
+            sigma_b in {0.3,1,3}, T=0.7
+  mixed512  B=512, k=7, f=4, V=151936, fp32, peaks at Zipf(1.1) ranks,
+            T=0 on half the rows (seeded permutation), U(0.5,1.2) elsewhere
+
+Draft tokens are drawn from softmax(D/T) with the Gumbel-max trick
+(argmax(D/T + G), G standard Gumbel), which needs no softmax; at T = 0 they
+are the draft argmax.  In SSD mode the draft holds k+1 rows and the extra
+token x_k (drawn from draft row k) is the mask at position k.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+# N(0, s): s is the standard deviation.
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    k: int
+    f: int            # 0: no forked recovery (sync SD)
+    V: int
+    dtype: str        # "f32" | "bf16"
+    z_std: float
+    d_std: float      # draft noise std (qwen_b64 overrides per row)
+    peaks: int
+    peak_boost: float
+    peak_place: str   # "uniform" | "zipf"
+    temp: str         # "1.0" | "0" | "0.7" | "mixed"
+    ssd: bool         # draft logits carry k+1 rows
+
+    @property
+    def Pd(self) -> int:
+        return self.k + 1 if self.ssd else self.k
+
+    def algorithmic_bytes(self) -> Dict[str, int]:
+        s = 4 if self.dtype == "f32" else 2
+        verify = self.B * (2 * self.k + 1) * self.V * s
+        fork = self.B * self.V * s if self.f > 0 else 0
+        return {"verify": verify, "fork": fork, "residual_max": 2 * self.B * self.V * s}
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 4, 2, 1000, "f32", 2.0, 0.5, 0, 0.0, "uniform", "1.0", True),
+    "llama_sd": Workload("llama_sd", 1, 6, 0, 128256, "bf16", 3.0, 1.0, 5, 8.0, "uniform", "1.0", False),
+    "ssd_fork": Workload("ssd_fork", 1, 7, 3, 128256, "bf16", 3.0, 1.0, 5, 8.0, "uniform", "1.0", True),
+    "qwen_b64": Workload("qwen_b64", 64, 5, 3, 151936, "bf16", 3.0, -1.0, 5, 8.0, "uniform", "0.7", True),
+    "mixed512": Workload("mixed512", 512, 7, 4, 151936, "f32", 3.0, 1.0, 5, 8.0, "zipf", "mixed", True),
+}
+ORDER = ["tiny", "llama_sd", "ssd_fork", "qwen_b64", "mixed512"]
+SEED_BASE = 1234
+
+
+def workload(name: str, **overrides) -> Workload:
+    return dataclasses.replace(WORKLOADS[name], **overrides)
+
+
+def default_seed(name: str) -> int:
+    return SEED_BASE + ORDER.index(name) + 1 if name in ORDER else SEED_BASE
+
+
+def _peak_indices(w: Workload, rows: int, rng: np.random.Generator) -> np.ndarray:
+    if w.peaks == 0:
+        return np.zeros((rows, 0), dtype=np.int64)
+    if w.peak_place == "uniform":
+        return rng.integers(0, w.V, size=(rows, w.peaks))
+    out = np.empty((rows, w.peaks), dtype=np.int64)
+    for r in range(rows):
+        for j in range(w.peaks):
+            while True:
+                v = int(rng.zipf(1.1)) - 1
+                if v < w.V:
+                    out[r, j] = v
+                    break
+    return out
+
+
+def temperatures(w: Workload, seed: int, temp: Optional[str] = None) -> torch.Tensor:
+    rng = np.random.default_rng(seed + 7)
+    t = temp if temp is not None else w.temp
+    if t == "mixed":
+        T = rng.uniform(0.5, 1.2, size=w.B).astype(np.float32)
+        zero = rng.permutation(w.B)[: w.B // 2]
+        T[zero] = 0.0
+    else:
+        T = np.full(w.B, float(t), dtype=np.float32)
+    return torch.from_numpy(T)
+
+
+def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
+                temp: Optional[str] = None, b_block: int = 32) -> Dict[str, torch.Tensor]:
+    """Draw one batch of the workload on ``device``.
+
+    Returns Z [B,k+1,V], D [B,Pd,V] (float32 or bfloat16), x [B,k] int32,
+    x_next [B] int32 (the draft token at position k in SSD mode, else -1),
+    mask [B,k+1,1] int32, T [B] f32, u_acc [B,k] f32, u_smp [B] f32.
+    Rows are generated in blocks of ``b_block`` batch rows to bound the
+    temporaries.
+    """
+    seed = default_seed(w.name) if seed is None else seed
+    device = torch.device(device)
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    B, k, V, Pd = w.B, w.k, w.V, w.Pd
+    rng = np.random.default_rng(seed)
+    peaks = torch.from_numpy(_peak_indices(w, B * (k + 1), rng)).to(device)
+    if w.d_std < 0:
+        sig = rng.choice(np.array([0.3, 1.0, 3.0]), size=B).astype(np.float32)
+    else:
+        sig = np.full(B, w.d_std, dtype=np.float32)
+    T = temperatures(w, seed, temp)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    Z = torch.empty((B, k + 1, V), dtype=dt, device=device)
+    D = torch.empty((B, Pd, V), dtype=dt, device=device)
+    x_all = torch.empty((B, Pd), dtype=torch.int32, device=device)
+    sig_t = torch.from_numpy(sig).to(device)
+    T_dev = T.to(device)
+    for b0 in range(0, B, b_block):
+        b1 = min(B, b0 + b_block)
+        nb = b1 - b0
+        z = torch.randn((nb, k + 1, V), generator=gen, device=device) * w.z_std
+        if w.peaks:
+            pk = peaks[b0 * (k + 1):b1 * (k + 1)].view(nb, k + 1, w.peaks)
+            z.scatter_add_(2, pk, torch.full(pk.shape, w.peak_boost, device=device))
+        zq = z.to(dt)
+        Z[b0:b1] = zq
+        # draft rows: target row i plus noise (row k of the target seeds the
+        # extra SSD draft row, as the other rows do)
+        src = zq[:, :Pd].float() if Pd <= k + 1 else None
+        d = src + torch.randn((nb, Pd, V), generator=gen, device=device) * sig_t[b0:b1].view(nb, 1, 1)
+        dq = d.to(dt)
+        D[b0:b1] = dq
+        # draft tokens: Gumbel-max sample from softmax(D/T); argmax at T = 0
+        tb = T_dev[b0:b1].view(nb, 1, 1)
+        u = torch.rand((nb, Pd, V), generator=gen, device=device)
+        g = -torch.log(-torch.log(u.clamp_min(1e-38)))
+        score = torch.where(tb > 0, dq.float() / torch.where(tb > 0, tb, torch.ones_like(tb)) + g,
+                            dq.float())
+        x_all[b0:b1] = torch.argmax(score, dim=2).to(torch.int32)
+        del z, zq, d, dq, u, g, score
+    u_acc = torch.rand((B, k), generator=gen, device=device)
+    u_smp = torch.rand((B,), generator=gen, device=device)
+    x = x_all[:, :k].contiguous()
+    if w.ssd:
+        x_next = x_all[:, k].contiguous()
+        mask = x_all[:, :, None].contiguous()
+    else:
+        x_next = torch.full((B,), -1, dtype=torch.int32, device=device)
+        mask = torch.cat([x, x_next[:, None]], dim=1)[:, :, None].contiguous()
+    return {"Z": Z, "D": D, "x": x, "x_next": x_next, "mask": mask,
+            "T": T_dev.contiguous(), "u_acc": u_acc.contiguous(),
+            "u_smp": u_smp.contiguous()}
+
+
+def cache_workload(fork_tok: torch.Tensor, depth: int, V: int, n_queries: int,
+                   seed: int) -> Dict[str, torch.Tensor]:
+    """Speculation-cache traffic for the SSD workload: one entry per forked
+    recovery token (b, j, fork_tok[b,j,r]) with a random depth-token payload,
+    plus ``n_queries`` lookups, half of them inserted keys and half keys that
+    were never inserted.  All tensors on the CPU (int32)."""
+    rng = np.random.default_rng(seed)
+    ft = fork_tok.detach().cpu().numpy()
+    B, P, f = ft.shape
+    bb, jj, rr = np.meshgrid(np.arange(B), np.arange(P), np.arange(f), indexing="ij")
+    ins_b = bb.reshape(-1).astype(np.int32)
+    ins_pos = jj.reshape(-1).astype(np.int32)
+    ins_tok = ft.reshape(-1).astype(np.int32)
+    keep = ins_tok >= 0
+    ins_b, ins_pos, ins_tok = ins_b[keep], ins_pos[keep], ins_tok[keep]
+    payload = rng.integers(0, V, size=(len(ins_b), depth)).astype(np.int32)
+    inserted = set(zip(ins_b.tolist(), ins_pos.tolist(), ins_tok.tolist()))
+    half = n_queries // 2
+    pick = rng.integers(0, len(ins_b), size=half)
+    qb = list(ins_b[pick]); qp = list(ins_pos[pick]); qt = list(ins_tok[pick])
+    while len(qb) < n_queries:
+        cand = (int(rng.integers(0, B)), int(rng.integers(0, P)), int(rng.integers(0, V)))
+        if cand in inserted:
+            continue
+        qb.append(cand[0]); qp.append(cand[1]); qt.append(cand[2])
+    order = rng.permutation(n_queries)
+    as_t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.int32)[order].copy())
+    return {"ins_b": torch.from_numpy(ins_b), "ins_pos": torch.from_numpy(ins_pos),
+            "ins_tok": torch.from_numpy(ins_tok), "payload": torch.from_numpy(payload),
+            "q_b": as_t(qb), "q_pos": as_t(qp), "q_tok": as_t(qt)}
