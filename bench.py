@@ -1,0 +1,415 @@
+"""Benchmark of the verify-and-recover step on GB300.
+
+One step = the whole hot path on one batch of the large-batch mixed-sampling
+workload (B=512, k=7, f=4, V=151936, fp32 logits, T=0 on half the rows and
+U(0.5,1.2) on the rest): ssd_verify_fork (row statistics, acceptance,
+first-reject prefix, recovery/bonus draw, forked top-f) followed by the
+speculation-cache step (clear, insert the forked recovery tokens, look up each
+row's realised outcome).  The metric is verified batch rows per second; the
+roofline object reports the achieved HBM bandwidth of the dominant kernel
+(the streaming statistics pass).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torch.distributed.run, one process per GPU, each on its own
+batch (weak scaling, no collective on the data path).  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mixed512"
+METRIC = "verify+recover rows/s"
+UNIT = "rows/s"
+FALLBACK_HBM_GBS = 6800.0
+CACHE_DEPTH = 7
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stats_kernel_mixed512.md")
+KERNEL_SOURCES = ["speculative_decoding_verification_70_gb300/csrc/ssd_stats.cu",
+                  "speculative_decoding_verification_70_gb300/csrc/ssd_device.cuh",
+                  "speculative_decoding_verification_70_gb300/csrc/ssd_layout.h"]
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as fh:
+                d = json.load(fh)
+            v = d.get("hbm_gbs")
+            if isinstance(v, dict):
+                v = v.get("value") or v.get("gbs")
+            if v:
+                return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic_per_launch():
+    """DRAM bytes per launch of the statistics kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    want = kernel_source_hash()
+    with open(PROFILE_SUMMARY) as fh:
+        for line in fh:
+            if line.startswith("machine:"):
+                try:
+                    d = json.loads(line[len("machine:"):])
+                except ValueError:
+                    return None
+                if d.get("kernel_source_hash") == want:
+                    return d.get("dram_bytes_per_launch_full")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+class Step:
+    """Device buffers and one step of the hot path."""
+
+    def __init__(self, ssd, w, inp, dev):
+        import torch
+        self.ssd, self.w, self.inp = ssd, w, inp
+        self.ws = ssd.new_workspace(ssd.workspace_bytes(w.B, w.k, w.V, w.f), dev)
+        self.out = {}
+        self.cache = ssd.SpecCache(1 << max(1, (2 * w.B * (w.k + 1) * w.f - 1).bit_length()),
+                                   CACHE_DEPTH)
+        g = torch.Generator(device=dev)
+        g.manual_seed(99)
+        self.payload = torch.randint(0, w.V, (w.B * (w.k + 1) * w.f, CACHE_DEPTH),
+                                     generator=g, device=dev, dtype=torch.int32)
+        self.look = None
+
+    def __call__(self):
+        i = self.inp
+        o = self.ssd.ssd_verify_fork(i["Z"], i["D"], i["x"], i["T"], i["u_acc"], i["u_smp"],
+                                     self.w.f, i["mask"], ws=self.ws, out=self.out)
+        self.cache.clear()
+        self.cache.insert_forks(o["fork_tok"], self.payload)
+        self.look = self.cache.lookup_outcome(o["accept_len"], o["out_tok"], out=self.look)
+        return o
+
+
+def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
+    """Time the oracle (as it stands, one host thread) on a bounded sample of
+    the batch rows: verify_recover + forked_topf + the dict cache."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    B = w.B if max_rows is None else min(w.B, max_rows)
+
+    def run(rows):
+        sel = {k: v[:rows].cpu() for k, v in inp.items()}
+        t0 = time.perf_counter()
+        ref = oracle.verify_recover(sel["Z"], sel["D"], sel["x"], sel["T"], sel["u_acc"],
+                                    sel["u_smp"])
+        fk = oracle.forked_topf(sel["D"], w.f, sel["mask"])
+        c = oracle.SpecCacheOracle(CACHE_DEPTH)
+        ft = fk["fork_tok"]
+        bb = np.repeat(np.arange(rows), (w.k + 1) * w.f)
+        pp = np.tile(np.repeat(np.arange(w.k + 1), w.f), rows)
+        c.insert(bb, pp, ft.reshape(-1), np.zeros((ft.size, CACHE_DEPTH), dtype=np.int32))
+        n = ref["accept_len"]
+        c.lookup(np.arange(rows), n, ref["out_tok"][np.arange(rows), np.maximum(n, 0)])
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    rows = int(max(1, min(B, target_s / max(t1, 1e-6))))
+    dt = run(rows)
+    return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d batch rows of %s, one host thread, %.1f s"
+                      % (rows, w.B, WORKLOAD, dt)}
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+    import speculative_decoding_verification_70_gb300 as ssd
+    from speculative_decoding_verification_70_gb300 import build as _build
+    from speculative_decoding_verification_70_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ssd.load_library()
+
+    w = W.workload(WORKLOAD)
+    inp = W.make_inputs(w, device=dev, seed=W.default_seed(WORKLOAD) + rank)
+    step = Step(ssd, w, inp, dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ssd.profile_begin(16 * args.steps + 16)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    prof = ssd.profile_end()
+    clock = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = world * w.B / (ms_max / 1e3 / args.steps)
+
+    # end to end through the public API with host buffers
+    e2e = e2e_run(ssd, w, inp, step, dev, max(3, min(args.steps, 40)), world)
+
+    launches = sum(v["launches"] for v in prof.values())
+    stats = prof.get("stats", {"launches": 0, "timed": 0, "total_ms": 0.0})
+    nbytes = w.B * 2 * (w.k + 1) * w.V * 4  # target k+1 rows + SSD draft k+1 rows, fp32
+    roof = None
+    if stats["timed"]:
+        per = stats["total_ms"] / stats["timed"]
+        peak, kind = measured_peaks()
+        achieved = nbytes / (per / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic_per_launch(),
+                "peak_kind": kind, "kernel": "stats_kernel", "bytes_per_launch": nbytes,
+                "ms_per_launch": round(per, 5),
+                "kernel_ms_per_step": {k: round(v["total_ms"] / max(1, v["timed"]), 5)
+                                       for k, v in prof.items()}}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded; shapes and value recipe of the large-batch mixed "
+                    "sampling workload)",
+            "config": {"workload": "%s: B=%d k=%d f=%d V=%d fp32 logits, T=0 on half the rows, "
+                                   "U(0.5,1.2) elsewhere; Zipf-placed peaks; cache depth %d"
+                                   % (WORKLOAD, w.B, w.k, w.f, w.V, CACHE_DEPTH),
+                       "global_batch": w.B * world, "per_gpu_batch": w.B,
+                       "l2": "inputs (%.2f GB per step) larger than L2" % (nbytes / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "gpu_launches": launches, "roofline": roof, "clocks": clock, "e2e": e2e}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(inp, w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    step.cache.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def e2e_run(ssd, w, inp, step, dev, steps, world):
+    """Same metric through the public API with pinned host buffers: every step
+    copies that step's inputs host->device, runs the step and reads the results
+    back device->host."""
+    import torch
+    names = ["Z", "D", "x", "T", "u_acc", "u_smp", "mask"]
+    host = {k: torch.empty(inp[k].shape, dtype=inp[k].dtype, pin_memory=True) for k in names}
+    for k in names:
+        host[k].copy_(inp[k])
+    outs = ["accept_len", "out_tok", "fork_tok"]
+    host_out = {}
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k in names:
+            inp[k].copy_(host[k], non_blocking=True)
+        o = step()
+        for k in outs:
+            if k not in host_out:
+                host_out[k] = torch.empty(o[k].shape, dtype=o[k].dtype, pin_memory=True)
+            host_out[k].copy_(o[k], non_blocking=True)
+        if "hit" not in host_out:
+            host_out["hit"] = torch.empty(step.look["hit"].shape, dtype=torch.int32, pin_memory=True)
+            host_out["tok_out"] = torch.empty(step.look["tok_out"].shape, dtype=torch.int32,
+                                              pin_memory=True)
+        host_out["hit"].copy_(step.look["hit"], non_blocking=True)
+        host_out["tok_out"].copy_(step.look["tok_out"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(world * w.B / (ms / 1e3 / steps), 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from speculative_decoding_verification_70_gb300 import workloads as W
+    oracle.build()
+    w0 = W.workload(WORKLOAD)
+    # bounded sample: rows per step chosen so that warm-up + timed steps take
+    # about a minute of host time
+    probe = W.make_inputs(W.workload(WORKLOAD, B=1), device="cpu", seed=W.default_seed(WORKLOAD))
+    t0 = time.perf_counter()
+    run_oracle_step(probe, w0, 1)
+    t_row = time.perf_counter() - t0
+    total = args.steps + max(3, args.warmup)
+    rows = int(max(1, min(64, 60.0 / (total * max(t_row, 1e-6)))))
+    w = W.workload(WORKLOAD, B=rows)
+    inp = W.make_inputs(w, device="cpu", seed=W.default_seed(WORKLOAD))
+    for _ in range(max(3, args.warmup)):
+        run_oracle_step(inp, w, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_oracle_step(inp, w, rows)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    sample = ("%d of %d batch rows of %s per step, one host thread" % (rows, w0.B, WORKLOAD))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; bounded sample of the workload)",
+            "config": {"workload": "%s: B=%d k=%d f=%d V=%d fp32 logits (sample of %d rows per step)"
+                                   % (WORKLOAD, w0.B, w0.k, w0.f, w0.V, rows)},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    del np
+    print(json.dumps(line), flush=True)
+
+
+def run_oracle_step(inp, w, rows):
+    import numpy as np
+    import oracle
+    ref = oracle.verify_recover(inp["Z"], inp["D"], inp["x"], inp["T"], inp["u_acc"], inp["u_smp"])
+    fk = oracle.forked_topf(inp["D"], w.f, inp["mask"])
+    c = oracle.SpecCacheOracle(CACHE_DEPTH)
+    ft = fk["fork_tok"]
+    bb = np.repeat(np.arange(rows), (w.k + 1) * w.f)
+    pp = np.tile(np.repeat(np.arange(w.k + 1), w.f), rows)
+    c.insert(bb, pp, ft.reshape(-1), np.zeros((ft.size, CACHE_DEPTH), dtype=np.int32))
+    n = ref["accept_len"]
+    c.lookup(np.arange(rows), n, ref["out_tok"][np.arange(rows), np.maximum(n, 0)])
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

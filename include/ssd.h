@@ -1,0 +1,294 @@
+/*
+ * ssd.h -- C ABI of the GB300 verify-and-recover library for speculative
+ * decoding (SD) and Speculative Speculative Decoding (SSD).
+ *
+ * Sources (page title, section):
+ *   [SUM]  "tanishqkumar/ssd" repository summary (thehardwarestore.ai),
+ *          module notes: the sampler mixes greedy and stochastic sampling by
+ *          temperature; get_forked_recovery_tokens_from_logits picks tokens by
+ *          top-k over logits with masking for cache hits and misses.
+ *   [SSD]  "SSD: drafting and verification on separate GPUs, in parallel"
+ *          (hysenlabs.com), "What changes in SSD": the target verifies the
+ *          draft in one forward pass; the method is exact; the drafter
+ *          pre-speculates likely outcomes and a correct guess is returned at
+ *          once; the roadmap's speculation cache.
+ *   [SPS]  speculative-sampling project summary (sourcepulse.org 1842340),
+ *          "How It Works": accept correct tokens, regenerate from the point of
+ *          divergence; Google's and DeepMind's algorithms.
+ *   [LKM]  the rule those algorithms share (Leviathan et al. 2023, Chen et
+ *          al. 2023): accept x_i with probability min(1, p_i(x_i)/q_i(x_i));
+ *          at the first rejection n draw from norm(max(0, p_n - q_n)); after
+ *          k accepts draw the bonus token from p_k.
+ *
+ * Conventions shared by every call:
+ *   - Tensor arguments are DEVICE pointers owned by the caller, unless a
+ *     parameter says "host".  Nothing is allocated per call; scratch comes
+ *     from a caller-supplied workspace (ssd_workspace_bytes) or from a
+ *     speculation cache made once by ssd_spec_cache_create.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and the call returns after enqueueing.
+ *   - Logits are row-major: row (b, i) of a [B, P, V] tensor starts at
+ *     element b*bstride + i*V.  dtype is SSD_F32 or SSD_BF16; bf16 is widened
+ *     to fp32 exactly before any arithmetic.
+ *   - Every call returns an ssd_status; no call aborts or throws.  Argument
+ *     errors are found on the host before anything is enqueued.  Errors in
+ *     the DATA (invalid temperature, NaN logits, out-of-range tokens, a full
+ *     cache) become per-row sentinels plus bits in a device error word, read
+ *     by ssd_get_device_error.
+ *   - Pointers need 4-byte alignment; logits, when the base pointer, V and
+ *     bstride all give 16-byte aligned rows, are read with 16-byte vector
+ *     loads, otherwise with scalar loads.
+ *   - A workspace must be zero-filled once before its first use (cudaMemset
+ *     or ssd_workspace_init); the calls keep it consistent afterwards.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssd_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,
+    SSD_ERR_UNSUPPORTED_DTYPE = 2,
+    SSD_ERR_CUDA = 3,
+    SSD_ERR_CACHE_FULL = 4,
+    SSD_ERR_TIMEOUT = 5,
+    SSD_ERR_WORKSPACE = 6
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+/* Bits of the device error word (ssd_get_device_error). */
+#define SSD_DEVERR_BAD_TEMPERATURE 0x1 /* T < 0 or NaN: row sentinel -1   */
+#define SSD_DEVERR_BAD_LOGITS 0x2      /* NaN (or +inf / all -inf at T>0) */
+#define SSD_DEVERR_BAD_TOKEN 0x4       /* draft token outside [0, V): -2  */
+#define SSD_DEVERR_CACHE_FULL 0x8      /* insert found no free slot       */
+#define SSD_DEVERR_TIMEOUT 0x10        /* a bounded wait on a copy ran out */
+
+/* Sentinels written to accept_len. */
+#define SSD_ROW_INVALID (-1)
+#define SSD_ROW_BAD_TOKEN (-2)
+
+/* Limits checked on the host. */
+#define SSD_MAX_K 31   /* draft length: one warp ballot holds k flags */
+#define SSD_MAX_F 16   /* forked recovery fan-out                    */
+#define SSD_MAX_M 64   /* masked tokens per (b, position)            */
+
+SSD_API const char *ssd_status_string(ssd_status s);
+
+/* Library version (major*10000 + minor*100 + patch). */
+SSD_API int ssd_version(void);
+
+/*
+ * Workspace bytes for ssd_verify / ssd_verify_fork / ssd_sample_residual /
+ * ssd_forked_recovery on batch B, draft length k, vocabulary V and fan-out
+ * f (0 if no forked recovery).  Returns 0 for invalid sizes.
+ */
+SSD_API size_t ssd_workspace_bytes(int B, int k, int V, int f);
+
+/* Workspace bytes for ssd_softmax_temp on `rows` rows of V logits. */
+SSD_API size_t ssd_softmax_workspace_bytes(int rows, int V);
+
+/* Zero-fill `bytes` of workspace `ws` on `stream` (one cudaMemsetAsync). */
+SSD_API ssd_status ssd_workspace_init(void *ws, size_t bytes, ssd_stream_t stream);
+
+/*
+ * Read (and, if clear != 0, reset) the device error word of a workspace or
+ * of a speculation cache workspace.  Synchronises `stream`.  *out is a host
+ * int32 receiving an OR of SSD_DEVERR_* bits.
+ */
+SSD_API ssd_status ssd_get_device_error(void *ws, ssd_stream_t stream, int32_t *out,
+                                int clear);
+
+/*
+ * ssd_softmax_temp -- temperature softmax per row ([SUM] sampler: greedy at
+ * temperature 0, stochastic otherwise).
+ *   logits : [rows, V] (dtype)
+ *   T      : [rows] fp32 temperatures.  T == 0 rows give the greedy
+ *            distribution: a one-hot at the argmax (lowest index on ties),
+ *            row_sum = 1.  T < 0 / NaN or an invalid row give m = S = NaN,
+ *            argmax = -1, probs = NaN and set the error word.
+ *   probs  : [rows, V] fp32 or NULL.  p_v = exp((z_v - m)/T) / S.
+ *   row_max, row_sum : [rows] fp32, m = max z, S = sum exp((z - m)/T).
+ *   row_argmax : [rows] int32.
+ *   ws     : ssd_softmax_workspace_bytes(rows, V) bytes.
+ */
+SSD_API ssd_status ssd_softmax_temp(const void *logits, ssd_dtype dtype, int rows, int V,
+                            const float *T, float *probs, float *row_max,
+                            float *row_sum, int32_t *row_argmax, void *ws,
+                            size_t ws_bytes, ssd_stream_t stream);
+
+/*
+ * ssd_verify -- acceptance, first-reject prefix and (optionally) the
+ * recovery/bonus draw, in one call ([SSD] verify in one pass; [SPS] point of
+ * divergence; [LKM] the rule).
+ *   Z        : target logits [B, k+1, V], batch stride z_bstride elements.
+ *   D        : draft logits [B, >=k, V], batch stride d_bstride; rows
+ *              0..k-1 are read.
+ *   x        : [B, k] int32 draft tokens.   T : [B] fp32 temperatures, used
+ *              for target and draft rows alike; T == 0 is greedy.
+ *   u_acc    : [B, k] fp32 uniforms in [0, 1).  Draft token i is accepted
+ *              iff u_acc[b,i] < p_i(x_i) / q_i(x_i) (q == 0: iff p > 0);
+ *              greedy rows accept iff x_i == argmax Z[b,i].
+ *   accept_len : [B] int32 out: n in 0..k, or SSD_ROW_INVALID /
+ *              SSD_ROW_BAD_TOKEN.
+ *   p_at_x, q_at_x : [B, k] fp32 out or NULL: p_i(x_i), q_i(x_i) (greedy:
+ *              1 if x_i is the argmax of that row, else 0).
+ *   u_smp    : [B] fp32 uniforms, or NULL to skip the draw.
+ *   out_tok  : [B, k+1] int32 out, required when u_smp is given: the n
+ *              accepted tokens, then the drawn token, then -1.  The draw is
+ *              the smallest j with C_j > u_smp * C_{V-1}, C the prefix sum of
+ *              w = max(0, p_n - q_n) (n < k; if w is all zero, w = p_n) or of
+ *              w = p_k (n == k); greedy rows take argmax Z[b,n].
+ *   ws       : ssd_workspace_bytes(B, k, V, 0) bytes (or more).
+ */
+SSD_API ssd_status ssd_verify(const void *Z, int64_t z_bstride, const void *D,
+                      int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                      const int32_t *x, const float *T, const float *u_acc,
+                      int32_t *accept_len, float *p_at_x, float *q_at_x,
+                      const float *u_smp, int32_t *out_tok, void *ws,
+                      size_t ws_bytes, ssd_stream_t stream);
+
+/*
+ * ssd_sample_residual -- the recovery/bonus draw alone, after an ssd_verify
+ * call on the same workspace, inputs and sizes that was given u_smp = NULL.
+ * accept_len may be that call's output or any values in 0..k (negative
+ * entries are skipped).  Writes out_tok [B, k+1] as ssd_verify does.
+ */
+SSD_API ssd_status ssd_sample_residual(const void *Z, int64_t z_bstride, const void *D,
+                               int64_t d_bstride, ssd_dtype dtype, int B, int k,
+                               int V, const int32_t *x, const float *T,
+                               const int32_t *accept_len, const float *u_smp,
+                               int32_t *out_tok, void *ws, size_t ws_bytes,
+                               ssd_stream_t stream);
+
+/*
+ * ssd_forked_recovery -- SSD's forked recovery tokens ([SUM]
+ * get_forked_recovery_tokens_from_logits: top-k over logits with masking).
+ *   L        : [B, P, V] logits, batch stride l_bstride.
+ *   mask     : [B, P, M] int32 tokens to skip at each (b, j) (entries
+ *              outside [0, V) skip nothing); may be NULL when M == 0.
+ *   fork_tok : [B, P, f] int32 out, fork_logit : [B, P, f] fp32 out: the f
+ *              largest unmasked logits of each row, logit descending then
+ *              index ascending.  Missing candidates are (-1, -inf); a row
+ *              holding a NaN gives (-1, NaN) and sets the error word.
+ *   ws       : ssd_workspace_bytes(B, P-1, V, f) bytes (or more).
+ */
+SSD_API ssd_status ssd_forked_recovery(const void *L, int64_t l_bstride, ssd_dtype dtype,
+                               int B, int P, int V, int f, const int32_t *mask,
+                               int M, int32_t *fork_tok, float *fork_logit,
+                               void *ws, size_t ws_bytes, ssd_stream_t stream);
+
+/*
+ * ssd_verify_fork -- ssd_verify and ssd_forked_recovery over the draft
+ * buffer in one pass over the logits.  D must hold P = k+1 rows per batch
+ * row (the SSD draft: rows 0..k-1 feed acceptance, rows 0..k the forked
+ * recovery).  Arguments as in the two calls; ws: ssd_workspace_bytes(B, k,
+ * V, f).
+ */
+SSD_API ssd_status ssd_verify_fork(const void *Z, int64_t z_bstride, const void *D,
+                           int64_t d_bstride, ssd_dtype dtype, int B, int k,
+                           int V, const int32_t *x, const float *T,
+                           const float *u_acc, int32_t *accept_len,
+                           float *p_at_x, float *q_at_x, const float *u_smp,
+                           int32_t *out_tok, int f, const int32_t *mask, int M,
+                           int32_t *fork_tok, float *fork_logit, void *ws,
+                           size_t ws_bytes, ssd_stream_t stream);
+
+/*
+ * Speculation cache ([SSD] roadmap: the speculation cache; [SUM] cache
+ * hits and misses).  An open-addressing table on the device mapping the key
+ * (b, position, token) to `depth` draft tokens.  Keys compare exactly, so the
+ * hash only decides slots, never results.  Inserts apply in input order (the
+ * last duplicate wins, also across calls).  Probing is bounded by the
+ * capacity: an insert that finds no slot is dropped and sets
+ * SSD_DEVERR_CACHE_FULL.  Limits: b < 2^24, position < 256, token >= 0.
+ */
+typedef struct ssd_spec_cache ssd_spec_cache;
+
+/* capacity: power of two >= 2; depth >= 1.  Allocates device memory once
+ * (on the current device). */
+SSD_API ssd_status ssd_spec_cache_create(int capacity, int depth, ssd_spec_cache **out);
+SSD_API void ssd_spec_cache_destroy(ssd_spec_cache *cache);
+SSD_API ssd_status ssd_spec_cache_clear(ssd_spec_cache *cache, ssd_stream_t stream);
+
+/* n keys (b[i], pos[i], tok[i]) -> payload[i*depth .. +depth). */
+SSD_API ssd_status ssd_spec_cache_insert(ssd_spec_cache *cache, const int32_t *b,
+                                 const int32_t *pos, const int32_t *tok,
+                                 const int32_t *payload, int n,
+                                 ssd_stream_t stream);
+
+/* hit[i] = 1 and tok_out[i*depth..] = payload on a hit; 0 and -1 on a miss
+ * (keys with a negative token or out-of-range b/pos always miss). */
+SSD_API ssd_status ssd_spec_cache_lookup(const ssd_spec_cache *cache, const int32_t *b,
+                                 const int32_t *pos, const int32_t *tok, int n,
+                                 int32_t *hit, int32_t *tok_out,
+                                 ssd_stream_t stream);
+
+/* Insert the forked recovery tokens directly: key (b, j, fork_tok[b,j,r])
+ * -> payload[((b*P + j)*f + r)*depth ..] for every fork_tok >= 0. */
+SSD_API ssd_status ssd_spec_cache_insert_forks(ssd_spec_cache *cache,
+                                       const int32_t *fork_tok, int B, int P,
+                                       int f, const int32_t *payload,
+                                       ssd_stream_t stream);
+
+/* Look up each row's realised outcome: key (b, n_b, out_tok[b, n_b]) with
+ * n_b = accept_len[b] (rows with n_b < 0 miss).  hit [B], tok_out [B,depth]. */
+SSD_API ssd_status ssd_spec_cache_lookup_outcome(const ssd_spec_cache *cache,
+                                         const int32_t *accept_len,
+                                         const int32_t *out_tok, int B, int k,
+                                         int32_t *hit, int32_t *tok_out,
+                                         ssd_stream_t stream);
+
+/* Read (and optionally clear) the cache's device error word; syncs stream. */
+SSD_API ssd_status ssd_spec_cache_get_error(ssd_spec_cache *cache, ssd_stream_t stream,
+                                    int32_t *out, int clear);
+
+SSD_API int ssd_spec_cache_capacity(const ssd_spec_cache *cache);
+SSD_API int ssd_spec_cache_depth(const ssd_spec_cache *cache);
+
+/*
+ * Launch profiler (observability, not part of the method).  Between
+ * ssd_profile_begin and ssd_profile_end every kernel the library launches
+ * from this process is bracketed by a pair of CUDA events recorded on the
+ * launch stream (at most max_launches launches; later ones go unrecorded but
+ * are still counted).  ssd_profile_end waits for the recorded events and
+ * fills out[0 .. *n_out) with one entry per kernel name: launches and total
+ * device time.  Events are created at begin and destroyed at end.
+ */
+typedef struct {
+    char name[40];
+    int launches;
+    int timed;          /* launches with recorded events */
+    double total_ms;    /* sum of event-measured durations of timed launches */
+} ssd_profile_entry;
+
+SSD_API ssd_status ssd_profile_begin(int max_launches);
+SSD_API ssd_status ssd_profile_end(ssd_profile_entry *out, int cap, int *n_out);
+
+/*
+ * Self-test hook for the library's extended-precision exponential (used by
+ * the recovery draw): out[i] = 2^(x_hi[i] + x_lo[i]) in double, for
+ * x_hi <= 0.  Device pointers, n >= 0.  Not part of the verify path.
+ */
+SSD_API ssd_status ssd_selftest_exp2(const float *x_hi, const float *x_lo, double *out,
+                             int n, ssd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_GB300_H */

@@ -1,0 +1,397 @@
+"""ctypes binding of libssd_gb300.so (include/ssd.h).
+
+Argument marshalling only: torch supplies device memory and the current
+stream; every step of the verify-and-recover path runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library is missing or a tensor is
+not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssd_gb300.so")
+
+SSD_F32 = 0
+SSD_BF16 = 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED_DTYPE",
+          3: "SSD_ERR_CUDA", 4: "SSD_ERR_CACHE_FULL", 5: "SSD_ERR_TIMEOUT",
+          6: "SSD_ERR_WORKSPACE"}
+DEVERR_BAD_TEMPERATURE = 0x1
+DEVERR_BAD_LOGITS = 0x2
+DEVERR_BAD_TOKEN = 0x4
+DEVERR_CACHE_FULL = 0x8
+
+# (name, restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L = ctypes.c_int64
+_Z = ctypes.c_size_t
+SIGNATURES = [
+    ("ssd_status_string", ctypes.c_char_p, [_I]),
+    ("ssd_version", _I, []),
+    ("ssd_workspace_bytes", _Z, [_I, _I, _I, _I]),
+    ("ssd_softmax_workspace_bytes", _Z, [_I, _I]),
+    ("ssd_workspace_init", _I, [_P, _Z, _P]),
+    ("ssd_get_device_error", _I, [_P, _P, _P, _I]),
+    ("ssd_softmax_temp", _I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    ("ssd_verify", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                        _P, _Z, _P]),
+    ("ssd_sample_residual", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                 _Z, _P]),
+    ("ssd_forked_recovery", _I, [_P, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _Z, _P]),
+    ("ssd_verify_fork", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                             _P, _I, _P, _I, _P, _P, _P, _Z, _P]),
+    ("ssd_spec_cache_create", _I, [_I, _I, _P]),
+    ("ssd_spec_cache_destroy", None, [_P]),
+    ("ssd_spec_cache_clear", _I, [_P, _P]),
+    ("ssd_spec_cache_insert", _I, [_P, _P, _P, _P, _P, _I, _P]),
+    ("ssd_spec_cache_lookup", _I, [_P, _P, _P, _P, _I, _P, _P, _P]),
+    ("ssd_spec_cache_insert_forks", _I, [_P, _P, _I, _I, _I, _P, _P]),
+    ("ssd_spec_cache_lookup_outcome", _I, [_P, _P, _P, _I, _I, _P, _P, _P]),
+    ("ssd_spec_cache_get_error", _I, [_P, _P, _P, _I]),
+    ("ssd_spec_cache_capacity", _I, [_P]),
+    ("ssd_spec_cache_depth", _I, [_P]),
+    ("ssd_selftest_exp2", _I, [_P, _P, _P, _I, _P]),
+    ("ssd_profile_begin", _I, [_I]),
+    ("ssd_profile_end", _I, [_P, _I, _P]),
+]
+
+
+class ProfileEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 40), ("launches", ctypes.c_int),
+                ("timed", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load the C-ABI library (raises if it is missing)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            "libssd_gb300.so is not built (%s); run __graft_entry__.build() or "
+            "python -m speculative_decoding_verification_70_gb300.build" % p)
+    lib = ctypes.CDLL(p)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class SSDError(RuntimeError):
+    def __init__(self, name: str, status: int):
+        lib = load_library()
+        msg = lib.ssd_status_string(status).decode()
+        super().__init__("%s failed: %s (%s)" % (name, STATUS.get(status, status), msg))
+        self.status = status
+
+
+def _check(name: str, status: int):
+    if status != 0:
+        raise SSDError(name, status)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (the library has no CPU path)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _opt(t: Optional[torch.Tensor], name: str):
+    return None if t is None else _dev(t, name)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSD_F32
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+def _want(t: torch.Tensor, dtype: torch.dtype, name: str):
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+# ---------------------------------------------------------------------------
+# workspace
+# ---------------------------------------------------------------------------
+def workspace_bytes(B: int, k: int, V: int, f: int = 0) -> int:
+    return int(load_library().ssd_workspace_bytes(B, k, V, f))
+
+
+def softmax_workspace_bytes(rows: int, V: int) -> int:
+    return int(load_library().ssd_softmax_workspace_bytes(rows, V))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled device workspace (torch memory, 256-byte aligned)."""
+    if nbytes <= 0:
+        raise ValueError("invalid workspace size")
+    return torch.zeros(int(nbytes) + 256, dtype=torch.uint8, device=device)
+
+
+def _ws_ptr(ws: torch.Tensor):
+    p = _dev(ws, "ws")
+    off = (-p) % 256
+    return p + off, ws.numel() - off
+
+
+def get_device_error(ws: torch.Tensor, clear: bool = False, stream=None) -> int:
+    p, _ = _ws_ptr(ws)
+    out = ctypes.c_int32(0)
+    _check("ssd_get_device_error",
+           load_library().ssd_get_device_error(p, _stream(stream), ctypes.byref(out), int(clear)))
+    return int(out.value)
+
+
+# ---------------------------------------------------------------------------
+# the five calls
+# ---------------------------------------------------------------------------
+def ssd_softmax_temp(logits: torch.Tensor, T: torch.Tensor, want_probs: bool = True, *,
+                     ws: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Temperature softmax per row of a [rows, V] tensor (T == 0: greedy)."""
+    lib = load_library()
+    rows, V = logits.shape
+    _want(T, torch.float32, "T")
+    dev = logits.device
+    if ws is None:
+        ws = new_workspace(softmax_workspace_bytes(rows, V), dev)
+    wp, wn = _ws_ptr(ws)
+    probs = torch.empty((rows, V), dtype=torch.float32, device=dev) if want_probs else None
+    m = torch.empty(rows, dtype=torch.float32, device=dev)
+    s = torch.empty(rows, dtype=torch.float32, device=dev)
+    a = torch.empty(rows, dtype=torch.int32, device=dev)
+    _check("ssd_softmax_temp", lib.ssd_softmax_temp(
+        _dev(logits, "logits"), _dtype_code(logits), rows, V, _dev(T, "T"),
+        _opt(probs, "probs"), _dev(m, "row_max"), _dev(s, "row_sum"), _dev(a, "row_argmax"),
+        wp, wn, _stream(stream)))
+    return {"probs": probs, "row_max": m, "row_sum": s, "row_argmax": a, "ws": ws}
+
+
+def _verify_outputs(B, k, dev, out, sample: bool, f: int = 0, P: int = 0):
+    out = {} if out is None else out
+    if "accept_len" not in out:
+        out["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        out["p_at_x"] = torch.empty((B, k), dtype=torch.float32, device=dev)
+        out["q_at_x"] = torch.empty((B, k), dtype=torch.float32, device=dev)
+        out["out_tok"] = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if f and "fork_tok" not in out:
+        out["fork_tok"] = torch.empty((B, P, f), dtype=torch.int32, device=dev)
+        out["fork_logit"] = torch.empty((B, P, f), dtype=torch.float32, device=dev)
+    return out
+
+
+def ssd_verify(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
+               u_acc: torch.Tensor, u_smp: Optional[torch.Tensor] = None, *,
+               ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+               stream=None) -> Dict[str, torch.Tensor]:
+    """Acceptance, first-reject prefix and (if u_smp is given) the recovery or
+    bonus draw.  Z [B,k+1,V], D [B,>=k,V] (same dtype), x [B,k] int32,
+    T [B], u_acc [B,k], u_smp [B] float32."""
+    lib = load_library()
+    B, kp1, V = Z.shape
+    k = kp1 - 1
+    if D.dim() != 3 or D.shape[0] != B or D.shape[2] != V or D.shape[1] < k:
+        raise ValueError("D must be [B, >=k, V]")
+    if Z.dtype != D.dtype:
+        raise TypeError("Z and D must share a dtype")
+    for t, n in ((x, "x"),):
+        _want(t, torch.int32, n)
+    for t, n in ((T, "T"), (u_acc, "u_acc")):
+        _want(t, torch.float32, n)
+    dev = Z.device
+    if ws is None:
+        ws = new_workspace(workspace_bytes(B, k, V, 0), dev)
+    wp, wn = _ws_ptr(ws)
+    o = _verify_outputs(B, k, dev, out, u_smp is not None)
+    _check("ssd_verify", lib.ssd_verify(
+        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), D.shape[1] * V, _dtype_code(Z), B, k, V,
+        _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
+        _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
+        _dev(o["out_tok"], "out_tok"), wp, wn, _stream(stream)))
+    o["ws"] = ws
+    return o
+
+
+def ssd_sample_residual(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
+                        accept_len: torch.Tensor, u_smp: torch.Tensor, ws: torch.Tensor, *,
+                        out_tok: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The recovery/bonus draw after an ssd_verify call (u_smp=None) that used
+    the same workspace."""
+    lib = load_library()
+    B, kp1, V = Z.shape
+    k = kp1 - 1
+    _want(accept_len, torch.int32, "accept_len")
+    if out_tok is None:
+        out_tok = torch.empty((B, k + 1), dtype=torch.int32, device=Z.device)
+    wp, wn = _ws_ptr(ws)
+    _check("ssd_sample_residual", lib.ssd_sample_residual(
+        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), D.shape[1] * V, _dtype_code(Z), B, k, V,
+        _dev(x, "x"), _dev(T, "T"), _dev(accept_len, "accept_len"), _dev(u_smp, "u_smp"),
+        _dev(out_tok, "out_tok"), wp, wn, _stream(stream)))
+    return out_tok
+
+
+def ssd_forked_recovery(L: torch.Tensor, f: int, mask: Optional[torch.Tensor] = None, *,
+                        ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                        stream=None) -> Dict[str, torch.Tensor]:
+    """Top-f forked recovery tokens per (b, j) of L [B,P,V], skipping the
+    tokens in mask [B,P,M] (int32, -1 = none)."""
+    lib = load_library()
+    B, P, V = L.shape
+    dev = L.device
+    M = 0 if mask is None else mask.shape[2]
+    if mask is not None:
+        _want(mask, torch.int32, "mask")
+    if ws is None:
+        ws = new_workspace(workspace_bytes(B, P - 1, V, f), dev)
+    wp, wn = _ws_ptr(ws)
+    out = {} if out is None else out
+    if "fork_tok" not in out:
+        out["fork_tok"] = torch.empty((B, P, f), dtype=torch.int32, device=dev)
+        out["fork_logit"] = torch.empty((B, P, f), dtype=torch.float32, device=dev)
+    _check("ssd_forked_recovery", lib.ssd_forked_recovery(
+        _dev(L, "L"), P * V, _dtype_code(L), B, P, V, f, _opt(mask, "mask"), M,
+        _dev(out["fork_tok"], "fork_tok"), _dev(out["fork_logit"], "fork_logit"), wp, wn,
+        _stream(stream)))
+    out["ws"] = ws
+    return out
+
+
+def ssd_verify_fork(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
+                    u_acc: torch.Tensor, u_smp: Optional[torch.Tensor], f: int,
+                    mask: Optional[torch.Tensor] = None, *, ws: Optional[torch.Tensor] = None,
+                    out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """ssd_verify plus the forked recovery over the SSD draft D [B,k+1,V] in
+    one pass over the logits."""
+    lib = load_library()
+    B, kp1, V = Z.shape
+    k = kp1 - 1
+    if tuple(D.shape) != (B, kp1, V):
+        raise ValueError("D must be [B, k+1, V] for the fused call")
+    if Z.dtype != D.dtype:
+        raise TypeError("Z and D must share a dtype")
+    _want(x, torch.int32, "x")
+    M = 0 if mask is None else mask.shape[2]
+    dev = Z.device
+    if ws is None:
+        ws = new_workspace(workspace_bytes(B, k, V, f), dev)
+    wp, wn = _ws_ptr(ws)
+    o = _verify_outputs(B, k, dev, out, u_smp is not None, f, kp1)
+    _check("ssd_verify_fork", lib.ssd_verify_fork(
+        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), kp1 * V, _dtype_code(Z), B, k, V,
+        _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
+        _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
+        _dev(o["out_tok"], "out_tok"), f, _opt(mask, "mask"), M,
+        _dev(o["fork_tok"], "fork_tok"), _dev(o["fork_logit"], "fork_logit"), wp, wn,
+        _stream(stream)))
+    o["ws"] = ws
+    return o
+
+
+class SpecCache:
+    """Device speculation cache: key (b, position, token) -> depth tokens."""
+
+    def __init__(self, capacity: int, depth: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check("ssd_spec_cache_create",
+               self._lib.ssd_spec_cache_create(capacity, depth, ctypes.byref(h)))
+        self._h = h
+        self.capacity = capacity
+        self.depth = depth
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            self._lib.ssd_spec_cache_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def clear(self, stream=None):
+        _check("ssd_spec_cache_clear", self._lib.ssd_spec_cache_clear(self._h, _stream(stream)))
+
+    def insert(self, b, pos, tok, payload, stream=None):
+        n = b.numel()
+        _check("ssd_spec_cache_insert", self._lib.ssd_spec_cache_insert(
+            self._h, _dev(b, "b"), _dev(pos, "pos"), _dev(tok, "tok"), _dev(payload, "payload"),
+            n, _stream(stream)))
+
+    def insert_forks(self, fork_tok, payload, stream=None):
+        B, P, f = fork_tok.shape
+        _check("ssd_spec_cache_insert_forks", self._lib.ssd_spec_cache_insert_forks(
+            self._h, _dev(fork_tok, "fork_tok"), B, P, f, _dev(payload, "payload"),
+            _stream(stream)))
+
+    def lookup(self, b, pos, tok, out=None, stream=None):
+        n = b.numel()
+        dev = b.device
+        out = out or {"hit": torch.empty(n, dtype=torch.int32, device=dev),
+                      "tok_out": torch.empty((n, self.depth), dtype=torch.int32, device=dev)}
+        _check("ssd_spec_cache_lookup", self._lib.ssd_spec_cache_lookup(
+            self._h, _dev(b, "b"), _dev(pos, "pos"), _dev(tok, "tok"), n,
+            _dev(out["hit"], "hit"), _dev(out["tok_out"], "tok_out"), _stream(stream)))
+        return out
+
+    def lookup_outcome(self, accept_len, out_tok, out=None, stream=None):
+        B, kp1 = out_tok.shape
+        dev = out_tok.device
+        out = out or {"hit": torch.empty(B, dtype=torch.int32, device=dev),
+                      "tok_out": torch.empty((B, self.depth), dtype=torch.int32, device=dev)}
+        _check("ssd_spec_cache_lookup_outcome", self._lib.ssd_spec_cache_lookup_outcome(
+            self._h, _dev(accept_len, "accept_len"), _dev(out_tok, "out_tok"), B, kp1 - 1,
+            _dev(out["hit"], "hit"), _dev(out["tok_out"], "tok_out"), _stream(stream)))
+        return out
+
+    def error(self, clear: bool = False, stream=None) -> int:
+        v = ctypes.c_int32(0)
+        _check("ssd_spec_cache_get_error", self._lib.ssd_spec_cache_get_error(
+            self._h, _stream(stream), ctypes.byref(v), int(clear)))
+        return int(v.value)
+
+
+def selftest_exp2(x_hi: torch.Tensor, x_lo: torch.Tensor, stream=None) -> torch.Tensor:
+    out = torch.empty(x_hi.numel(), dtype=torch.float64, device=x_hi.device)
+    _check("ssd_selftest_exp2", load_library().ssd_selftest_exp2(
+        _dev(x_hi, "x_hi"), _dev(x_lo, "x_lo"), _dev(out, "out"), x_hi.numel(), _stream(stream)))
+    return out
+
+
+def profile_begin(max_launches: int = 4096):
+    """Start bracketing every library kernel launch with CUDA events."""
+    _check("ssd_profile_begin", load_library().ssd_profile_begin(max_launches))
+
+
+def profile_end() -> Dict[str, dict]:
+    """Stop profiling; returns {kernel: {launches, timed, total_ms}}."""
+    arr = (ProfileEntry * 64)()
+    n = ctypes.c_int(0)
+    _check("ssd_profile_end", load_library().ssd_profile_end(arr, 64, ctypes.byref(n)))
+    return {arr[i].name.decode(): {"launches": arr[i].launches, "timed": arr[i].timed,
+                                   "total_ms": arr[i].total_ms} for i in range(n.value)}

@@ -1,0 +1,644 @@
+// ssd_api.cu -- the C-ABI entry points (include/ssd.h): host-side argument
+// checks, workspace layout and kernel launches.  No entry point allocates
+// memory except ssd_spec_cache_create.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/ssd.h"
+#include "ssd_layout.h"
+
+#ifndef SSD_TOPF_STAGED
+#define SSD_TOPF_STAGED 0
+#endif
+
+namespace ssd {
+cudaError_t launch_stats_rows(const StatsParams& p, int B, int dtype, bool vec, int r0, int rows,
+                              bool topf, cudaStream_t s);
+cudaError_t launch_stats_topf(const StatsParams& p, int B, int dtype, cudaStream_t s);
+cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
+cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
+cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
+cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_residual_mass(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s);
+cudaError_t launch_selftest_exp2(const float* xh, const float* xl, double* out, int n, cudaStream_t s);
+
+cudaError_t launch_cache_claim(const CacheView& c, const InsertArgs& a, cudaStream_t s);
+cudaError_t launch_cache_write(const CacheView& c, const InsertArgs& a, cudaStream_t s);
+cudaError_t launch_cache_lookup(const CacheView& c, const LookupArgs& a, cudaStream_t s);
+}  // namespace ssd
+
+using namespace ssd;
+
+struct ssd_spec_cache {
+  CacheView view;
+  unsigned long long calls;
+  int device;
+};
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// launch profiler
+// ---------------------------------------------------------------------------
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t a, b;
+};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  int cap = 0;
+  std::vector<cudaEvent_t> pool;
+  std::vector<ProfRecord> recs;
+  std::vector<const char*> names;
+  std::vector<int> counts;
+  int kernel_id(const char* n) {
+    for (size_t i = 0; i < names.size(); ++i)
+      if (strcmp(names[i], n) == 0) return static_cast<int>(i);
+    names.push_back(n);
+    counts.push_back(0);
+    return static_cast<int>(names.size() - 1);
+  }
+};
+Profiler g_prof;
+
+// Brackets one kernel launch when profiling is on.
+struct ProfScope {
+  cudaStream_t s;
+  int rec = -1;
+  ProfScope(const char* name, cudaStream_t st) : s(st) {
+    if (!g_prof.on) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    int id = g_prof.kernel_id(name);
+    g_prof.counts[id] += 1;
+    size_t used = g_prof.recs.size();
+    if (static_cast<int>(used) >= g_prof.cap) return;
+    ProfRecord r;
+    r.kernel = id;
+    r.a = g_prof.pool[2 * used];
+    r.b = g_prof.pool[2 * used + 1];
+    if (cudaEventRecord(r.a, s) != cudaSuccess) return;
+    g_prof.recs.push_back(r);
+    rec = static_cast<int>(used);
+  }
+  ~ProfScope() {
+    if (rec < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    cudaEventRecord(g_prof.recs[rec].b, s);
+  }
+};
+
+inline cudaStream_t S(ssd_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t esize(ssd_dtype dt) { return dt == SSD_BF16 ? 2 : 4; }
+
+inline bool dtype_ok(ssd_dtype dt) { return dt == SSD_F32 || dt == SSD_BF16; }
+
+// 16-byte vector loads are legal when every row start is 16-byte aligned.
+inline bool vec_ok(const void* base, int64_t bstride, int V, ssd_dtype dt) {
+  const size_t s = esize(dt);
+  return aligned(base, 16) && (static_cast<size_t>(bstride) * s) % 16 == 0 &&
+         (static_cast<size_t>(V) * s) % 16 == 0;
+}
+
+inline char* wsp(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+
+struct VerifyCall {
+  const void* Z; int64_t zb;
+  const void* D; int64_t db;
+  ssd_dtype dt;
+  int B, k, V;
+  const int32_t* x; const float* T; const float* u_acc;
+  int32_t* accept_len; float* p_at_x; float* q_at_x;
+  const float* u_smp; int32_t* out_tok;
+  int f; const int32_t* mask; int M; int32_t* fork_tok; float* fork_logit;
+  void* ws; size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+ssd_status check_common(const VerifyCall& c, bool fork) {
+  if (!dtype_ok(c.dt)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!c.Z || !c.D || !c.x || !c.T || !c.u_acc || !c.accept_len || !c.ws) return SSD_ERR_INVALID_ARG;
+  if (c.B < 1 || c.k < 1 || c.k > SSD_MAX_K || c.V < 2) return SSD_ERR_INVALID_ARG;
+  if ((c.p_at_x == nullptr) != (c.q_at_x == nullptr)) return SSD_ERR_INVALID_ARG;
+  if (c.u_smp && !c.out_tok) return SSD_ERR_INVALID_ARG;
+  const int64_t rowz = static_cast<int64_t>(c.k + 1) * c.V;
+  const int64_t rowd = static_cast<int64_t>(fork ? c.k + 1 : c.k) * c.V;
+  if (c.zb < rowz || c.db < rowd) return SSD_ERR_INVALID_ARG;
+  if (!aligned(c.Z, esize(c.dt)) || !aligned(c.D, esize(c.dt))) return SSD_ERR_INVALID_ARG;
+  if (fork) {
+    if (c.f < 1 || c.f > SSD_MAX_F || c.f >= c.V) return SSD_ERR_INVALID_ARG;
+    if (c.M < 0 || c.M > SSD_MAX_M || (c.M > 0 && !c.mask)) return SSD_ERR_INVALID_ARG;
+    if (!c.fork_tok || !c.fork_logit) return SSD_ERR_INVALID_ARG;
+  }
+  // the kernels index rows with int for element offsets within a row and
+  // int64 across rows; V must fit chunk arithmetic
+  if (c.V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  return SSD_OK;
+}
+
+// The streaming pass: rows without forked top-f in one kernel ("stats"),
+// the draft rows that feed the forked recovery in another ("stats_topf").
+cudaError_t run_stats(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s) {
+  StatsParams sp = sp0;
+  const bool topf = sp.Pdf > 0 && sp.f > 0;
+  // plain rows: up to 4 chunks (128 KB) per CTA while the grid still has
+  // at least ~16 CTAs per SM
+  const int rows_plain = topf ? sp.Pz : sp.R;
+  sp.G = 1;
+  while (sp.G < 4 && static_cast<long long>(B) * rows_plain * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
+    sp.G *= 2;
+  const int plain_rows = topf ? sp.Pz : sp.R;
+  cudaError_t e = cudaSuccess;
+  if (plain_rows > 0) {
+    ProfScope ps("stats", s);
+    e = launch_stats_rows(sp, B, dtype, vec, 0, plain_rows, false, s);
+  }
+  if (e != cudaSuccess || !topf) return e;
+  ProfScope ps("stats_topf", s);
+#if SSD_TOPF_STAGED
+  if (vec) {  // chunks staged into shared memory by bulk copies
+    StatsParams p = sp;
+    p.r0 = sp.Pz;
+    return launch_stats_topf(p, B, dtype, s);
+  }
+#endif
+  StatsParams pt = sp;
+  pt.G = 1;
+  while (pt.G < 4 && static_cast<long long>(B) * sp.Pdf * ((sp.C + 2 * pt.G - 1) / (2 * pt.G)) >= 2432)
+    pt.G *= 2;
+  return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s);
+}
+
+cudaError_t cache_insert(const CacheView& v, const InsertArgs& a, cudaStream_t s) {
+  cudaError_t e;
+  {
+    ProfScope ps("cache_claim", s);
+    e = launch_cache_claim(v, a, s);
+  }
+  if (e != cudaSuccess) return e;
+  ProfScope ps("cache_write", s);
+  return launch_cache_write(v, a, s);
+}
+
+cudaError_t run_residual(const ResidualParams& rp, int B, int dtype, bool vec, cudaStream_t s) {
+  cudaError_t e;
+  {
+    ProfScope ps("residual_norm", s);
+    e = launch_residual_norm(rp, B, dtype, vec, s);
+  }
+  if (e != cudaSuccess) return e;
+  {
+    ProfScope ps("residual_mass", s);
+    e = launch_residual_mass(rp, B, dtype, vec, s);
+  }
+  if (e != cudaSuccess) return e;
+  ProfScope ps("residual_select", s);
+  return launch_residual_select(rp, B, dtype, vec, s);
+}
+
+ssd_status run_verify(const VerifyCall& c, bool fork) {
+  ssd_status st = check_common(c, fork);
+  if (st != SSD_OK) return st;
+  const WsLayout L = make_layout(c.B, c.k, c.V, fork ? c.f : 0, static_cast<int>(esize(c.dt)));
+  if (c.ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  if (!aligned(c.ws, 256)) return SSD_ERR_INVALID_ARG;
+  const bool vec = vec_ok(c.Z, c.zb, c.V, c.dt) && vec_ok(c.D, c.db, c.V, c.dt);
+
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = c.Z; sp.zb = c.zb; sp.Pz = c.k + 1;
+  sp.D = c.D; sp.db = c.db; sp.Pds = c.k; sp.Pdf = fork ? c.k + 1 : 0;
+  sp.T = c.T;
+  sp.mask = c.mask; sp.M = fork ? c.M : 0; sp.f = fork ? c.f : 0;
+  sp.V = c.V; sp.C = L.ch.C; sp.CH = L.ch.CH;
+  sp.R = sp.Pz + (sp.Pdf > sp.Pds ? sp.Pdf : sp.Pds);
+  sp.Rp = L.R;
+  sp.part = reinterpret_cast<PartStat*>(wsp(c.ws, L.part));
+  sp.topk = reinterpret_cast<TopEntry*>(wsp(c.ws, L.topk));
+  sp.err = reinterpret_cast<int*>(wsp(c.ws, L.err));
+  cudaError_t e = run_stats(sp, c.B, c.dt == SSD_BF16 ? 1 : 0, vec, c.stream);
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+
+  FinalizeParams fp;
+  memset(&fp, 0, sizeof fp);
+  fp.Z = c.Z; fp.zb = c.zb; fp.Pz = sp.Pz;
+  fp.D = c.D; fp.db = c.db; fp.Pds = sp.Pds; fp.Pdf = sp.Pdf;
+  fp.dtype = c.dt == SSD_BF16 ? 1 : 0;
+  fp.B = c.B; fp.k = c.k; fp.V = c.V; fp.C = L.ch.C; fp.R = sp.R; fp.Rp = L.R; fp.f = sp.f;
+  fp.T = c.T; fp.x = c.x; fp.u_acc = c.u_acc;
+  fp.accept_len = c.accept_len; fp.p_at_x = c.p_at_x; fp.q_at_x = c.q_at_x;
+  fp.out_tok = c.out_tok;
+  fp.fork_tok = fork ? c.fork_tok : nullptr;
+  fp.fork_logit = fork ? c.fork_logit : nullptr;
+  fp.part = sp.part; fp.topk = sp.topk;
+  fp.rowstat = reinterpret_cast<RowStat*>(wsp(c.ws, L.rowstat));
+  fp.bstate = reinterpret_cast<BState*>(wsp(c.ws, L.bstate));
+  fp.err = reinterpret_cast<int*>(wsp(c.ws, L.err));
+  {
+    ProfScope ps("finalize", c.stream);
+    e = launch_finalize(fp, c.stream);
+  }
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+
+  if (c.u_smp) {
+    ResidualParams rp;
+    memset(&rp, 0, sizeof rp);
+    rp.Z = c.Z; rp.zb = c.zb; rp.Pz = sp.Pz;
+    rp.D = c.D; rp.db = c.db;
+    rp.V = c.V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = c.k;
+    rp.T = c.T; rp.u_smp = c.u_smp;
+    rp.rowstat = fp.rowstat; rp.bstate = fp.bstate;
+    rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm));
+    rp.rmass = reinterpret_cast<long long*>(wsp(c.ws, L.rmass));
+    rp.out_tok = c.out_tok;
+    e = run_residual(rp, c.B, fp.dtype, vec, c.stream);
+    if (e != cudaSuccess) return SSD_ERR_CUDA;
+  }
+  return SSD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ssd_status_string(ssd_status s) {
+  switch (s) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_CACHE_FULL: return "speculation cache full";
+    case SSD_ERR_TIMEOUT: return "timeout";
+    case SSD_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+int ssd_version(void) { return 100; }
+
+size_t ssd_workspace_bytes(int B, int k, int V, int f) {
+  if (B < 1 || k < 0 || k > SSD_MAX_K || V < 2 || f < 0 || f > SSD_MAX_F) return 0;
+  return make_layout(B, k, V, f).total;
+}
+
+size_t ssd_softmax_workspace_bytes(int rows, int V) {
+  if (rows < 1 || V < 1) return 0;
+  return make_softmax_layout(rows, V).total;
+}
+
+ssd_status ssd_workspace_init(void* ws, size_t bytes, ssd_stream_t stream) {
+  if (!ws) return SSD_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, bytes, S(stream)));
+}
+
+ssd_status ssd_get_device_error(void* ws, ssd_stream_t stream, int32_t* out, int clear) {
+  if (!ws || !out) return SSD_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, S(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  *out = v;
+  if (clear) {
+    e = cudaMemsetAsync(ws, 0, sizeof v, S(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+  }
+  return cuda_status(e);
+}
+
+ssd_status ssd_softmax_temp(const void* logits, ssd_dtype dtype, int rows, int V, const float* T,
+                            float* probs, float* row_max, float* row_sum, int32_t* row_argmax,
+                            void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!logits || !T || !row_max || !row_sum || !row_argmax || !ws) return SSD_ERR_INVALID_ARG;
+  if (rows < 1 || V < 1 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (!aligned(logits, esize(dtype)) || !aligned(ws, 256)) return SSD_ERR_INVALID_ARG;
+  const WsLayout L = make_softmax_layout(rows, V, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(logits, V, V, dtype);
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = logits; sp.zb = V; sp.Pz = 1;
+  sp.D = logits; sp.db = V;
+  sp.T = T;
+  sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = 1; sp.Rp = 1;
+  sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  cudaError_t e = run_stats(sp, rows, dtype == SSD_BF16 ? 1 : 0, vec, S(stream));
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  SoftmaxParams p;
+  memset(&p, 0, sizeof p);
+  p.L = logits; p.dtype = dtype == SSD_BF16 ? 1 : 0; p.rows = rows; p.V = V;
+  p.C = L.ch.C; p.CH = L.ch.CH; p.T = T; p.part = sp.part;
+  p.rowstat = reinterpret_cast<RowStat*>(wsp(ws, L.rowstat));
+  p.probs = probs; p.row_max = row_max; p.row_sum = row_sum; p.row_argmax = row_argmax;
+  p.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  {
+    ProfScope ps("softmax_finalize", S(stream));
+    e = launch_softmax_finalize(p, S(stream));
+  }
+  if (e == cudaSuccess && probs) {
+    ProfScope ps("softmax_probs", S(stream));
+    e = launch_softmax_probs(p, S(stream));
+  }
+  return cuda_status(e);
+}
+
+ssd_status ssd_verify(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                      ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
+                      const float* u_acc, int32_t* accept_len, float* p_at_x, float* q_at_x,
+                      const float* u_smp, int32_t* out_tok, void* ws, size_t ws_bytes,
+                      ssd_stream_t stream) {
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
+  c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
+  c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
+  c.u_smp = u_smp; c.out_tok = out_tok; c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
+  return run_verify(c, false);
+}
+
+ssd_status ssd_verify_fork(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                           ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
+                           const float* u_acc, int32_t* accept_len, float* p_at_x, float* q_at_x,
+                           const float* u_smp, int32_t* out_tok, int f, const int32_t* mask, int M,
+                           int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
+                           ssd_stream_t stream) {
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
+  c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
+  c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
+  c.u_smp = u_smp; c.out_tok = out_tok;
+  c.f = f; c.mask = mask; c.M = M; c.fork_tok = fork_tok; c.fork_logit = fork_logit;
+  c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
+  return run_verify(c, true);
+}
+
+ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                               ssd_dtype dtype, int B, int k, int V, const int32_t* x,
+                               const float* T, const int32_t* accept_len, const float* u_smp,
+                               int32_t* out_tok, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!Z || !D || !x || !T || !accept_len || !u_smp || !out_tok || !ws) return SSD_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (z_bstride < static_cast<int64_t>(k + 1) * V || d_bstride < static_cast<int64_t>(k) * V)
+    return SSD_ERR_INVALID_ARG;
+  if (!aligned(Z, esize(dtype)) || !aligned(D, esize(dtype)) || !aligned(ws, 256))
+    return SSD_ERR_INVALID_ARG;
+  // the row statistics of the verify call sit at f-independent offsets
+  const WsLayout L = make_layout(B, k, V, 0, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(Z, z_bstride, V, dtype) && vec_ok(D, d_bstride, V, dtype);
+  PrepParams pp;
+  pp.B = B; pp.k = k; pp.T = T; pp.x = x; pp.accept_len = accept_len;
+  pp.rowstat = reinterpret_cast<RowStat*>(wsp(ws, L.rowstat));
+  pp.R = L.R;
+  pp.bstate = reinterpret_cast<BState*>(wsp(ws, L.bstate));
+  pp.out_tok = out_tok;
+  cudaError_t e;
+  {
+    ProfScope ps("residual_prep", S(stream));
+    e = launch_residual_prep(pp, S(stream));
+  }
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  ResidualParams rp;
+  memset(&rp, 0, sizeof rp);
+  rp.Z = Z; rp.zb = z_bstride; rp.Pz = k + 1;
+  rp.D = D; rp.db = d_bstride;
+  rp.V = V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = k;
+  rp.T = T; rp.u_smp = u_smp;
+  rp.rowstat = pp.rowstat; rp.bstate = pp.bstate;
+  rp.rnorm = reinterpret_cast<long long*>(wsp(ws, L.rnorm));
+  rp.rmass = reinterpret_cast<long long*>(wsp(ws, L.rmass));
+  rp.out_tok = out_tok;
+  return cuda_status(run_residual(rp, B, dtype == SSD_BF16 ? 1 : 0, vec, S(stream)));
+}
+
+ssd_status ssd_forked_recovery(const void* L_, int64_t l_bstride, ssd_dtype dtype, int B, int P,
+                               int V, int f, const int32_t* mask, int M, int32_t* fork_tok,
+                               float* fork_logit, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!L_ || !fork_tok || !fork_logit || !ws) return SSD_ERR_INVALID_ARG;
+  if (B < 1 || P < 1 || P > SSD_MAX_K + 1 || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (f < 1 || f > SSD_MAX_F || f >= V) return SSD_ERR_INVALID_ARG;
+  if (M < 0 || M > SSD_MAX_M || (M > 0 && !mask)) return SSD_ERR_INVALID_ARG;
+  if (l_bstride < static_cast<int64_t>(P) * V) return SSD_ERR_INVALID_ARG;
+  if (!aligned(L_, esize(dtype)) || !aligned(ws, 256)) return SSD_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(B, P - 1, V, f, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(L_, l_bstride, V, dtype);
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = nullptr; sp.zb = 0; sp.Pz = 0;
+  sp.D = L_; sp.db = l_bstride; sp.Pds = 0; sp.Pdf = P;
+  sp.T = nullptr;
+  sp.mask = mask; sp.M = M; sp.f = f;
+  sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = P; sp.Rp = L.R;
+  sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  sp.topk = reinterpret_cast<TopEntry*>(wsp(ws, L.topk));
+  sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  cudaError_t e = run_stats(sp, B, dtype == SSD_BF16 ? 1 : 0, vec, S(stream));
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  FinalizeParams fp;
+  memset(&fp, 0, sizeof fp);
+  fp.Z = nullptr; fp.Pz = 0;
+  fp.D = L_; fp.db = l_bstride; fp.Pds = 0; fp.Pdf = P;
+  fp.dtype = dtype == SSD_BF16 ? 1 : 0;
+  fp.B = B; fp.k = 0; fp.V = V; fp.C = L.ch.C; fp.R = P; fp.Rp = L.R; fp.f = f;
+  fp.fork_tok = fork_tok; fp.fork_logit = fork_logit;
+  fp.part = sp.part; fp.topk = sp.topk;
+  fp.rowstat = reinterpret_cast<RowStat*>(wsp(ws, L.rowstat));
+  fp.bstate = reinterpret_cast<BState*>(wsp(ws, L.bstate));
+  fp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  ProfScope ps("finalize", S(stream));
+  return cuda_status(launch_finalize(fp, S(stream)));
+}
+
+// ---------------------------------------------------------------------------
+// Speculation cache
+// ---------------------------------------------------------------------------
+ssd_status ssd_spec_cache_create(int capacity, int depth, ssd_spec_cache** out) {
+  if (!out) return SSD_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (capacity < 2 || (capacity & (capacity - 1)) != 0 || capacity > (1 << 28) || depth < 1 ||
+      depth > 4096)
+    return SSD_ERR_INVALID_ARG;
+  ssd_spec_cache* c = new (std::nothrow) ssd_spec_cache;
+  if (!c) return SSD_ERR_INVALID_ARG;
+  memset(c, 0, sizeof *c);
+  c->view.capacity = capacity;
+  c->view.depth = depth;
+  cudaGetDevice(&c->device);
+  const size_t kb = sizeof(unsigned long long) * capacity;
+  const size_t pb = sizeof(int32_t) * static_cast<size_t>(capacity) * depth;
+  cudaError_t e = cudaMalloc(&c->view.keys, kb);
+  if (e == cudaSuccess) e = cudaMalloc(&c->view.winner, kb);
+  if (e == cudaSuccess) e = cudaMalloc(&c->view.payload, pb);
+  if (e == cudaSuccess) e = cudaMalloc(&c->view.err, 16);
+  if (e == cudaSuccess) e = cudaMemset(c->view.keys, 0xff, kb);
+  if (e == cudaSuccess) e = cudaMemset(c->view.winner, 0, kb);
+  if (e == cudaSuccess) e = cudaMemset(c->view.payload, 0xff, pb);
+  if (e == cudaSuccess) e = cudaMemset(c->view.err, 0, 16);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    ssd_spec_cache_destroy(c);
+    return SSD_ERR_CUDA;
+  }
+  *out = c;
+  return SSD_OK;
+}
+
+void ssd_spec_cache_destroy(ssd_spec_cache* c) {
+  if (!c) return;
+  if (c->view.keys) cudaFree(c->view.keys);
+  if (c->view.winner) cudaFree(c->view.winner);
+  if (c->view.payload) cudaFree(c->view.payload);
+  if (c->view.err) cudaFree(c->view.err);
+  delete c;
+}
+
+ssd_status ssd_spec_cache_clear(ssd_spec_cache* c, ssd_stream_t stream) {
+  if (!c) return SSD_ERR_INVALID_ARG;
+  const size_t kb = sizeof(unsigned long long) * c->view.capacity;
+  cudaError_t e = cudaMemsetAsync(c->view.keys, 0xff, kb, S(stream));
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->view.winner, 0, kb, S(stream));
+  return cuda_status(e);
+}
+
+ssd_status ssd_spec_cache_insert(ssd_spec_cache* c, const int32_t* b, const int32_t* pos,
+                                 const int32_t* tok, const int32_t* payload, int n,
+                                 ssd_stream_t stream) {
+  if (!c || n < 0) return SSD_ERR_INVALID_ARG;
+  if (n == 0) return SSD_OK;
+  if (!b || !pos || !tok || !payload) return SSD_ERR_INVALID_ARG;
+  if (c->calls >= 0xffffffffull) return SSD_ERR_INVALID_ARG;
+  InsertArgs a;
+  memset(&a, 0, sizeof a);
+  a.b = b; a.pos = pos; a.tok = tok; a.payload = payload; a.n = n;
+  a.seq = (++c->calls) << 32;
+  return cuda_status(cache_insert(c->view, a, S(stream)));
+}
+
+ssd_status ssd_spec_cache_insert_forks(ssd_spec_cache* c, const int32_t* fork_tok, int B, int P,
+                                       int f, const int32_t* payload, ssd_stream_t stream) {
+  if (!c || !fork_tok || !payload || B < 1 || P < 1 || P > 256 || f < 1) return SSD_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * P * f > 0x7fffffff) return SSD_ERR_INVALID_ARG;
+  if (c->calls >= 0xffffffffull) return SSD_ERR_INVALID_ARG;
+  InsertArgs a;
+  memset(&a, 0, sizeof a);
+  a.fork_tok = fork_tok; a.P = P; a.f = f; a.payload = payload; a.n = B * P * f;
+  a.seq = (++c->calls) << 32;
+  return cuda_status(cache_insert(c->view, a, S(stream)));
+}
+
+ssd_status ssd_spec_cache_lookup(const ssd_spec_cache* c, const int32_t* b, const int32_t* pos,
+                                 const int32_t* tok, int n, int32_t* hit, int32_t* tok_out,
+                                 ssd_stream_t stream) {
+  if (!c || n < 0) return SSD_ERR_INVALID_ARG;
+  if (n == 0) return SSD_OK;
+  if (!b || !pos || !tok || !hit || !tok_out) return SSD_ERR_INVALID_ARG;
+  LookupArgs a;
+  memset(&a, 0, sizeof a);
+  a.b = b; a.pos = pos; a.tok = tok; a.n = n; a.hit = hit; a.tok_out = tok_out;
+  ProfScope ps("cache_lookup", S(stream));
+  return cuda_status(launch_cache_lookup(c->view, a, S(stream)));
+}
+
+ssd_status ssd_spec_cache_lookup_outcome(const ssd_spec_cache* c, const int32_t* accept_len,
+                                         const int32_t* out_tok, int B, int k, int32_t* hit,
+                                         int32_t* tok_out, ssd_stream_t stream) {
+  if (!c || !accept_len || !out_tok || !hit || !tok_out || B < 1 || k < 1 || k > SSD_MAX_K)
+    return SSD_ERR_INVALID_ARG;
+  LookupArgs a;
+  memset(&a, 0, sizeof a);
+  a.accept_len = accept_len; a.out_tok = out_tok; a.k = k; a.n = B; a.hit = hit; a.tok_out = tok_out;
+  ProfScope ps("cache_lookup", S(stream));
+  return cuda_status(launch_cache_lookup(c->view, a, S(stream)));
+}
+
+ssd_status ssd_spec_cache_get_error(ssd_spec_cache* c, ssd_stream_t stream, int32_t* out,
+                                    int clear) {
+  if (!c || !out) return SSD_ERR_INVALID_ARG;
+  return ssd_get_device_error(c->view.err, stream, out, clear);
+}
+
+int ssd_spec_cache_capacity(const ssd_spec_cache* c) { return c ? c->view.capacity : 0; }
+int ssd_spec_cache_depth(const ssd_spec_cache* c) { return c ? c->view.depth : 0; }
+
+ssd_status ssd_selftest_exp2(const float* x_hi, const float* x_lo, double* out, int n,
+                             ssd_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x_hi || !x_lo || !out))) return SSD_ERR_INVALID_ARG;
+  if (n == 0) return SSD_OK;
+  return cuda_status(launch_selftest_exp2(x_hi, x_lo, out, n, S(stream)));
+}
+
+ssd_status ssd_profile_begin(int max_launches) {
+  if (max_launches < 0 || max_launches > (1 << 20)) return SSD_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (g_prof.on) return SSD_ERR_INVALID_ARG;
+  g_prof.recs.clear();
+  g_prof.names.clear();
+  g_prof.counts.clear();
+  g_prof.pool.assign(2 * static_cast<size_t>(max_launches), nullptr);
+  for (auto& ev : g_prof.pool) {
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+      for (auto& e2 : g_prof.pool)
+        if (e2) cudaEventDestroy(e2);
+      g_prof.pool.clear();
+      return SSD_ERR_CUDA;
+    }
+  }
+  g_prof.cap = max_launches;
+  g_prof.recs.reserve(max_launches);
+  g_prof.on = true;
+  return SSD_OK;
+}
+
+ssd_status ssd_profile_end(ssd_profile_entry* out, int cap, int* n_out) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.on) return SSD_ERR_INVALID_ARG;
+  g_prof.on = false;
+  ssd_status st = SSD_OK;
+  std::vector<double> ms(g_prof.names.size(), 0.0);
+  std::vector<int> timed(g_prof.names.size(), 0);
+  for (const ProfRecord& r : g_prof.recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) {
+      st = SSD_ERR_CUDA;
+      continue;
+    }
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+      st = SSD_ERR_CUDA;
+      continue;
+    }
+    ms[r.kernel] += t;
+    timed[r.kernel] += 1;
+  }
+  int n = 0;
+  for (size_t i = 0; i < g_prof.names.size() && out && n < cap; ++i, ++n) {
+    memset(&out[n], 0, sizeof out[n]);
+    strncpy(out[n].name, g_prof.names[i], sizeof out[n].name - 1);
+    out[n].launches = g_prof.counts[i];
+    out[n].timed = timed[i];
+    out[n].total_ms = ms[i];
+  }
+  if (n_out) *n_out = n;
+  for (auto& ev : g_prof.pool) cudaEventDestroy(ev);
+  g_prof.pool.clear();
+  g_prof.recs.clear();
+  return st;
+}
+
+}  // extern "C"

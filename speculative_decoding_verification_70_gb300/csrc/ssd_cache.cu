@@ -1,0 +1,144 @@
+// ssd_cache.cu -- the speculation cache on the device (kernel K-D).
+//
+// "SSD: drafting and verification on separate GPUs", "What changes in SSD":
+// the drafter speculates for the likely verification outcomes ahead of time
+// and a correct guess is returned at once; the roadmap names the speculation
+// cache.  "tanishqkumar/ssd" summary, module notes: forked recovery tokens are
+// chosen with masking to handle cache hits and misses.
+//
+// Table: open addressing over `capacity` (a power of two) slots, linear
+// probing bounded by the capacity, exact 64-bit key compare.  Key layout:
+// b << 40 | position << 32 | token.  Slot choice: the splitmix64 finaliser
+// (Steele, Lea & Flood 2014) of the key, masked to the capacity.  An empty
+// slot holds all-ones, which no valid key can equal (token < 2^31).
+//
+// Insert is two kernels so that duplicates resolve deterministically: claim
+// (CAS the key into a slot, then atomicMax a 64-bit sequence number
+// call << 32 | input index into the slot's winner word) and write (the input
+// whose sequence number won copies its payload).  The last duplicate, in
+// input order and across calls, wins.
+#include <stdint.h>
+
+#include "ssd_device.cuh"
+#include "ssd_layout.h"
+
+namespace ssd {
+
+constexpr unsigned long long kEmptyKey = 0xffffffffffffffffull;
+
+__device__ __forceinline__ unsigned long long splitmix64(unsigned long long z) {
+  z ^= z >> 30;
+  z *= 0xbf58476d1ce4e5b9ull;
+  z ^= z >> 27;
+  z *= 0x94d049bb133111ebull;
+  z ^= z >> 31;
+  return z;
+}
+
+__device__ __forceinline__ bool make_key(int b, int pos, int tok, unsigned long long& key) {
+  if (b < 0 || b >= (1 << 24) || pos < 0 || pos >= 256 || tok < 0) return false;
+  key = (static_cast<unsigned long long>(b) << 40) | (static_cast<unsigned long long>(pos) << 32) |
+        static_cast<unsigned long long>(static_cast<uint32_t>(tok));
+  return true;
+}
+
+// Slot holding `key`, or -1 (bounded probe).
+__device__ __forceinline__ int find_slot(const CacheView& c, unsigned long long key) {
+  const unsigned mask = static_cast<unsigned>(c.capacity - 1);
+  unsigned h = static_cast<unsigned>(splitmix64(key)) & mask;
+  for (int probe = 0; probe < c.capacity; ++probe) {
+    unsigned long long k = c.keys[h];
+    if (k == key) return static_cast<int>(h);
+    if (k == kEmptyKey) return -1;
+    h = (h + 1) & mask;
+  }
+  return -1;
+}
+
+__device__ __forceinline__ bool insert_key(const InsertArgs& a, int i, unsigned long long& key) {
+  int b, pos, tok;
+  if (a.b) {
+    b = a.b[i];
+    pos = a.pos[i];
+    tok = a.tok[i];
+  } else {
+    tok = a.fork_tok[i];
+    int bj = i / a.f;
+    b = bj / a.P;
+    pos = bj % a.P;
+  }
+  return make_key(b, pos, tok, key);
+}
+
+__global__ void cache_claim_kernel(CacheView c, InsertArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  unsigned long long key;
+  if (!insert_key(a, i, key)) return;
+  const unsigned mask = static_cast<unsigned>(c.capacity - 1);
+  unsigned h = static_cast<unsigned>(splitmix64(key)) & mask;
+  for (int probe = 0; probe < c.capacity; ++probe) {
+    unsigned long long prev = atomicCAS(&c.keys[h], kEmptyKey, key);
+    if (prev == kEmptyKey || prev == key) {
+      atomicMax(&c.winner[h], a.seq | static_cast<unsigned long long>(i));
+      return;
+    }
+    h = (h + 1) & mask;
+  }
+  atomicOr(c.err, 0x8);  // table full: the entry is dropped
+}
+
+__global__ void cache_write_kernel(CacheView c, InsertArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  unsigned long long key;
+  if (!insert_key(a, i, key)) return;
+  int s = find_slot(c, key);
+  if (s < 0) return;
+  if (c.winner[s] != (a.seq | static_cast<unsigned long long>(i))) return;
+  const int32_t* src = a.payload + static_cast<int64_t>(i) * c.depth;
+  int32_t* dst = c.payload + static_cast<int64_t>(s) * c.depth;
+  for (int d = 0; d < c.depth; ++d) dst[d] = src[d];
+}
+
+__global__ void cache_lookup_kernel(CacheView c, LookupArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  int b, pos, tok;
+  if (a.b) {
+    b = a.b[i];
+    pos = a.pos[i];
+    tok = a.tok[i];
+  } else {
+    b = i;
+    pos = a.accept_len[i];
+    tok = (pos >= 0 && pos <= a.k) ? a.out_tok[static_cast<int64_t>(i) * (a.k + 1) + pos] : -1;
+  }
+  unsigned long long key;
+  int s = -1;
+  if (make_key(b, pos, tok, key)) s = find_slot(c, key);
+  a.hit[i] = s >= 0 ? 1 : 0;
+  int32_t* dst = a.tok_out + static_cast<int64_t>(i) * c.depth;
+  const int32_t* src = c.payload + static_cast<int64_t>(s < 0 ? 0 : s) * c.depth;
+  for (int d = 0; d < c.depth; ++d) dst[d] = s >= 0 ? src[d] : -1;
+}
+
+cudaError_t launch_cache_claim(const CacheView& c, const InsertArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  cache_claim_kernel<<<(a.n + 255) / 256, 256, 0, s>>>(c, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_write(const CacheView& c, const InsertArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  cache_write_kernel<<<(a.n + 255) / 256, 256, 0, s>>>(c, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cache_lookup(const CacheView& c, const LookupArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return cudaSuccess;
+  cache_lookup_kernel<<<(a.n + 255) / 256, 256, 0, s>>>(c, a);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

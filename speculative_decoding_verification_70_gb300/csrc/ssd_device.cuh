@@ -1,0 +1,305 @@
+// ssd_device.cuh -- device helpers shared by the verify-and-recover kernels:
+// 16-byte streaming loads of fp32 / bf16 logit rows, the fast MUFU exp2 used
+// by the streaming statistics pass, an extended-precision exp2 and
+// double-float arithmetic used by the recovery draw, and deterministic
+// integer (fixed-point) block scans.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "exp2_table.inc"
+
+namespace ssd {
+
+constexpr int kThreads = 256;           // threads per CTA in every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Fixed-point scales of the recovery draw.  Probabilities (p - q, p) are at
+// most 1 each and sum to at most 1 (+ rounding): 2^60 units.  Unnormalised
+// exponentials 2^x, x <= 0, are at most 1 each and sum to at most V < 2^21:
+// 2^42 units.
+constexpr float kFixResidual = 1152921504606846976.0f;  // 2^60
+constexpr float kFixMass = 4398046511104.0f;            // 2^42
+constexpr double kInvFixMass = 1.0 / 4398046511104.0;
+
+// ---------------------------------------------------------------------------
+// Logit element types.  bf16 is the upper half of a binary32, so widening is
+// a 16-bit shift.
+// ---------------------------------------------------------------------------
+struct F32Tag {
+  using Elem = float;
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  using Raw = float4;
+  __device__ __forceinline__ static float load1(const Elem* p) { return __ldg(p); }
+  __device__ __forceinline__ static Raw loadraw(const Elem* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+  }
+  __device__ __forceinline__ static void unpackraw(const Raw& v, float (&o)[8]) {
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+  __device__ __forceinline__ static void loadv(const Elem* p, float (&o)[8]) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+  // cached (L1) variant for rows read more than once
+  __device__ __forceinline__ static void loadv_cached(const Elem* p, float (&o)[8]) {
+    float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+};
+
+struct BF16Tag {
+  using Elem = uint16_t;
+  static constexpr int kVec = 8;
+  using Raw = uint4;
+  __device__ __forceinline__ static Raw loadraw(const Elem* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+  }
+  __device__ __forceinline__ static void unpackraw(const Raw& v, float (&o)[8]) {
+    unpack(v.x, v.y, v.z, v.w, o);
+  }
+  __device__ __forceinline__ static float load1(const Elem* p) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+  }
+  __device__ __forceinline__ static void unpack(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                float (&o)[8]) {
+    o[0] = __uint_as_float(a << 16); o[1] = __uint_as_float(a & 0xffff0000u);
+    o[2] = __uint_as_float(b << 16); o[3] = __uint_as_float(b & 0xffff0000u);
+    o[4] = __uint_as_float(c << 16); o[5] = __uint_as_float(c & 0xffff0000u);
+    o[6] = __uint_as_float(d << 16); o[7] = __uint_as_float(d & 0xffff0000u);
+  }
+  __device__ __forceinline__ static void loadv(const Elem* p, float (&o)[8]) {
+    uint32_t a, b, c, d;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "l"(p));
+    unpack(a, b, c, d, o);
+  }
+  __device__ __forceinline__ static void loadv_cached(const Elem* p, float (&o)[8]) {
+    uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    unpack(v.x, v.y, v.z, v.w, o);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Fast exp2 (one MUFU op).  Used where an error of a few ulp is harmless: the
+// streaming row statistics, whose sums feed p(x)/q(x) for acceptance.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// Error-free transformations (Knuth's TwoSum, FMA-based TwoProduct).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Exact argument x = (z - m) * (c_hi + c_lo) as a float pair (xh, xl); the
+// product error is kept to ~2^-46 relative.
+__device__ __forceinline__ void arg_df(float z, float m, float c_hi, float c_lo, float& xh,
+                                       float& xl) {
+  float dh, dl;
+  two_sum(z, -m, dh, dl);
+  xh = __fmul_rn(dh, c_hi);
+  xl = __fmaf_rn(dh, c_hi, -xh);
+  xl = __fmaf_rn(dh, c_lo, xl);
+  xl = __fmaf_rn(dl, c_hi, xl);
+}
+
+// 2^(xh + xl) for xh <= 0 as a float pair (hi, lo), relative error ~1e-9.
+// Method: x = n + j/64 + g with n integer, j in [-32, 32], |g| <= 1/128;
+// 2^x = 2^n * 2^(j/64) * (1 + P(g)) with the table 2^(j/64) held as float
+// pairs and P the degree-4 Taylor polynomial of 2^g - 1 (truncation < 4e-14).
+// Results below 2^-125 (relative to the row maximum 1) return 0.
+// `tab` is a shared-memory copy of kExp2Tab.
+__device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, float& hi,
+                                        float& lo) {
+  if (!(xh > -125.0f)) {
+    hi = 0.f;
+    lo = 0.f;
+    return;
+  }
+  float n = rintf(xh);
+  float r = __fsub_rn(xh, n);                  // exact, |r| <= 1/2
+  float jf = rintf(__fmul_rn(r, 64.0f));       // j in [-32, 32]
+  float g = __fmaf_rn(jf, -0.015625f, r);      // exact, |g| <= 1/128
+  g = __fadd_rn(g, xl);
+  float P = __fmaf_rn(g, SSD_EXP2_C4, SSD_EXP2_C3);
+  P = __fmaf_rn(g, P, SSD_EXP2_C2);
+  P = __fmaf_rn(g, P, SSD_LN2_LO);
+  P = __fmul_rn(g, P);
+  P = __fmaf_rn(g, SSD_LN2_HI, P);             // 2^g - 1
+  float2 t = tab[static_cast<int>(jf) + 32];
+  float l = __fmaf_rn(t.x, P, __fmaf_rn(t.y, P, t.y));
+  float scale = __int_as_float((static_cast<int>(n) + 127) << 23);  // n in [-125, 0]
+  hi = __fmul_rn(t.x, scale);
+  lo = __fmul_rn(l, scale);
+}
+
+// Copy the exp2 table to shared memory (call before the first exp2_df; a
+// __syncthreads() must follow).
+__device__ __forceinline__ void load_exp2_table(float2* tab) {
+  for (int i = threadIdx.x; i < 65; i += blockDim.x) tab[i] = kExp2Tab[i];
+}
+
+// double-float helpers
+__device__ __forceinline__ void df_mul(float ah, float al, float bh, float bl, float& ph,
+                                       float& pl) {
+  ph = __fmul_rn(ah, bh);
+  pl = __fmaf_rn(ah, bh, -ph);
+  pl = __fmaf_rn(ah, bl, pl);
+  pl = __fmaf_rn(al, bh, pl);
+}
+
+// s = a - b renormalised (|sl| <= ulp(sh)/2)
+__device__ __forceinline__ void df_sub(float ah, float al, float bh, float bl, float& sh,
+                                       float& sl) {
+  float s, e;
+  two_sum(ah, -bh, s, e);
+  e = __fadd_rn(e, __fsub_rn(al, bl));
+  sh = __fadd_rn(s, e);
+  sl = __fsub_rn(e, __fsub_rn(sh, s));
+}
+
+// acc += v (double-float, renormalised)
+__device__ __forceinline__ void df_acc(float& ah, float& al, float vh, float vl) {
+  float s, e;
+  two_sum(ah, vh, s, e);
+  e = __fadd_rn(e, __fadd_rn(al, vl));
+  ah = __fadd_rn(s, e);
+  al = __fsub_rn(e, __fsub_rn(ah, s));
+}
+
+// double-float -> fixed point (round to nearest unit of 2^-scale_log2)
+__device__ __forceinline__ long long df_to_fix(float h, float l, float scale) {
+  return __float2ll_rn(__fmul_rn(h, scale)) + __float2ll_rn(__fmul_rn(l, scale));
+}
+
+// Split a positive double into a float pair.
+__device__ __forceinline__ void split_double(double v, float& h, float& l) {
+  h = __double2float_rn(v);
+  l = __double2float_rn(v - static_cast<double>(h));
+}
+
+// c = log2(e) / T as a float pair, clamped so that c stays finite.
+__device__ __forceinline__ void temp_coeff(float T, float& c_hi, float& c_lo) {
+  double c = SSD_LOG2E / static_cast<double>(T);
+  if (c > 1e37) c = 1e37;
+  split_double(c, c_hi, c_lo);
+}
+
+// The same coefficient computed by thread 0 only and broadcast through
+// shared memory: the double division runs once per CTA instead of once per
+// thread (the FP64 pipe is narrow).  Every thread must call this (it holds
+// a __syncthreads()).
+__device__ __forceinline__ float2 cta_temp_coeff(float T, float2* slot) {
+  if (threadIdx.x == 0) {
+    float h, l;
+    temp_coeff(T, h, l);
+    *slot = make_float2(h, l);
+  }
+  __syncthreads();
+  return *slot;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide inclusive scan of int64 (exact: integer addition is associative,
+// so the result does not depend on the order).  Returns the inclusive value;
+// *total receives the block total.  `sm` holds kWarps entries.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ long long block_scan_i64(long long v, long long* sm,
+                                                    long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) sm[warp] = v;
+  __syncthreads();
+  long long off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    long long s = sm[w];
+    if (w < warp) off += s;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return v + off;
+}
+
+__device__ __forceinline__ long long block_sum_i64(long long v, long long* sm) {
+  long long tot;
+  block_scan_i64(v, sm, &tot);
+  return tot;
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (TMA, non-tensor form) completing on an mbarrier.
+// Addresses are 16-byte aligned and sizes multiples of 16 bytes (callers
+// guarantee both).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* mbar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(mbar)), "r"(count)
+               : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(mbar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(mbar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier, giving up after `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* mbar, unsigned parity, int limit) {
+  for (int it = 0; it < limit; ++it)
+    if (mbar_try_wait(mbar, parity)) return true;
+  return false;
+}
+
+}  // namespace ssd

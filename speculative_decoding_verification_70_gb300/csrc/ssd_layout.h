@@ -1,0 +1,237 @@
+// ssd_layout.h -- workspace layout and kernel parameter blocks shared by the
+// host entry points and the kernels of the verify-and-recover library.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssd {
+
+constexpr int kMaxMask = 64;        // masked tokens per (b, position)
+constexpr int kMaxChunkBytes = 32768;  // a chunk fits one shared-memory stage
+
+// Partial statistics of one chunk of one logit row.
+struct PartStat {
+  float m;    // chunk maximum (NaN-free; -inf if the chunk is all -inf/NaN)
+  float s;    // sum over the chunk of 2^((z - m) * c), 0 for greedy rows
+  int idx;    // lowest index attaining m
+  int flags;  // bit 0: a NaN was seen
+};
+
+struct TopEntry {
+  float v;
+  int i;  // 0x7fffffff marks an empty slot
+};
+
+// Merged statistics of one logit row.
+struct RowStat {
+  double S;    // sum over the row of 2^((z - m) * c)
+  float m;
+  int argmax;
+  int flags;   // bit 0: NaN seen; bit 1: row invalid for its use
+  int pad;
+};
+
+enum ResidualMode : int { kModeNone = 0, kModeResidual = 1, kModeTarget = 2 };
+
+struct BState {
+  int n;      // accepted prefix length (or sentinel)
+  int mode;   // ResidualMode
+  int pad0, pad1;
+};
+
+struct Chunking {
+  int C;   // chunks per row
+  int CH;  // elements per chunk (multiple of 8), last chunk ragged
+  int E;   // elements per thread in the recovery kernels (multiple of 8)
+};
+
+// Workspace of the verify / fork / residual calls.
+struct WsLayout {
+  size_t err, part, topk, rowstat, bstate, rnorm, rmass, total;
+  int B, R, Pf, f;
+  Chunking ch;
+};
+
+struct StatsParams {
+  const void* Z;       // target logits (may be null when Pz == 0)
+  int64_t zb;          // batch stride (elements)
+  int Pz;              // target rows per batch row
+  const void* D;       // draft logits
+  int64_t db;
+  int Pds;             // draft rows needing softmax statistics
+  int Pdf;             // draft rows needing top-f
+  const float* T;      // [B] temperatures (null: no exponentials)
+  const int32_t* mask; // [B, Pdf, M]
+  int M, f;
+  int V, C, CH, R;     // R: rows per batch row
+  int Rp;              // row pitch of part[] (>= R)
+  int r0;              // first row of this launch
+  int G;               // chunks per CTA in the plain statistics kernel
+  PartStat* part;      // [B][Rp][C]
+  TopEntry* topk;      // [B][Pdf][C][f]
+  int* err;            // device error word
+};
+
+struct FinalizeParams {
+  const void* Z; int64_t zb; int Pz;
+  const void* D; int64_t db; int Pds; int Pdf;
+  int dtype;           // 0 f32, 1 bf16
+  int B, k, V, C, R, f;
+  int Rp;              // row pitch of part[] and rowstat[]
+  const float* T;
+  const int32_t* x;
+  const float* u_acc;
+  int32_t* accept_len;
+  float* p_at_x;
+  float* q_at_x;
+  int32_t* out_tok;    // may be null
+  int32_t* fork_tok;   // may be null
+  float* fork_logit;
+  const PartStat* part;
+  const TopEntry* topk;
+  RowStat* rowstat;    // [B][Rp]
+  BState* bstate;      // [B]
+  int* err;
+};
+
+struct ResidualParams {
+  const void* Z; int64_t zb; int Pz;
+  const void* D; int64_t db;
+  int V, C, CH, E, R, k;  // R: row pitch of rowstat[]
+  const float* T;
+  const float* u_smp;
+  const RowStat* rowstat;
+  const BState* bstate;
+  long long* rnorm;    // [B][C][2]
+  long long* rmass;    // [B][C]
+  int32_t* out_tok;    // [B][k+1]
+};
+
+struct SoftmaxParams {
+  const void* L;
+  int dtype, rows, V, C, CH;
+  const float* T;
+  const PartStat* part;
+  RowStat* rowstat;
+  float* probs;
+  float* row_max;
+  float* row_sum;
+  int32_t* row_argmax;
+  int* err;
+};
+
+struct PrepParams {
+  int B, k;
+  const float* T;
+  const int32_t* x;
+  const int32_t* accept_len;
+  const RowStat* rowstat;
+  int R;
+  BState* bstate;
+  int32_t* out_tok;
+};
+
+struct CacheView {
+  unsigned long long* keys;
+  unsigned long long* winner;
+  int32_t* payload;
+  int* err;
+  int capacity;
+  int depth;
+};
+
+struct InsertArgs {
+  const int32_t* b;
+  const int32_t* pos;
+  const int32_t* tok;
+  const int32_t* payload;
+  const int32_t* fork_tok;
+  int P, f;
+  int n;
+  unsigned long long seq;
+};
+
+struct LookupArgs {
+  const int32_t* b;
+  const int32_t* pos;
+  const int32_t* tok;
+  const int32_t* accept_len;
+  const int32_t* out_tok;
+  int k;
+  int n;
+  int32_t* hit;
+  int32_t* tok_out;
+};
+
+// Chunking policy: chunks of at most 32 KB (so that one chunk fits a
+// shared-memory stage); for small batches more chunks so the grid fills the
+// GPU (at least ~16 CTAs per SM on 152 SMs), but no chunk below 2048
+// elements.  esize is the logit element size; sizing with esize = 4 gives
+// the most chunks, which is what the workspace is sized for.
+inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
+  Chunking c;
+  long long rows = static_cast<long long>(B) * (rows_per_b > 0 ? rows_per_b : 1);
+  const long long max_ch = kMaxChunkBytes / esize;
+  long long c0 = (V + max_ch - 1) / max_ch;
+  long long want = (2432 + rows - 1) / rows;
+  long long cap = (V + 2047) / 2048;
+  long long C = want < cap ? want : cap;
+  if (C < c0) C = c0;
+  if (C > 256) C = 256;
+  if (C < 1) C = 1;
+  long long CH = (V + C - 1) / C;
+  CH = (CH + 7) / 8 * 8;
+  C = (V + CH - 1) / CH;
+  c.C = static_cast<int>(C);
+  c.CH = static_cast<int>(CH);
+  long long E = (CH + 255) / 256;
+  E = (E + 7) / 8 * 8;
+  c.E = static_cast<int>(E);
+  return c;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
+  WsLayout L;
+  L.B = B;
+  L.R = 2 * (k + 1);
+  L.Pf = k + 1;
+  L.f = f;
+  L.ch = make_chunking(B, L.R, V, esize);
+  const size_t C = static_cast<size_t>(L.ch.C);
+  size_t off = 0;
+  L.err = off;                      off = align256(off + 16);
+  // every region but the forked top-f lists is independent of f, so a
+  // workspace sized for (B, k, V, f) serves the f = 0 calls too
+  L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
+  L.rowstat = off;                  off = align256(off + sizeof(RowStat) * B * L.R);
+  L.bstate = off;                   off = align256(off + sizeof(BState) * B);
+  L.rnorm = off;                    off = align256(off + sizeof(long long) * 2 * B * C);
+  L.rmass = off;                    off = align256(off + sizeof(long long) * B * C);
+  L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
+  L.total = off;
+  return L;
+}
+
+// Workspace of ssd_softmax_temp: rows are "batch rows" with one target row.
+inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
+  WsLayout L;
+  L.B = rows;
+  L.R = 1;
+  L.Pf = 0;
+  L.f = 0;
+  L.ch = make_chunking(rows, 1, V, esize);
+  const size_t C = static_cast<size_t>(L.ch.C);
+  size_t off = 0;
+  L.err = off;                      off = align256(off + 16);
+  L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
+  L.topk = off;
+  L.rowstat = off;                  off = align256(off + sizeof(RowStat) * rows);
+  L.bstate = off; L.rnorm = off; L.rmass = off;
+  L.total = off;
+  return L;
+}
+
+}  // namespace ssd

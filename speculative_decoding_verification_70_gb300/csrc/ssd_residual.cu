@@ -1,0 +1,408 @@
+// ssd_residual.cu -- the recovery / bonus draw (kernel K-B).
+//
+// Rule (speculative-sampling summary, "How It Works": regenerate from the
+// point of divergence; Leviathan et al. / Chen et al.): after the first
+// rejection at position n < k draw from w = max(0, p_n - q_n) (if w is all
+// zero, from p_n); after k accepts draw the bonus token from p_k.  The draw
+// is the inverse CDF: the smallest j with C_j > u * C_{V-1}.
+//
+// The draw decides an integer from sums over ~10^5 tiny weights, so fp32
+// would move CDF boundaries across the dense tail of the distribution and
+// change ~1e-3 of the draws.  Here every weight is evaluated in double-float
+// (exp2_df, ~1e-9 relative), each thread sums a contiguous index range in
+// double-float, and everything above a thread is exact 64-bit fixed point,
+// so every level of the three-level select (chunk, thread, element) sees the
+// same totals.
+//
+// Kernels (one CTA per chunk of row n, then one CTA per batch row):
+//   residual_norm   S_z = sum 2^((z - m_z) c) and S_d over row n of Z and D
+//   residual_mass   W_c = sum over chunk c of max(0, p - q)
+//   residual_select chunk -> thread -> element select, writes out_tok[b, n]
+#include <math.h>
+
+#include "ssd_device.cuh"
+#include "ssd_layout.h"
+
+namespace ssd {
+
+struct RowCtx {
+  float mz, md;        // row maxima
+  float c_hi, c_lo;    // log2(e)/T
+  float iz_hi, iz_lo;  // 1/S_z
+  float id_hi, id_lo;  // 1/S_d
+};
+
+// Weight of element i in the given quantity:
+//   Q_NORM_Z : 2^((z - m_z) c)         (unnormalised, for S_z and the p_k draw)
+//   Q_NORM_D : 2^((d - m_d) c)
+//   Q_RESID  : max(0, p - q)
+enum Quantity { Q_NORM_Z = 0, Q_NORM_D = 1, Q_RESID = 2 };
+
+template <int Q>
+__device__ __forceinline__ void weight(float z, float d, const RowCtx& cx, const float2* tab,
+                                       float& h, float& l) {
+  float xh, xl;
+  if (Q == Q_NORM_Z) {
+    arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, h, l);
+  } else if (Q == Q_NORM_D) {
+    arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, h, l);
+  } else {
+    float ah, al, bh, bl, ph, pl, qh, ql;
+    arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, ah, al);
+    arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, bh, bl);
+    df_mul(ah, al, cx.iz_hi, cx.iz_lo, ph, pl);
+    df_mul(bh, bl, cx.id_hi, cx.id_lo, qh, ql);
+    df_sub(ph, pl, qh, ql, h, l);
+    if (!(h > 0.f)) {
+      h = 0.f;
+      l = 0.f;
+    }
+  }
+}
+
+// Double-float sum of the weights over [lo, hi) in index order.  Z and D
+// rows start 16-byte aligned when VEC.
+template <typename Tag, bool VEC, int Q>
+__device__ __forceinline__ void range_sum(const typename Tag::Elem* zr,
+                                          const typename Tag::Elem* dr, int lo, int hi,
+                                          const RowCtx& cx, const float2* tab, float& sh,
+                                          float& sl) {
+  sh = 0.f;
+  sl = 0.f;
+  constexpr int kV = Tag::kVec;
+  int i = lo;
+  if (VEC) {
+    for (; i + kV <= hi; i += kV) {
+      float z[8], d[8];
+      if (Q != Q_NORM_D) Tag::loadv_cached(zr + i, z);
+      if (Q != Q_NORM_Z) Tag::loadv_cached(dr + i, d);
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        float h, l;
+        weight<Q>(z[e], d[e], cx, tab, h, l);
+        df_acc(sh, sl, h, l);
+      }
+    }
+  }
+  for (; i < hi; ++i) {
+    float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
+    float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
+    float h, l;
+    weight<Q>(z, d, cx, tab, h, l);
+    df_acc(sh, sl, h, l);
+  }
+}
+
+__device__ __forceinline__ void norm_inverses(const ResidualParams& p, int b, RowCtx& cx) {
+  long long sz = 0, sd = 0;
+  for (int q = 0; q < p.C; ++q) {
+    sz += p.rnorm[(static_cast<int64_t>(b) * p.C + q) * 2 + 0];
+    sd += p.rnorm[(static_cast<int64_t>(b) * p.C + q) * 2 + 1];
+  }
+  double Sz = static_cast<double>(sz) * kInvFixMass;
+  double Sd = static_cast<double>(sd) * kInvFixMass;
+  split_double(1.0 / Sz, cx.iz_hi, cx.iz_lo);
+  split_double(1.0 / Sd, cx.id_hi, cx.id_lo);
+}
+
+// Row context of batch row b, computed by thread 0 (its double divisions run
+// once per CTA) and shared through s_cx.  Returns false (uniformly) when the
+// row draws nothing.  Holds a __syncthreads() when it returns true.
+__device__ __forceinline__ bool load_ctx(const ResidualParams& p, int b, BState& bs, RowCtx& cx,
+                                         RowCtx* s_cx, bool with_inverses) {
+  bs = p.bstate[b];
+  if (bs.mode == kModeNone) return false;
+  if (threadIdx.x == 0) {
+    RowCtx c;
+    const RowStat rz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n];
+    c.mz = rz.m;
+    c.md = 0.f;
+    if (bs.mode == kModeResidual) c.md = p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m;
+    temp_coeff(p.T[b], c.c_hi, c.c_lo);
+    c.iz_hi = c.iz_lo = c.id_hi = c.id_lo = 0.f;
+    if (with_inverses) norm_inverses(p, b, c);
+    *s_cx = c;
+  }
+  __syncthreads();
+  cx = *s_cx;
+  return true;
+}
+
+template <typename Tag>
+__device__ __forceinline__ void row_ptrs(const ResidualParams& p, int b, int n,
+                                         const typename Tag::Elem*& zr,
+                                         const typename Tag::Elem*& dr) {
+  zr = static_cast<const typename Tag::Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb +
+       static_cast<int64_t>(n) * p.V;
+  dr = static_cast<const typename Tag::Elem*>(p.D) + static_cast<int64_t>(b) * p.db +
+       static_cast<int64_t>(n) * p.V;
+}
+
+// grid (C, B)
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams p) {
+  __shared__ float2 tab[65];
+  __shared__ long long sm[kWarps];
+  __shared__ RowCtx s_cx;
+  const int c = blockIdx.x, b = blockIdx.y;
+  BState bs;
+  RowCtx cx;
+  load_exp2_table(tab);
+  if (!load_ctx(p, b, bs, cx, &s_cx, false)) return;
+  const typename Tag::Elem *zr, *dr;
+  row_ptrs<Tag>(p, b, bs.n, zr, dr);
+  const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
+  const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
+  const int hi = min(chi, lo + p.E);
+  float h, l;
+  range_sum<Tag, VEC, Q_NORM_Z>(zr, dr, lo, hi, cx, tab, h, l);
+  long long fz = df_to_fix(h, l, kFixMass);
+  long long fd = 0;
+  if (bs.mode == kModeResidual) {
+    range_sum<Tag, VEC, Q_NORM_D>(zr, dr, lo, hi, cx, tab, h, l);
+    fd = df_to_fix(h, l, kFixMass);
+  }
+  long long tz = block_sum_i64(fz, sm);
+  long long td = block_sum_i64(fd, sm);
+  if (threadIdx.x == 0) {
+    p.rnorm[(static_cast<int64_t>(b) * p.C + c) * 2 + 0] = tz;
+    p.rnorm[(static_cast<int64_t>(b) * p.C + c) * 2 + 1] = td;
+  }
+}
+
+// grid (C, B)
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams p) {
+  __shared__ float2 tab[65];
+  __shared__ long long sm[kWarps];
+  __shared__ RowCtx s_cx;
+  const int c = blockIdx.x, b = blockIdx.y;
+  if (p.bstate[b].mode != kModeResidual) return;
+  BState bs;
+  RowCtx cx;
+  load_exp2_table(tab);
+  load_ctx(p, b, bs, cx, &s_cx, true);
+  const typename Tag::Elem *zr, *dr;
+  row_ptrs<Tag>(p, b, bs.n, zr, dr);
+  const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
+  const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
+  const int hi = min(chi, lo + p.E);
+  float h, l;
+  range_sum<Tag, VEC, Q_RESID>(zr, dr, lo, hi, cx, tab, h, l);
+  long long fw = df_to_fix(h, l, kFixResidual);
+  long long tw = block_sum_i64(fw, sm);
+  if (threadIdx.x == 0) p.rmass[static_cast<int64_t>(b) * p.C + c] = tw;
+}
+
+// floor(total * u) exactly, u a binary32 in [0, 1).
+__device__ __forceinline__ unsigned long long scale_by_uniform(unsigned long long total, float u) {
+  if (!(u > 0.f)) return 0ull;
+  uint32_t bits = __float_as_uint(u);
+  uint32_t ex = (bits >> 23) & 0xffu;
+  uint64_t mant = bits & 0x7fffffu;
+  if (ex != 0) mant |= 0x800000u;
+  else ex = 1;
+  // u = mant * 2^(ex - 150), shift = 150 - ex >= 24 since u < 1
+  int shift = 150 - static_cast<int>(ex);
+  unsigned long long lo = total * mant;
+  unsigned long long hi = __umul64hi(total, mant);
+  if (shift >= 128) return 0ull;
+  if (shift >= 64) return hi >> (shift - 64);
+  return (lo >> shift) | (shift ? (hi << (64 - shift)) : 0ull);
+}
+
+template <typename Tag, bool VEC, int Q>
+__device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag::Elem* dr,
+                               int clo, int chi, int E, const RowCtx& cx, const float2* tab,
+                               float scale, long long target, long long* sm, int* s_pick) {
+  const int tid = threadIdx.x;
+  const int lo = min(chi, clo + tid * E);
+  const int hi = min(chi, lo + E);
+  float h, l;
+  range_sum<Tag, VEC, Q>(zr, dr, lo, hi, cx, tab, h, l);
+  long long own = df_to_fix(h, l, scale);
+  long long tot;
+  long long incl = block_scan_i64(own, sm, &tot);
+  if (tid == 0) *s_pick = kThreads;
+  __syncthreads();
+  if (incl > target && incl - own <= target) atomicMin(s_pick, tid);
+  __syncthreads();
+  const int pick = *s_pick;
+  int tok = -1;
+  if (pick == kThreads) {  // cannot happen: the chunk total exceeds target by construction
+    __syncthreads();
+    return chi - 1;
+  }
+  if (tid == pick) {
+    // walk the thread's range with the same double-float accumulation
+    const long long base = incl - own;
+    float ah = 0.f, al = 0.f;
+    int last_pos = -1;
+    for (int i = lo; i < hi; ++i) {
+      float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
+      float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
+      float wh, wl;
+      weight<Q>(z, d, cx, tab, wh, wl);
+      if (wh > 0.f) last_pos = i;
+      df_acc(ah, al, wh, wl);
+      if (base + df_to_fix(ah, al, scale) > target) {
+        tok = i;
+        break;
+      }
+    }
+    if (tok < 0) tok = last_pos >= 0 ? last_pos : hi - 1;  // rounding guard
+    *s_pick = -1 - tok;
+  }
+  __syncthreads();
+  return -1 - *s_pick;
+}
+
+// grid B
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParams p) {
+  __shared__ float2 tab[65];
+  __shared__ long long sm[kWarps];
+  __shared__ int s_pick;
+  __shared__ int s_chunk;
+  __shared__ long long s_target;
+  __shared__ RowCtx s_cx;
+  const int b = blockIdx.x;
+  BState bs;
+  RowCtx cx;
+  load_exp2_table(tab);
+  if (!load_ctx(p, b, bs, cx, &s_cx, p.bstate[b].mode == kModeResidual)) return;
+  int mode = bs.mode;
+  if (threadIdx.x == 0) {
+    // chunk masses: residual (2^60 units) or, for the bonus draw and the
+    // all-zero-residual fallback, unnormalised target weights (2^42 units)
+    long long W = 0;
+    if (mode == kModeResidual) {
+      for (int q = 0; q < p.C; ++q) W += p.rmass[static_cast<int64_t>(b) * p.C + q];
+      if (W == 0) mode = kModeTarget;
+    }
+    const long long* mass;
+    int stride;
+    if (mode == kModeResidual) {
+      mass = p.rmass + static_cast<int64_t>(b) * p.C;
+      stride = 1;
+    } else {
+      mass = p.rnorm + static_cast<int64_t>(b) * p.C * 2;
+      stride = 2;
+      W = 0;
+      for (int q = 0; q < p.C; ++q) W += mass[q * stride];
+    }
+    unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
+    long long cum = 0;
+    int pick = p.C - 1;
+    long long before = 0;
+    for (int q = 0; q < p.C; ++q) {
+      long long nx = cum + mass[q * stride];
+      if (nx > static_cast<long long>(t)) {
+        pick = q;
+        before = cum;
+        break;
+      }
+      cum = nx;
+      before = cum;
+    }
+    s_chunk = pick | (mode == kModeResidual ? 0 : 0x40000000);
+    s_target = static_cast<long long>(t) - before;
+  }
+  __syncthreads();
+  const int q = s_chunk & 0xffff;
+  const bool resid = (s_chunk & 0x40000000) == 0;
+  const long long target = s_target;
+  const typename Tag::Elem *zr, *dr;
+  row_ptrs<Tag>(p, b, bs.n, zr, dr);
+  const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
+  int tok;
+  if (resid)
+    tok = select_in_chunk<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual, target, sm, &s_pick);
+  else
+    tok = select_in_chunk<Tag, VEC, Q_NORM_Z>(zr, dr, clo, chi, p.E, cx, tab, kFixMass, target, sm, &s_pick);
+  if (threadIdx.x == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
+}
+
+// Prepare the per-row draw state from a caller-supplied accept_len (used by
+// the stand-alone residual call).  grid ceil(B / kThreads).
+
+__global__ void residual_prep_kernel(PrepParams p) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  const int n = p.accept_len[b];
+  const float T = p.T[b];
+  const bool greedy = !(T > 0.f);
+  BState bs;
+  bs.n = n;
+  bs.mode = (n < 0 || n > p.k || greedy || isnan(T)) ? kModeNone
+                                                       : (n < p.k ? kModeResidual : kModeTarget);
+  bs.pad0 = bs.pad1 = 0;
+  p.bstate[b] = bs;
+  int32_t* o = p.out_tok + static_cast<int64_t>(b) * (p.k + 1);
+  for (int j = 0; j <= p.k; ++j) {
+    int v = -1;
+    if (n >= 0 && n <= p.k) {
+      if (j < n) v = p.x[static_cast<int64_t>(b) * p.k + j];
+      else if (j == n && greedy && !isnan(T)) v = p.rowstat[static_cast<int64_t>(b) * p.R + n].argmax;
+    }
+    o[j] = v;
+  }
+}
+
+#define SSD_DISPATCH(KERNEL, GRID)                                                  \
+  do {                                                                              \
+    if (dtype == 1) {                                                               \
+      if (vec) KERNEL<BF16Tag, true><<<GRID, kThreads, 0, s>>>(p);                  \
+      else KERNEL<BF16Tag, false><<<GRID, kThreads, 0, s>>>(p);                     \
+    } else {                                                                        \
+      if (vec) KERNEL<F32Tag, true><<<GRID, kThreads, 0, s>>>(p);                   \
+      else KERNEL<F32Tag, false><<<GRID, kThreads, 0, s>>>(p);                      \
+    }                                                                               \
+  } while (0)
+
+cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
+  SSD_DISPATCH(residual_norm_kernel, dim3(p.C, B));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_mass(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
+  SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
+  SSD_DISPATCH(residual_select_kernel, dim3(B));
+  return cudaGetLastError();
+}
+#undef SSD_DISPATCH
+
+cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s) {
+  residual_prep_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Self-test of exp2_df: out[i] = 2^(x_hi + x_lo).
+__global__ void selftest_exp2_kernel(const float* xh, const float* xl, double* out, int n) {
+  __shared__ float2 tab[65];
+  load_exp2_table(tab);
+  __syncthreads();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    float h, l;
+    exp2_df(xh[i], xl[i], tab, h, l);
+    out[i] = static_cast<double>(h) + static_cast<double>(l);
+  }
+}
+
+cudaError_t launch_selftest_exp2(const float* xh, const float* xl, double* out, int n, cudaStream_t s) {
+  int blocks = (n + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  if (blocks < 1) blocks = 1;
+  selftest_exp2_kernel<<<blocks, 256, 0, s>>>(xh, xl, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -1,0 +1,180 @@
+// ssd_scan.cuh -- per-thread streaming statistics (running max, lowest
+// argmax, online exponential sum) and small warp helpers shared by the row
+// statistics kernels.
+#pragma once
+
+#include <math.h>
+
+#include "ssd_device.cuh"
+#include "ssd_layout.h"
+
+namespace ssd {
+
+constexpr int kIdxNone = 0x7fffffff;
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// (v1, i1) ranks before (v2, i2): larger value, then lower index.
+__device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// Order-preserving map of binary32 to uint32 (for atomicMax on floats).
+__device__ __forceinline__ unsigned f2ord(float x) {
+  unsigned b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord2f(unsigned o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
+// Per-thread running statistics of the streaming pass.
+struct ScanState {
+  float m;    // running maximum
+  float s;    // running sum of 2^((z - m) c)
+  int idx;    // lowest index attaining m
+  int nan;    // a NaN was seen
+  float m2;   // second largest value -- kept only for top-f rows
+};
+
+__device__ __forceinline__ void scan_init(ScanState& st) {
+  st.m = -INFINITY;
+  st.s = 0.f;
+  st.idx = kIdxNone;
+  st.nan = 0;
+  st.m2 = -INFINITY;
+}
+
+// Max / argmax / NaN / (optionally) the online exponential sum over one
+// vector of n logits starting at index base_idx.  vm is the vector maximum
+// with NaN propagation (NaN iff the vector holds a NaN).
+// Second largest of the first n values of z (n = 1, 4 or 8), branch-free.
+__device__ __forceinline__ float second_max(const float (&z)[8], int n) {
+  if (n == 1) return -INFINITY;
+  const float h01 = fmaxf(z[0], z[1]), l01 = fminf(z[0], z[1]);
+  const float h23 = fmaxf(z[2], z[3]), l23 = fminf(z[2], z[3]);
+  const float m4 = fmaxf(h01, h23);
+  const float s4 = fmaxf(fminf(h01, h23), fmaxf(l01, l23));
+  if (n == 4) return s4;
+  const float h45 = fmaxf(z[4], z[5]), l45 = fminf(z[4], z[5]);
+  const float h67 = fmaxf(z[6], z[7]), l67 = fminf(z[6], z[7]);
+  const float n4 = fmaxf(h45, h67);
+  const float t4 = fmaxf(fminf(h45, h67), fmaxf(l45, l67));
+  return fmaxf(fminf(m4, n4), fmaxf(s4, t4));
+}
+
+// With SECOND the thread also keeps m2, the second largest value among its
+// elements (m2 <- max(m2, min(vector max, old max), second max of the
+// vector), exact for values, no branch).
+template <bool DO_EXP, bool SECOND = false>
+__device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], int n,
+                                            float vm, int base_idx, float c) {
+  if (vm != vm) {  // a NaN in the vector: the row is invalid
+    st.nan = 1;
+    return;
+  }
+  if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(fminf(vm, st.m), second_max(z, n)));
+  if (vm > st.m || st.idx == kIdxNone) {
+    int e_star = n - 1;
+#pragma unroll
+    for (int e = 7; e >= 0; --e)
+      if (e < n && z[e] == vm) e_star = e;
+    if (DO_EXP) {
+      // rescale the running sum to the new maximum
+      float f = (st.m == vm) ? 1.f : ex2_fast((st.m - vm) * c);
+      st.s = st.s * f;
+    }
+    st.m = vm;
+    st.idx = base_idx + e_star;
+  }
+  if (DO_EXP) {
+    float base = (st.m == -INFINITY) ? 0.f : st.m;
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < n) st.s += ex2_fast((z[e] - base) * c);
+  }
+}
+
+__device__ __forceinline__ void merge_stat(float& m, float& s, int& idx, float m2, float s2,
+                                           int i2, float c, bool do_exp) {
+  float mm = fmaxf(m, m2);
+  if (do_exp) {
+    float f1 = (m == mm) ? 1.f : ex2_fast((m - mm) * c);
+    float f2 = (m2 == mm) ? 1.f : ex2_fast((m2 - mm) * c);
+    s = s * f1 + s2 * f2;
+  }
+  int ni;
+  if (m > m2) ni = idx;
+  else if (m2 > m) ni = i2;
+  else ni = min(idx, i2);
+  m = mm;
+  idx = ni;
+}
+
+__device__ __forceinline__ bool is_masked(int idx, const int* msk, int M) {
+  bool m = false;
+  for (int q = 0; q < M; ++q) m |= (msk[q] == idx);
+  return m;
+}
+
+__device__ __forceinline__ float pick8(const float (&z)[8], int e) {
+  float r = z[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) r = (e == k) ? z[k] : r;
+  return r;
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(kFull, v, o);
+    int oi = __shfl_xor_sync(kFull, i, o);
+    if (ranks_before(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// Block reduction of the per-thread statistics; thread 0 writes the chunk's
+// partial record.  Contains a __syncthreads().
+__device__ __forceinline__ void block_stats_write(const ScanState& st, float c, bool do_exp,
+                                                  float* sm_m, float* sm_s, int* sm_i,
+                                                  int* sm_n, PartStat* out_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float m = st.m, s = st.s;
+  int idx = st.idx, nan = st.nan;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float m2 = __shfl_xor_sync(kFull, m, o);
+    float s2 = __shfl_xor_sync(kFull, s, o);
+    int i2 = __shfl_xor_sync(kFull, idx, o);
+    nan |= __shfl_xor_sync(kFull, nan, o);
+    merge_stat(m, s, idx, m2, s2, i2, c, do_exp);
+  }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_s[warp] = s;
+    sm_i[warp] = idx;
+    sm_n[warp] = nan;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kWarps; ++w) {
+      nan |= sm_n[w];
+      merge_stat(m, s, idx, sm_m[w], sm_s[w], sm_i[w], c, do_exp);
+    }
+    PartStat ps;
+    ps.m = m;
+    ps.s = do_exp ? s : 0.f;
+    ps.idx = idx;
+    ps.flags = nan;
+    *out_part = ps;
+  }
+}
+
+}  // namespace ssd

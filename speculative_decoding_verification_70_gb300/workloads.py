@@ -46,7 +46,8 @@ class Workload:
     peaks: int
     peak_boost: float
     peak_place: str   # "uniform" | "zipf"
-    temp: str         # "1.0" | "0" | "0.7" | "mixed"
+    temp: str         # a number, "mixed" (half 0, half U(0.5,1.2)) or
+                      # "stochastic" (all U(0.5,1.2))
     ssd: bool         # draft logits carry k+1 rows
 
     @property
@@ -98,10 +99,11 @@ def _peak_indices(w: Workload, rows: int, rng: np.random.Generator) -> np.ndarra
 def temperatures(w: Workload, seed: int, temp: Optional[str] = None) -> torch.Tensor:
     rng = np.random.default_rng(seed + 7)
     t = temp if temp is not None else w.temp
-    if t == "mixed":
+    if t in ("mixed", "stochastic"):
         T = rng.uniform(0.5, 1.2, size=w.B).astype(np.float32)
-        zero = rng.permutation(w.B)[: w.B // 2]
-        T[zero] = 0.0
+        if t == "mixed":  # exactly half the rows greedy
+            zero = rng.permutation(w.B)[: w.B // 2]
+            T[zero] = 0.0
     else:
         T = np.full(w.B, float(t), dtype=np.float32)
     return torch.from_numpy(T)

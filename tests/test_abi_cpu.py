@@ -1,0 +1,157 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads,
+exports every symbol include/ssd.h declares, and rejects bad arguments on
+the host before touching CUDA.  Also checks that the oracle and the CUDA path
+share no code."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "speculative_decoding_verification_70_gb300")
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_70_gb300 import build
+    path = build.build()
+    from speculative_decoding_verification_70_gb300 import _binding
+    return _binding.load_library(path)
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^SSD_API\s+[\w\s\*]+?\b(ssd_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_symbols()
+    for n in ("ssd_softmax_temp", "ssd_verify", "ssd_sample_residual", "ssd_forked_recovery",
+              "ssd_spec_cache_lookup"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only",
+                          os.path.join(PKG, "libssd_gb300.so")],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ssd_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_binding_covers_the_header():
+    from speculative_decoding_verification_70_gb300._binding import SIGNATURES
+    assert sorted(s[0] for s in SIGNATURES) == declared_symbols()
+
+
+def test_status_strings(lib):
+    assert lib.ssd_status_string(0) == b"ok"
+    assert lib.ssd_status_string(1) == b"invalid argument"
+    assert lib.ssd_status_string(6) == b"workspace too small"
+    assert lib.ssd_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    assert lib.ssd_workspace_bytes(0, 5, 100, 0) == 0
+    assert lib.ssd_workspace_bytes(1, 32, 100, 0) == 0      # k > 31
+    assert lib.ssd_workspace_bytes(1, 5, 100, 17) == 0      # f > 16
+    a = lib.ssd_workspace_bytes(512, 7, 151936, 0)
+    b = lib.ssd_workspace_bytes(512, 7, 151936, 4)
+    assert 0 < a < b
+    assert b % 256 == 0
+    assert lib.ssd_softmax_workspace_bytes(4, 1000) > 0
+
+
+def _call_verify(lib, **kw):
+    args = dict(Z=1 << 20, zb=0, D=1 << 20, db=0, dt=0, B=1, k=2, V=8, x=1 << 20, T=1 << 20,
+                ua=1 << 20, acc=1 << 20, px=None, qx=None, us=None, out=None,
+                ws=1 << 20, wsb=1 << 30)
+    args.update(kw)
+    if args["zb"] == 0:
+        args["zb"] = (args["k"] + 1) * args["V"]
+    if args["db"] == 0:
+        args["db"] = args["k"] * args["V"]
+    return lib.ssd_verify(args["Z"], args["zb"], args["D"], args["db"], args["dt"], args["B"],
+                          args["k"], args["V"], args["x"], args["T"], args["ua"], args["acc"],
+                          args["px"], args["qx"], args["us"], args["out"], args["ws"],
+                          args["wsb"], None)
+
+
+def test_verify_rejects_bad_arguments_on_host(lib):
+    INVALID, DTYPE, WS = 1, 2, 6
+    assert _call_verify(lib, Z=None) == INVALID
+    assert _call_verify(lib, x=None) == INVALID
+    assert _call_verify(lib, B=0) == INVALID
+    assert _call_verify(lib, k=0) == INVALID
+    assert _call_verify(lib, k=32) == INVALID
+    assert _call_verify(lib, V=1) == INVALID
+    assert _call_verify(lib, dt=7) == DTYPE
+    assert _call_verify(lib, px=1 << 20) == INVALID          # p_at_x without q_at_x
+    assert _call_verify(lib, us=1 << 20) == INVALID          # u_smp without out_tok
+    assert _call_verify(lib, zb=5) == INVALID                # stride below a batch row
+    assert _call_verify(lib, Z=(1 << 20) + 2) == INVALID     # misaligned fp32 pointer
+    assert _call_verify(lib, ws=(1 << 20) + 64) == INVALID   # workspace not 256-aligned
+    assert _call_verify(lib, wsb=16) == WS
+
+
+def test_fork_and_cache_reject_bad_arguments_on_host(lib):
+    P = 1 << 20
+    # f >= V, f > 16, M > 64
+    assert lib.ssd_forked_recovery(P, 8, 0, 1, 2, 4, 4, None, 0, P, P, P, 1 << 30, None) == 1
+    assert lib.ssd_forked_recovery(P, 8 * 40, 0, 1, 2, 40, 17, None, 0, P, P, P, 1 << 30, None) == 1
+    assert lib.ssd_forked_recovery(P, 8, 0, 1, 2, 4, 2, P, 65, P, P, P, 1 << 30, None) == 1
+    assert lib.ssd_forked_recovery(P, 8, 0, 1, 2, 4, 2, None, 1, P, P, P, 1 << 30, None) == 1
+    h = ctypes.c_void_p()
+    assert lib.ssd_spec_cache_create(100, 7, ctypes.byref(h)) == 1   # not a power of two
+    assert lib.ssd_spec_cache_create(64, 0, ctypes.byref(h)) == 1
+    assert lib.ssd_spec_cache_create(64, 7, None) == 1
+    assert lib.ssd_spec_cache_lookup(None, P, P, P, 4, P, P, None) == 1
+    assert lib.ssd_softmax_temp(None, 0, 1, 8, P, None, P, P, P, P, 1 << 30, None) == 1
+    assert lib.ssd_selftest_exp2(None, None, None, 4, None) == 1
+
+
+def test_exp2_table_is_current(tmp_path):
+    sys.path.insert(0, os.path.join(PKG, "csrc"))
+    try:
+        import gen_exp2_table
+    finally:
+        sys.path.pop(0)
+    p = gen_exp2_table.main(str(tmp_path / "t.inc"))
+    assert open(p).read() == open(os.path.join(PKG, "csrc", "exp2_table.inc")).read()
+
+
+def test_exp2_table_values():
+    """The table entries are 2^(j/64) split into two binary32 values."""
+    import math
+    import struct
+    text = open(os.path.join(PKG, "csrc", "exp2_table.inc")).read()
+    rows = re.findall(r"\{(\S+)f, (\S+)f\}, // j = (-?\d+)", text)
+    assert len(rows) == 65
+    for hi, lo, j in rows:
+        h, l = float.fromhex(hi), float.fromhex(lo)
+        assert struct.unpack("f", struct.pack("f", h))[0] == h
+        assert abs(h + l - 2.0 ** (int(j) / 64)) <= 2.0 ** (int(j) / 64) * 2e-15
+
+
+def test_oracle_and_cuda_path_share_no_code():
+    """Neither side imports, includes or links the other."""
+    for dirpath, _, files in os.walk(PKG):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".inc")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "ssd_oracle" not in text, f
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c", ".h")):
+            text = open(os.path.join(ROOT, "oracle", f)).read()
+            assert "speculative_decoding_verification_70_gb300" not in text, f
+            assert "ssd.h" not in text, f
