@@ -164,6 +164,34 @@ SSD_API ssd_status ssd_verify(const void *Z, int64_t z_bstride, const void *D,
                       size_t ws_bytes, ssd_stream_t stream);
 
 /*
+ * ssd_verify_noalloc -- ssd_verify for callers that cannot allocate device
+ * memory (the pages have no counterpart; this is a deployment aid).  Some
+ * callers cannot call cudaMalloc or an allocating library routine: code that
+ * runs inside a framework that owns every allocation, or a process whose
+ * device memory is fully pre-reserved.  This call takes no workspace: its
+ * scratch is a file-scope device array of SSD_NOALLOC_SCRATCH_BYTES (8 MiB)
+ * that every GPU which loads the library holds until exit.
+ *   - Arguments and results are those of ssd_verify without ws/ws_bytes.
+ *   - Sizes whose workspace (ssd_workspace_bytes(B, k, V, 0)) exceeds the
+ *     array return SSD_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents;
+ *     each call writes every part it reads, so nothing needs clearing.  Calls
+ *     that overlap on the GPU (other streams, other host threads) race.
+ *   - The array's device error word is not exposed: data errors show as the
+ *     accept_len sentinels.
+ */
+#define SSD_NOALLOC_SCRATCH_BYTES (8u << 20)
+SSD_API ssd_status ssd_verify_noalloc(const void *Z, int64_t z_bstride, const void *D,
+                                      int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                                      const int32_t *x, const float *T, const float *u_acc,
+                                      int32_t *accept_len, float *p_at_x, float *q_at_x,
+                                      const float *u_smp, int32_t *out_tok,
+                                      ssd_stream_t stream);
+
+/*
  * ssd_sample_residual -- the recovery/bonus draw alone, after an ssd_verify
  * call on the same workspace, inputs and sizes that was given u_smp = NULL.
  * accept_len may be that call's output or any values in 0..k (negative

@@ -57,6 +57,8 @@ SIGNATURES = [
     ("ssd_spec_cache_capacity", _I, [_P]),
     ("ssd_spec_cache_depth", _I, [_P]),
     ("ssd_selftest_exp2", _I, [_P, _P, _P, _I, _P]),
+    ("ssd_verify_noalloc", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                _P, _P]),
     ("ssd_profile_begin", _I, [_I]),
     ("ssd_profile_end", _I, [_P, _I, _P]),
 ]

@@ -584,6 +584,56 @@ ssd_status ssd_selftest_exp2(const float* x_hi, const float* x_lo, double* out, 
   return cuda_status(launch_selftest_exp2(x_hi, x_lo, out, n, S(stream)));
 }
 
+// ---------------------------------------------------------------------------
+// ssd_verify_noalloc: the verify path with its scratch in a static array.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+// Scratch of ssd_verify_noalloc.  In host code this name is only a stand-in:
+// the kernels get the device address from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device (looked up once per
+// device, with that device current).
+ssd_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SSD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SSD_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SSD_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ssd_status ssd_verify_noalloc(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                              ssd_dtype dtype, int B, int k, int V, const int32_t* x,
+                              const float* T, const float* u_acc, int32_t* accept_len,
+                              float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
+                              ssd_stream_t stream) {
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
+  c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
+  c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
+  c.u_smp = u_smp; c.out_tok = out_tok; c.stream = S(stream);
+  if (ssd_workspace_bytes(B, k, V, 0) > SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
+  ssd_status st = noalloc_scratch(&c.ws);
+  if (st != SSD_OK) return st;
+  c.ws_bytes = SSD_NOALLOC_SCRATCH_BYTES;
+  return run_verify(c, false);  // checks the other arguments first
+}
+
 ssd_status ssd_profile_begin(int max_launches) {
   if (max_launches < 0 || max_launches > (1 << 20)) return SSD_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_prof.mu);
