@@ -125,6 +125,7 @@ struct VerifyCall {
   int f; const int32_t* mask; int M; int32_t* fork_tok; float* fork_logit;
   void* ws; size_t ws_bytes;
   cudaStream_t stream;
+  bool single_stream;  // no internal streams (the no-allocation entry point)
 };
 
 ssd_status check_common(const VerifyCall& c, bool fork) {
@@ -150,35 +151,49 @@ ssd_status check_common(const VerifyCall& c, bool fork) {
 
 // The streaming pass: rows without forked top-f in one kernel ("stats"),
 // the draft rows that feed the forked recovery in another ("stats_topf").
-cudaError_t run_stats(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s) {
+// When s_plain != s_topf, the target rows and the draft rows go to the two
+// streams and run concurrently.
+cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s_plain,
+                       cudaStream_t s_topf) {
   StatsParams sp = sp0;
   const bool topf = sp.Pdf > 0 && sp.f > 0;
+  const bool split = s_plain != s_topf;
   // plain rows: up to 4 chunks (128 KB) per CTA while the grid still has
   // at least ~16 CTAs per SM
-  const int rows_plain = topf ? sp.Pz : sp.R;
+  const int rows_plain = topf ? sp.Pz : (split ? sp.Pz : sp.R);
   sp.G = 1;
   while (sp.G < 4 && static_cast<long long>(B) * rows_plain * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
     sp.G *= 2;
-  const int plain_rows = topf ? sp.Pz : sp.R;
   cudaError_t e = cudaSuccess;
-  if (plain_rows > 0) {
-    ProfScope ps("stats", s);
-    e = launch_stats_rows(sp, B, dtype, vec, 0, plain_rows, false, s);
+  if (rows_plain > 0) {
+    ProfScope ps("stats", s_plain);
+    e = launch_stats_rows(sp, B, dtype, vec, 0, rows_plain, false, s_plain);
   }
-  if (e != cudaSuccess || !topf) return e;
-  ProfScope ps("stats_topf", s);
+  if (e != cudaSuccess) return e;
+  if (!topf) {
+    if (split && sp.R > sp.Pz) {  // draft statistics rows on the second stream
+      ProfScope ps("stats", s_topf);
+      e = launch_stats_rows(sp, B, dtype, vec, sp.Pz, sp.R - sp.Pz, false, s_topf);
+    }
+    return e;
+  }
+  ProfScope ps("stats_topf", s_topf);
 #if SSD_TOPF_STAGED
   if (vec) {  // chunks staged into shared memory by bulk copies
     StatsParams p = sp;
     p.r0 = sp.Pz;
-    return launch_stats_topf(p, B, dtype, s);
+    return launch_stats_topf(p, B, dtype, s_topf);
   }
 #endif
   StatsParams pt = sp;
   pt.G = 1;
   while (pt.G < 4 && static_cast<long long>(B) * sp.Pdf * ((sp.C + 2 * pt.G - 1) / (2 * pt.G)) >= 2432)
     pt.G *= 2;
-  return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s);
+  return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s_topf);
+}
+
+cudaError_t run_stats(const StatsParams& sp, int B, int dtype, bool vec, cudaStream_t s) {
+  return run_stats2(sp, B, dtype, vec, s, s);
 }
 
 cudaError_t cache_insert(const CacheView& v, const InsertArgs& a, cudaStream_t s) {
@@ -208,6 +223,141 @@ cudaError_t run_residual(const ResidualParams& rp, int B, int dtype, bool vec, c
   return launch_residual_select(rp, B, dtype, vec, s);
 }
 
+// ---------------------------------------------------------------------------
+// Per-device internal streams for the pipelined verify schedule.
+// ---------------------------------------------------------------------------
+constexpr int kMaxSlices = 8;
+constexpr int kMaxDevs = 64;
+
+struct DevStreams {
+  std::mutex mu;
+  bool ready = false;
+  bool failed = false;
+  cudaStream_t s1 = nullptr, s2 = nullptr;
+  cudaEvent_t ev[1 + 2 * kMaxSlices] = {};
+};
+DevStreams g_streams[kMaxDevs];
+
+// Streams and events of the current device, created on first use (no
+// device memory is allocated).  Returns null if they cannot be created.
+DevStreams* device_streams() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevs) return nullptr;
+  DevStreams& d = g_streams[dev];
+  std::lock_guard<std::mutex> lk(d.mu);
+  if (d.ready) return &d;
+  if (d.failed) return nullptr;
+  bool ok = cudaStreamCreateWithFlags(&d.s1, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&d.s2, cudaStreamNonBlocking) == cudaSuccess;
+  for (auto& e : d.ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    d.failed = true;
+    return nullptr;
+  }
+  d.ready = true;
+  return &d;
+}
+
+// Number of batch slices of the pipelined schedule (0: the plain
+// single-stream schedule).  Measured on mixed512 (B=512): one slice with the
+// target-row and draft-row statistics on two concurrent streams beats 2, 4
+// or 8 slices, whose per-slice draw launches put their latency on the
+// critical path.
+#ifndef SSD_SLICE_ROWS
+#define SSD_SLICE_ROWS 1024
+#endif
+int verify_slices(int B) {
+  if (B < 32) return 0;
+  int S = B / SSD_SLICE_ROWS;
+  if (S < 1) S = 1;
+  return S > kMaxSlices ? kMaxSlices : S;
+}
+
+struct SliceParams {
+  StatsParams sp;
+  FinalizeParams fp;
+  ResidualParams rp;
+};
+
+// Parameter blocks of batch rows [b0, b0 + Bs): every per-row pointer and
+// workspace region is offset by b0 rows.
+SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int b0, int Bs) {
+  SliceParams q;
+  const size_t es = esize(c.dt);
+  const char* Zb = static_cast<const char*>(c.Z) + static_cast<size_t>(b0) * c.zb * es;
+  const char* Db = static_cast<const char*>(c.D) + static_cast<size_t>(b0) * c.db * es;
+  const int Pf = c.k + 1;
+  const size_t C = static_cast<size_t>(L.ch.C);
+  PartStat* part = reinterpret_cast<PartStat*>(wsp(c.ws, L.part)) + static_cast<size_t>(b0) * L.R * C;
+  TopEntry* topk = reinterpret_cast<TopEntry*>(wsp(c.ws, L.topk)) +
+                   static_cast<size_t>(b0) * Pf * C * (fork ? c.f : 0);
+  RowStat* rowstat = reinterpret_cast<RowStat*>(wsp(c.ws, L.rowstat)) + static_cast<size_t>(b0) * L.R;
+  BState* bstate = reinterpret_cast<BState*>(wsp(c.ws, L.bstate)) + b0;
+  int* err = reinterpret_cast<int*>(wsp(c.ws, L.err));
+
+  StatsParams& sp = q.sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = Zb; sp.zb = c.zb; sp.Pz = c.k + 1;
+  sp.D = Db; sp.db = c.db; sp.Pds = c.k; sp.Pdf = fork ? Pf : 0;
+  sp.T = c.T + b0;
+  sp.mask = fork && c.M > 0 ? c.mask + static_cast<size_t>(b0) * Pf * c.M : nullptr;
+  sp.M = fork ? c.M : 0; sp.f = fork ? c.f : 0;
+  sp.V = c.V; sp.C = L.ch.C; sp.CH = L.ch.CH;
+  sp.R = sp.Pz + (sp.Pdf > sp.Pds ? sp.Pdf : sp.Pds);
+  sp.Rp = L.R;
+  sp.part = part; sp.topk = topk; sp.err = err;
+
+  FinalizeParams& fp = q.fp;
+  memset(&fp, 0, sizeof fp);
+  fp.Z = Zb; fp.zb = c.zb; fp.Pz = sp.Pz;
+  fp.D = Db; fp.db = c.db; fp.Pds = sp.Pds; fp.Pdf = sp.Pdf;
+  fp.dtype = c.dt == SSD_BF16 ? 1 : 0;
+  fp.B = Bs; fp.k = c.k; fp.V = c.V; fp.C = L.ch.C; fp.R = sp.R; fp.Rp = L.R; fp.f = sp.f;
+  fp.T = c.T + b0; fp.x = c.x + static_cast<size_t>(b0) * c.k;
+  fp.u_acc = c.u_acc + static_cast<size_t>(b0) * c.k;
+  fp.accept_len = c.accept_len + b0;
+  fp.p_at_x = c.p_at_x ? c.p_at_x + static_cast<size_t>(b0) * c.k : nullptr;
+  fp.q_at_x = c.q_at_x ? c.q_at_x + static_cast<size_t>(b0) * c.k : nullptr;
+  fp.out_tok = c.out_tok ? c.out_tok + static_cast<size_t>(b0) * (c.k + 1) : nullptr;
+  fp.fork_tok = fork ? c.fork_tok + static_cast<size_t>(b0) * Pf * c.f : nullptr;
+  fp.fork_logit = fork ? c.fork_logit + static_cast<size_t>(b0) * Pf * c.f : nullptr;
+  fp.part = part; fp.topk = topk;
+  fp.rowstat = rowstat; fp.bstate = bstate; fp.err = err;
+
+  ResidualParams& rp = q.rp;
+  memset(&rp, 0, sizeof rp);
+  rp.Z = Zb; rp.zb = c.zb; rp.Pz = sp.Pz;
+  rp.D = Db; rp.db = c.db;
+  rp.V = c.V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = c.k;
+  rp.T = c.T + b0; rp.u_smp = c.u_smp ? c.u_smp + b0 : nullptr;
+  rp.rowstat = rowstat; rp.bstate = bstate;
+  rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm)) + static_cast<size_t>(b0) * C * 2;
+  rp.rmass = reinterpret_cast<long long*>(wsp(c.ws, L.rmass)) + static_cast<size_t>(b0) * C;
+  rp.racc = reinterpret_cast<long long*>(wsp(c.ws, L.racc)) + static_cast<size_t>(b0) * C * 2;
+  rp.amb_cnt = reinterpret_cast<int*>(wsp(c.ws, L.amb_cnt)) + b0;
+  rp.amb_idx = reinterpret_cast<int*>(wsp(c.ws, L.amb_idx)) + static_cast<size_t>(b0) * kAmbCap;
+  rp.out_tok = fp.out_tok;
+  fp.amb_cnt = rp.amb_cnt;
+  return q;
+}
+
+// finalize + (optional) draw of one slice on stream s
+cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool vec,
+                         cudaStream_t s) {
+  cudaError_t e;
+  {
+    ProfScope ps("finalize", s);
+    e = launch_finalize(q.fp, s);
+  }
+  if (e != cudaSuccess || !c.u_smp) return e;
+  return run_residual(q.rp, Bs, q.fp.dtype, vec, s);
+}
+
+// Schedule: for B >= 32 the batch is cut into S slices.  The target-row and
+// draft-row statistics of each slice run on two internal streams; the
+// slice's finalisation and draw run on the caller's stream after both
+// (events), overlapping the next slice's statistics.  The caller's stream
+// waits for everything before its next work, so stream order is kept.
 ssd_status run_verify(const VerifyCall& c, bool fork) {
   ssd_status st = check_common(c, fork);
   if (st != SSD_OK) return st;
@@ -215,58 +365,30 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
   if (c.ws_bytes < L.total) return SSD_ERR_WORKSPACE;
   if (!aligned(c.ws, 256)) return SSD_ERR_INVALID_ARG;
   const bool vec = vec_ok(c.Z, c.zb, c.V, c.dt) && vec_ok(c.D, c.db, c.V, c.dt);
-
-  StatsParams sp;
-  memset(&sp, 0, sizeof sp);
-  sp.Z = c.Z; sp.zb = c.zb; sp.Pz = c.k + 1;
-  sp.D = c.D; sp.db = c.db; sp.Pds = c.k; sp.Pdf = fork ? c.k + 1 : 0;
-  sp.T = c.T;
-  sp.mask = c.mask; sp.M = fork ? c.M : 0; sp.f = fork ? c.f : 0;
-  sp.V = c.V; sp.C = L.ch.C; sp.CH = L.ch.CH;
-  sp.R = sp.Pz + (sp.Pdf > sp.Pds ? sp.Pdf : sp.Pds);
-  sp.Rp = L.R;
-  sp.part = reinterpret_cast<PartStat*>(wsp(c.ws, L.part));
-  sp.topk = reinterpret_cast<TopEntry*>(wsp(c.ws, L.topk));
-  sp.err = reinterpret_cast<int*>(wsp(c.ws, L.err));
-  cudaError_t e = run_stats(sp, c.B, c.dt == SSD_BF16 ? 1 : 0, vec, c.stream);
-  if (e != cudaSuccess) return SSD_ERR_CUDA;
-
-  FinalizeParams fp;
-  memset(&fp, 0, sizeof fp);
-  fp.Z = c.Z; fp.zb = c.zb; fp.Pz = sp.Pz;
-  fp.D = c.D; fp.db = c.db; fp.Pds = sp.Pds; fp.Pdf = sp.Pdf;
-  fp.dtype = c.dt == SSD_BF16 ? 1 : 0;
-  fp.B = c.B; fp.k = c.k; fp.V = c.V; fp.C = L.ch.C; fp.R = sp.R; fp.Rp = L.R; fp.f = sp.f;
-  fp.T = c.T; fp.x = c.x; fp.u_acc = c.u_acc;
-  fp.accept_len = c.accept_len; fp.p_at_x = c.p_at_x; fp.q_at_x = c.q_at_x;
-  fp.out_tok = c.out_tok;
-  fp.fork_tok = fork ? c.fork_tok : nullptr;
-  fp.fork_logit = fork ? c.fork_logit : nullptr;
-  fp.part = sp.part; fp.topk = sp.topk;
-  fp.rowstat = reinterpret_cast<RowStat*>(wsp(c.ws, L.rowstat));
-  fp.bstate = reinterpret_cast<BState*>(wsp(c.ws, L.bstate));
-  fp.err = reinterpret_cast<int*>(wsp(c.ws, L.err));
-  {
-    ProfScope ps("finalize", c.stream);
-    e = launch_finalize(fp, c.stream);
+  const int dtype = c.dt == SSD_BF16 ? 1 : 0;
+  const int S = c.single_stream ? 0 : verify_slices(c.B);
+  DevStreams* ds = S > 0 ? device_streams() : nullptr;
+  if (!ds) {
+    const SliceParams q = slice_params(c, fork, L, 0, c.B);
+    if (run_stats(q.sp, c.B, dtype, vec, c.stream) != cudaSuccess) return SSD_ERR_CUDA;
+    return enqueue_tail(c, q, c.B, vec, c.stream) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }
-  if (e != cudaSuccess) return SSD_ERR_CUDA;
-
-  if (c.u_smp) {
-    ResidualParams rp;
-    memset(&rp, 0, sizeof rp);
-    rp.Z = c.Z; rp.zb = c.zb; rp.Pz = sp.Pz;
-    rp.D = c.D; rp.db = c.db;
-    rp.V = c.V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = c.k;
-    rp.T = c.T; rp.u_smp = c.u_smp;
-    rp.rowstat = fp.rowstat; rp.bstate = fp.bstate;
-    rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm));
-    rp.rmass = reinterpret_cast<long long*>(wsp(c.ws, L.rmass));
-    rp.out_tok = c.out_tok;
-    e = run_residual(rp, c.B, fp.dtype, vec, c.stream);
-    if (e != cudaSuccess) return SSD_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(ds->mu);
+  cudaError_t e = cudaEventRecord(ds->ev[0], c.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->s1, ds->ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->s2, ds->ev[0], 0);
+  for (int i = 0; i < S && e == cudaSuccess; ++i) {
+    const int b0 = static_cast<int>(static_cast<long long>(c.B) * i / S);
+    const int b1 = static_cast<int>(static_cast<long long>(c.B) * (i + 1) / S);
+    const SliceParams q = slice_params(c, fork, L, b0, b1 - b0);
+    e = run_stats2(q.sp, b1 - b0, dtype, vec, ds->s1, ds->s2);
+    if (e == cudaSuccess) e = cudaEventRecord(ds->ev[1 + 2 * i], ds->s1);
+    if (e == cudaSuccess) e = cudaEventRecord(ds->ev[2 + 2 * i], ds->s2);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[1 + 2 * i], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[2 + 2 * i], 0);
+    if (e == cudaSuccess) e = enqueue_tail(c, q, b1 - b0, vec, c.stream);
   }
-  return SSD_OK;
+  return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 }  // namespace
@@ -407,6 +529,7 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
   pp.R = L.R;
   pp.bstate = reinterpret_cast<BState*>(wsp(ws, L.bstate));
   pp.out_tok = out_tok;
+  pp.amb_cnt = reinterpret_cast<int*>(wsp(ws, L.amb_cnt));
   cudaError_t e;
   {
     ProfScope ps("residual_prep", S(stream));
@@ -422,6 +545,9 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
   rp.rowstat = pp.rowstat; rp.bstate = pp.bstate;
   rp.rnorm = reinterpret_cast<long long*>(wsp(ws, L.rnorm));
   rp.rmass = reinterpret_cast<long long*>(wsp(ws, L.rmass));
+  rp.racc = reinterpret_cast<long long*>(wsp(ws, L.racc));
+  rp.amb_cnt = reinterpret_cast<int*>(wsp(ws, L.amb_cnt));
+  rp.amb_idx = reinterpret_cast<int*>(wsp(ws, L.amb_idx));
   rp.out_tok = out_tok;
   return cuda_status(run_residual(rp, B, dtype == SSD_BF16 ? 1 : 0, vec, S(stream)));
 }
@@ -631,6 +757,7 @@ ssd_status ssd_verify_noalloc(const void* Z, int64_t z_bstride, const void* D, i
   ssd_status st = noalloc_scratch(&c.ws);
   if (st != SSD_OK) return st;
   c.ws_bytes = SSD_NOALLOC_SCRATCH_BYTES;
+  c.single_stream = true;
   return run_verify(c, false);  // checks the other arguments first
 }
 

@@ -126,11 +126,14 @@ __device__ __forceinline__ void arg_df(float z, float m, float c_hi, float c_lo,
 }
 
 // 2^(xh + xl) for xh <= 0 as a float pair (hi, lo), relative error ~1e-9.
-// Method: x = n + j/64 + g with n integer, j in [-32, 32], |g| <= 1/128;
-// 2^x = 2^n * 2^(j/64) * (1 + P(g)) with the table 2^(j/64) held as float
-// pairs and P the degree-4 Taylor polynomial of 2^g - 1 (truncation < 4e-14).
-// Results below 2^-125 (relative to the row maximum 1) return 0.
-// `tab` is a shared-memory copy of kExp2Tab.
+// Method: J = round(64 xh) (one add of 1.5 * 2^23 gives both the rounded
+// float and the integer), x = J/64 + g with |g| <= 1/128 (exact) plus xl;
+// 2^x = 2^(J >> 6) * 2^((J & 63)/64) * (1 + P(g)) with the table 2^(j/64)
+// held as float pairs and P the degree-4 Taylor polynomial of 2^g - 1
+// (truncation < 4e-14).  Results below 2^-125 (relative to the row maximum
+// 1) return 0.  `tab` is a shared-memory copy of kExp2Tab.  The pair is
+// not normalised: hi is the scaled table value alone and lo carries the
+// polynomial part (up to 0.55% of hi), so callers use hi + lo, never hi alone.
 __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, float& hi,
                                         float& lo) {
   if (!(xh > -125.0f)) {
@@ -138,19 +141,20 @@ __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, f
     lo = 0.f;
     return;
   }
-  float n = rintf(xh);
-  float r = __fsub_rn(xh, n);                  // exact, |r| <= 1/2
-  float jf = rintf(__fmul_rn(r, 64.0f));       // j in [-32, 32]
-  float g = __fmaf_rn(jf, -0.015625f, r);      // exact, |g| <= 1/128
+  const float kMagic = 12582912.0f;  // 1.5 * 2^23: exact rounding for |v| < 2^22
+  const float tj = __fmaf_rn(xh, 64.0f, kMagic);
+  const float Jf = __fsub_rn(tj, kMagic);
+  const int J = __float_as_int(tj) - 0x4B400000;
+  float g = __fmaf_rn(Jf, -0.015625f, xh);     // exact, |g| <= 1/128
   g = __fadd_rn(g, xl);
   float P = __fmaf_rn(g, SSD_EXP2_C4, SSD_EXP2_C3);
   P = __fmaf_rn(g, P, SSD_EXP2_C2);
   P = __fmaf_rn(g, P, SSD_LN2_LO);
   P = __fmul_rn(g, P);
   P = __fmaf_rn(g, SSD_LN2_HI, P);             // 2^g - 1
-  float2 t = tab[static_cast<int>(jf) + 32];
-  float l = __fmaf_rn(t.x, P, __fmaf_rn(t.y, P, t.y));
-  float scale = __int_as_float((static_cast<int>(n) + 127) << 23);  // n in [-125, 0]
+  const float2 t = tab[J & 63];
+  const float l = __fmaf_rn(t.x, P, __fmaf_rn(t.y, P, t.y));
+  const float scale = __int_as_float(((J >> 6) + 127) << 23);  // J >> 6 in [-126, 0]
   hi = __fmul_rn(t.x, scale);
   lo = __fmul_rn(l, scale);
 }
@@ -158,7 +162,7 @@ __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, f
 // Copy the exp2 table to shared memory (call before the first exp2_df; a
 // __syncthreads() must follow).
 __device__ __forceinline__ void load_exp2_table(float2* tab) {
-  for (int i = threadIdx.x; i < 65; i += blockDim.x) tab[i] = kExp2Tab[i];
+  for (int i = threadIdx.x; i < 64; i += blockDim.x) tab[i] = kExp2Tab[i];
 }
 
 // double-float helpers

@@ -8,6 +8,7 @@
 namespace ssd {
 
 constexpr int kMaxMask = 64;        // masked tokens per (b, position)
+constexpr int kAmbCap = 2048;       // ambiguous-sign elements kept per row (draw)
 constexpr int kMaxChunkBytes = 32768;  // a chunk fits one shared-memory stage
 
 // Partial statistics of one chunk of one logit row.
@@ -48,7 +49,7 @@ struct Chunking {
 
 // Workspace of the verify / fork / residual calls.
 struct WsLayout {
-  size_t err, part, topk, rowstat, bstate, rnorm, rmass, total;
+  size_t err, part, topk, rowstat, bstate, rnorm, rmass, racc, amb_cnt, amb_idx, total;
   int B, R, Pf, f;
   Chunking ch;
 };
@@ -93,6 +94,7 @@ struct FinalizeParams {
   RowStat* rowstat;    // [B][Rp]
   BState* bstate;      // [B]
   int* err;
+  int* amb_cnt;        // [B], zeroed here for the draw
 };
 
 struct ResidualParams {
@@ -105,6 +107,9 @@ struct ResidualParams {
   const BState* bstate;
   long long* rnorm;    // [B][C][2]
   long long* rmass;    // [B][C]
+  long long* racc;     // [B][C][2]
+  int* amb_cnt;        // [B]
+  int* amb_idx;        // [B][kAmbCap]
   int32_t* out_tok;    // [B][k+1]
 };
 
@@ -130,6 +135,7 @@ struct PrepParams {
   int R;
   BState* bstate;
   int32_t* out_tok;
+  int* amb_cnt;
 };
 
 struct CacheView {
@@ -210,6 +216,9 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.bstate = off;                   off = align256(off + sizeof(BState) * B);
   L.rnorm = off;                    off = align256(off + sizeof(long long) * 2 * B * C);
   L.rmass = off;                    off = align256(off + sizeof(long long) * B * C);
+  L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * C);
+  L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
+  L.amb_idx = off;                  off = align256(off + sizeof(int) * B * kAmbCap);
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
   L.total = off;
   return L;
@@ -229,7 +238,7 @@ inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
   L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
   L.topk = off;
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * rows);
-  L.bstate = off; L.rnorm = off; L.rmass = off;
+  L.bstate = off; L.rnorm = off; L.rmass = off; L.racc = off; L.amb_cnt = off; L.amb_idx = off;
   L.total = off;
   return L;
 }

@@ -15,8 +15,17 @@
 // same totals.
 //
 // Kernels (one CTA per chunk of row n, then one CTA per batch row):
-//   residual_norm   S_z = sum 2^((z - m_z) c) and S_d over row n of Z and D
-//   residual_mass   W_c = sum over chunk c of max(0, p - q)
+//   residual_norm   one pass over row n of Z and D: S_z = sum a, S_d = sum b
+//                   with a = 2^((z - m_z) c), b = 2^((d - m_d) c), and the
+//                   residual mass by sign: with rho~ = S_z/S_d taken from the
+//                   streaming statistics (relative error ~1e-7), elements with
+//                   a - rho~ b clearly positive (margin 1e-3) add to A and B,
+//                   so that S_z * W_c = A_c - rho B_c exactly for them once
+//                   rho = S_z/S_d is known; clearly negative ones add
+//                   nothing; the few ambiguous ones are listed and evaluated
+//                   exactly by the select kernel.
+//   residual_mass   the direct W_c = sum max(0, p - q), run only for rows
+//                   whose ambiguous list overflowed
 //   residual_select chunk -> thread -> element select, writes out_tok[b, n]
 #include <math.h>
 
@@ -30,7 +39,13 @@ struct RowCtx {
   float c_hi, c_lo;    // log2(e)/T
   float iz_hi, iz_lo;  // 1/S_z
   float id_hi, id_lo;  // 1/S_d
+  float rho;           // approximate S_z / S_d from the streaming statistics
 };
+
+constexpr float kSignMargin = 1e-3f;
+constexpr float kFixAcc = 1125899906842624.0f;     // 2^50: per-chunk A, B
+constexpr double kInvFixAcc = 1.0 / 1125899906842624.0;
+constexpr double kInvFixResidual = 1.0 / 1152921504606846976.0;  // 2^-60
 
 // Weight of element i in the given quantity:
 //   Q_NORM_Z : 2^((z - m_z) c)         (unnormalised, for S_z and the p_k draw)
@@ -121,7 +136,12 @@ __device__ __forceinline__ bool load_ctx(const ResidualParams& p, int b, BState&
     const RowStat rz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n];
     c.mz = rz.m;
     c.md = 0.f;
-    if (bs.mode == kModeResidual) c.md = p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m;
+    c.rho = 1.f;
+    if (bs.mode == kModeResidual) {
+      const RowStat rd = p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n];
+      c.md = rd.m;
+      c.rho = static_cast<float>(rz.S / rd.S);
+    }
     temp_coeff(p.T[b], c.c_hi, c.c_lo);
     c.iz_hi = c.iz_lo = c.id_hi = c.id_lo = 0.f;
     if (with_inverses) norm_inverses(p, b, c);
@@ -142,10 +162,41 @@ __device__ __forceinline__ void row_ptrs(const ResidualParams& p, int b, int n,
        static_cast<int64_t>(n) * p.V;
 }
 
+// One element of the fused pass: a (and b) added to the normaliser sums; in
+// residual mode the sign split against rho~.
+__device__ __forceinline__ void pass_element(float z, float d, int idx, bool resid,
+                                             const RowCtx& cx, const float2* tab, float& sah,
+                                             float& sal, float& sbh, float& sbl, float& ah,
+                                             float& al, float& bh, float& bl, int* amb_cnt,
+                                             int* amb_idx) {
+  float xh, xl, a_h, a_l;
+  arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
+  exp2_df(xh, xl, tab, a_h, a_l);
+  df_acc(sah, sal, a_h, a_l);
+  if (!resid) return;
+  float b_h, b_l;
+  arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
+  exp2_df(xh, xl, tab, b_h, b_l);
+  df_acc(sbh, sbl, b_h, b_l);
+  // exp2_df's pair is not normalised (lo holds up to 0.55% of hi), so the
+  // split compares the rounded sums, good to ~1e-7 against the 1e-3 margin
+  const float a1 = __fadd_rn(a_h, a_l);
+  const float rb = cx.rho * __fadd_rn(b_h, b_l);
+  const float diff = a1 - rb;
+  const float lim = kSignMargin * fmaxf(a1, rb);
+  if (diff > lim) {
+    df_acc(ah, al, a_h, a_l);
+    df_acc(bh, bl, b_h, b_l);
+  } else if (diff >= -lim && (a1 > 0.f || rb > 0.f)) {
+    const int q = atomicAdd(amb_cnt, 1);
+    if (q < kAmbCap) amb_idx[q] = idx;
+  }
+}
+
 // grid (C, B)
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams p) {
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
   const int c = blockIdx.x, b = blockIdx.y;
@@ -155,33 +206,54 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   if (!load_ctx(p, b, bs, cx, &s_cx, false)) return;
   const typename Tag::Elem *zr, *dr;
   row_ptrs<Tag>(p, b, bs.n, zr, dr);
+  const bool resid = bs.mode == kModeResidual;
   const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
   const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
   const int hi = min(chi, lo + p.E);
-  float h, l;
-  range_sum<Tag, VEC, Q_NORM_Z>(zr, dr, lo, hi, cx, tab, h, l);
-  long long fz = df_to_fix(h, l, kFixMass);
-  long long fd = 0;
-  if (bs.mode == kModeResidual) {
-    range_sum<Tag, VEC, Q_NORM_D>(zr, dr, lo, hi, cx, tab, h, l);
-    fd = df_to_fix(h, l, kFixMass);
+  int* amb_cnt = p.amb_cnt + b;
+  int* amb_idx = p.amb_idx + static_cast<int64_t>(b) * kAmbCap;
+  float sah = 0.f, sal = 0.f, sbh = 0.f, sbl = 0.f, ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
+  constexpr int kV = Tag::kVec;
+  int i = lo;
+  if (VEC) {
+    for (; i + kV <= hi; i += kV) {
+      float z[8], d[8];
+      Tag::loadv_cached(zr + i, z);
+      if (resid) Tag::loadv_cached(dr + i, d);
+#pragma unroll
+      for (int e = 0; e < kV; ++e)
+        pass_element(z[e], resid ? d[e] : 0.f, i + e, resid, cx, tab, sah, sal, sbh, sbl, ah, al,
+                     bh, bl, amb_cnt, amb_idx);
+    }
   }
-  long long tz = block_sum_i64(fz, sm);
-  long long td = block_sum_i64(fd, sm);
+  for (; i < hi; ++i)
+    pass_element(Tag::load1(zr + i), resid ? Tag::load1(dr + i) : 0.f, i, resid, cx, tab, sah,
+                 sal, sbh, sbl, ah, al, bh, bl, amb_cnt, amb_idx);
+  long long tz = block_sum_i64(df_to_fix(sah, sal, kFixMass), sm);
+  long long td = 0, ta = 0, tb = 0;
+  if (resid) {
+    td = block_sum_i64(df_to_fix(sbh, sbl, kFixMass), sm);
+    ta = block_sum_i64(df_to_fix(ah, al, kFixAcc), sm);
+    tb = block_sum_i64(df_to_fix(bh, bl, kFixAcc), sm);
+  }
   if (threadIdx.x == 0) {
-    p.rnorm[(static_cast<int64_t>(b) * p.C + c) * 2 + 0] = tz;
-    p.rnorm[(static_cast<int64_t>(b) * p.C + c) * 2 + 1] = td;
+    const int64_t o = (static_cast<int64_t>(b) * p.C + c) * 2;
+    p.rnorm[o + 0] = tz;
+    p.rnorm[o + 1] = td;
+    p.racc[o + 0] = ta;
+    p.racc[o + 1] = tb;
   }
 }
 
 // grid (C, B)
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams p) {
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
   const int c = blockIdx.x, b = blockIdx.y;
-  if (p.bstate[b].mode != kModeResidual) return;
+  // only rows whose ambiguous list overflowed need the direct mass
+  if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= kAmbCap) return;
   BState bs;
   RowCtx cx;
   load_exp2_table(tab);
@@ -227,6 +299,10 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
   long long own = df_to_fix(h, l, scale);
   long long tot;
   long long incl = block_scan_i64(own, sm, &tot);
+  // a chunk mass taken from the sign split can exceed this chunk's direct
+  // total by rounding (~1e-10 relative); such a target picks the chunk's
+  // last positive element
+  if (target >= tot) target = tot - 1;
   if (tid == 0) *s_pick = kThreads;
   __syncthreads();
   if (incl > target && incl - own <= target) atomicMin(s_pick, tid);
@@ -264,8 +340,9 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
 // grid B
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParams p) {
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
+  __shared__ long long s_amb[256];  // per-chunk exact mass of the ambiguous elements (2^60)
   __shared__ int s_pick;
   __shared__ int s_chunk;
   __shared__ long long s_target;
@@ -274,50 +351,112 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
   BState bs;
   RowCtx cx;
   load_exp2_table(tab);
+  for (int q = threadIdx.x; q < p.C; q += kThreads) s_amb[q] = 0;
   if (!load_ctx(p, b, bs, cx, &s_cx, p.bstate[b].mode == kModeResidual)) return;
+  const typename Tag::Elem *zr, *dr;
+  row_ptrs<Tag>(p, b, bs.n, zr, dr);
   int mode = bs.mode;
+  const int n_amb = (mode == kModeResidual) ? p.amb_cnt[b] : 0;
+  const bool split = mode == kModeResidual && n_amb <= kAmbCap;
+  if (split) {
+    const int* amb = p.amb_idx + static_cast<int64_t>(b) * kAmbCap;
+    for (int q = threadIdx.x; q < n_amb; q += kThreads) {
+      const int i = amb[q];
+      float wh, wl;
+      weight<Q_RESID>(Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[i / p.CH]),
+                static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
+    }
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    // chunk masses: residual (2^60 units) or, for the bonus draw and the
-    // all-zero-residual fallback, unnormalised target weights (2^42 units)
-    long long W = 0;
-    if (mode == kModeResidual) {
-      for (int q = 0; q < p.C; ++q) W += p.rmass[static_cast<int64_t>(b) * p.C + q];
-      if (W == 0) mode = kModeTarget;
-    }
-    const long long* mass;
-    int stride;
-    if (mode == kModeResidual) {
-      mass = p.rmass + static_cast<int64_t>(b) * p.C;
-      stride = 1;
-    } else {
-      mass = p.rnorm + static_cast<int64_t>(b) * p.C * 2;
-      stride = 2;
-      W = 0;
-      for (int q = 0; q < p.C; ++q) W += mass[q * stride];
-    }
-    unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
-    long long cum = 0;
+    const int64_t rb = static_cast<int64_t>(b) * p.C;
+    bool resid = mode == kModeResidual;
+    double t_in = 0.0;  // target offset inside the chosen chunk, in w units
     int pick = p.C - 1;
-    long long before = 0;
-    for (int q = 0; q < p.C; ++q) {
-      long long nx = cum + mass[q * stride];
-      if (nx > static_cast<long long>(t)) {
-        pick = q;
-        before = cum;
-        break;
+    long long t_fix = 0;
+    if (resid && split) {
+      // W_c = (A_c - rho B_c) / S_z + ambiguous part, rho = S_z / S_d
+      long long sz = 0, sd = 0;
+      for (int q = 0; q < p.C; ++q) {
+        sz += p.rnorm[(rb + q) * 2 + 0];
+        sd += p.rnorm[(rb + q) * 2 + 1];
       }
-      cum = nx;
-      before = cum;
+      const double Sz = static_cast<double>(sz) * kInvFixMass;
+      const double rho = static_cast<double>(sz) / static_cast<double>(sd);
+      double W = 0.0;
+      for (int q = 0; q < p.C; ++q) {
+        const double wc = (static_cast<double>(p.racc[(rb + q) * 2 + 0]) -
+                           rho * static_cast<double>(p.racc[(rb + q) * 2 + 1])) *
+                              kInvFixAcc / Sz +
+                          static_cast<double>(s_amb[q]) * kInvFixResidual;
+        W += wc > 0.0 ? wc : 0.0;
+      }
+      if (W > 0.0) {
+        const double t = static_cast<double>(p.u_smp[b]) * W;
+        double cum = 0.0;
+        for (int q = 0; q < p.C; ++q) {
+          double wc = (static_cast<double>(p.racc[(rb + q) * 2 + 0]) -
+                       rho * static_cast<double>(p.racc[(rb + q) * 2 + 1])) *
+                          kInvFixAcc / Sz +
+                      static_cast<double>(s_amb[q]) * kInvFixResidual;
+          wc = wc > 0.0 ? wc : 0.0;
+          if (cum + wc > t) {
+            pick = q;
+            t_in = t - cum;
+            break;
+          }
+          cum += wc;
+          t_in = t - cum;
+        }
+        t_fix = static_cast<long long>(t_in * 1152921504606846976.0);
+      } else {
+        resid = false;  // all-zero residual: draw from p_n
+      }
+    } else if (resid) {
+      // overflowed ambiguous list: the direct masses (2^60 units)
+      long long W = 0;
+      for (int q = 0; q < p.C; ++q) W += p.rmass[rb + q];
+      if (W == 0) {
+        resid = false;
+      } else {
+        const unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
+        long long cum = 0;
+        for (int q = 0; q < p.C; ++q) {
+          const long long nx = cum + p.rmass[rb + q];
+          if (nx > static_cast<long long>(t)) {
+            pick = q;
+            break;
+          }
+          cum = nx;
+        }
+        t_fix = static_cast<long long>(t) - cum;
+      }
     }
-    s_chunk = pick | (mode == kModeResidual ? 0 : 0x40000000);
-    s_target = static_cast<long long>(t) - before;
+    if (!resid) {
+      // bonus draw, or the all-zero-residual fallback: target weights (2^42)
+      long long W = 0;
+      for (int q = 0; q < p.C; ++q) W += p.rnorm[(rb + q) * 2];
+      const unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
+      long long cum = 0;
+      pick = p.C - 1;
+      for (int q = 0; q < p.C; ++q) {
+        const long long nx = cum + p.rnorm[(rb + q) * 2];
+        if (nx > static_cast<long long>(t)) {
+          pick = q;
+          break;
+        }
+        cum = nx;
+      }
+      t_fix = static_cast<long long>(t) - cum;
+    }
+    s_chunk = pick | (resid ? 0 : 0x40000000);
+    s_target = t_fix;
   }
   __syncthreads();
   const int q = s_chunk & 0xffff;
   const bool resid = (s_chunk & 0x40000000) == 0;
   const long long target = s_target;
-  const typename Tag::Elem *zr, *dr;
-  row_ptrs<Tag>(p, b, bs.n, zr, dr);
   const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
   int tok;
   if (resid)
@@ -342,6 +481,7 @@ __global__ void residual_prep_kernel(PrepParams p) {
                                                        : (n < p.k ? kModeResidual : kModeTarget);
   bs.pad0 = bs.pad1 = 0;
   p.bstate[b] = bs;
+  p.amb_cnt[b] = 0;
   int32_t* o = p.out_tok + static_cast<int64_t>(b) * (p.k + 1);
   for (int j = 0; j <= p.k; ++j) {
     int v = -1;
@@ -387,7 +527,7 @@ cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s) {
 
 // Self-test of exp2_df: out[i] = 2^(x_hi + x_lo).
 __global__ void selftest_exp2_kernel(const float* xh, const float* xl, double* out, int n) {
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   load_exp2_table(tab);
   __syncthreads();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {

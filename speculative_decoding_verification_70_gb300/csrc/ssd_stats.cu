@@ -370,7 +370,7 @@ __device__ __forceinline__ float logit_at(const void* base, int dtype, int64_t i
 __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   __shared__ RowStat rs[2 * (32 + 1)];
   __shared__ int heads[kWarps][256];
   load_exp2_table(tab);
@@ -479,6 +479,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
     bs.mode = (n < 0 || greedy) ? kModeNone : (n < k ? kModeResidual : kModeTarget);
     bs.pad0 = bs.pad1 = 0;
     p.bstate[b] = bs;
+    if (p.amb_cnt) p.amb_cnt[b] = 0;
     int e = 0;
     if (t_bad) e |= 0x1;
     else if (any_tok_bad) e |= 0x4;
@@ -493,7 +494,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
 
 // grid: ceil(rows / kWarps); one warp per row
 __global__ void __launch_bounds__(kThreads) softmax_finalize_kernel(SoftmaxParams p) {
-  __shared__ float2 tab[65];
+  __shared__ float2 tab[64];
   load_exp2_table(tab);
   __syncthreads();
   const int lane = threadIdx.x & 31;
