@@ -43,9 +43,9 @@ struct RowCtx {
 };
 
 constexpr float kSignMargin = 1e-3f;
-constexpr float kFixAcc = 1125899906842624.0f;     // 2^50: per-chunk A, B
-constexpr double kInvFixAcc = 1.0 / 1125899906842624.0;
-constexpr double kInvFixResidual = 1.0 / 1152921504606846976.0;  // 2^-60
+// 2^48: per-chunk A, B.  a, b <= 1 and a chunk holds at most 2^14
+// elements, so a chunk sum stays below 2^62.
+constexpr float kFixAcc = 281474976710656.0f;
 
 // Weight of element i in the given quantity:
 //   Q_NORM_Z : 2^((z - m_z) c)         (unnormalised, for S_z and the p_k draw)
@@ -337,30 +337,61 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
   return -1 - *s_pick;
 }
 
-// grid B
+// grid B.  One CTA per batch row; every chunk-level step runs one chunk per
+// thread (C <= kThreads): the chunk weights are formed in parallel, an int64
+// block scan places the target, and one 128-bit product gives
+// floor(u * W).  Only the two normaliser inverses are taken by one thread.
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParams p) {
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
-  __shared__ long long s_amb[256];  // per-chunk exact mass of the ambiguous elements (2^60)
+  __shared__ long long s_amb[kThreads];  // per-chunk exact mass of the ambiguous elements (2^60)
   __shared__ int s_pick;
   __shared__ int s_chunk;
   __shared__ long long s_target;
   __shared__ RowCtx s_cx;
-  const int b = blockIdx.x;
-  BState bs;
-  RowCtx cx;
+  __shared__ double s_acc[2];            // rho = S_z / S_d and 2^12 / S_z
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const BState bs = p.bstate[b];
+  if (bs.mode == kModeNone) return;
   load_exp2_table(tab);
-  for (int q = threadIdx.x; q < p.C; q += kThreads) s_amb[q] = 0;
-  if (!load_ctx(p, b, bs, cx, &s_cx, p.bstate[b].mode == kModeResidual)) return;
+  const bool resid_row = bs.mode == kModeResidual;
+  const int64_t rb = static_cast<int64_t>(b) * p.C;
+  long long cz = 0, cd = 0, ca = 0, cb = 0;
+  if (tid < p.C) {
+    cz = p.rnorm[(rb + tid) * 2 + 0];
+    if (resid_row) {
+      cd = p.rnorm[(rb + tid) * 2 + 1];
+      ca = p.racc[(rb + tid) * 2 + 0];
+      cb = p.racc[(rb + tid) * 2 + 1];
+    }
+  }
+  s_amb[tid] = 0;
+  const long long sz = block_sum_i64(cz, sm);
+  const long long sd = resid_row ? block_sum_i64(cd, sm) : 1;
+  if (tid == 0) {
+    RowCtx c;
+    c.mz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n].m;
+    c.md = resid_row ? p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m : 0.f;
+    c.rho = 1.f;
+    temp_coeff(p.T[b], c.c_hi, c.c_lo);
+    const double Sz = static_cast<double>(sz) * kInvFixMass;
+    const double Sd = static_cast<double>(sd) * kInvFixMass;
+    split_double(1.0 / Sz, c.iz_hi, c.iz_lo);
+    split_double(1.0 / Sd, c.id_hi, c.id_lo);
+    s_cx = c;
+    s_acc[0] = static_cast<double>(sz) / static_cast<double>(sd);
+    s_acc[1] = 4096.0 / Sz;
+  }
+  __syncthreads();
+  const RowCtx cx = s_cx;
   const typename Tag::Elem *zr, *dr;
   row_ptrs<Tag>(p, b, bs.n, zr, dr);
-  int mode = bs.mode;
-  const int n_amb = (mode == kModeResidual) ? p.amb_cnt[b] : 0;
-  const bool split = mode == kModeResidual && n_amb <= kAmbCap;
+  const int n_amb = resid_row ? p.amb_cnt[b] : 0;
+  const bool split = resid_row && n_amb <= kAmbCap;
   if (split) {
     const int* amb = p.amb_idx + static_cast<int64_t>(b) * kAmbCap;
-    for (int q = threadIdx.x; q < n_amb; q += kThreads) {
+    for (int q = tid; q < n_amb; q += kThreads) {
       const int i = amb[q];
       float wh, wl;
       weight<Q_RESID>(Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
@@ -369,93 +400,42 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    const int64_t rb = static_cast<int64_t>(b) * p.C;
-    bool resid = mode == kModeResidual;
-    double t_in = 0.0;  // target offset inside the chosen chunk, in w units
-    int pick = p.C - 1;
-    long long t_fix = 0;
-    if (resid && split) {
-      // W_c = (A_c - rho B_c) / S_z + ambiguous part, rho = S_z / S_d
-      long long sz = 0, sd = 0;
-      for (int q = 0; q < p.C; ++q) {
-        sz += p.rnorm[(rb + q) * 2 + 0];
-        sd += p.rnorm[(rb + q) * 2 + 1];
-      }
-      const double Sz = static_cast<double>(sz) * kInvFixMass;
-      const double rho = static_cast<double>(sz) / static_cast<double>(sd);
-      double W = 0.0;
-      for (int q = 0; q < p.C; ++q) {
-        const double wc = (static_cast<double>(p.racc[(rb + q) * 2 + 0]) -
-                           rho * static_cast<double>(p.racc[(rb + q) * 2 + 1])) *
-                              kInvFixAcc / Sz +
-                          static_cast<double>(s_amb[q]) * kInvFixResidual;
-        W += wc > 0.0 ? wc : 0.0;
-      }
-      if (W > 0.0) {
-        const double t = static_cast<double>(p.u_smp[b]) * W;
-        double cum = 0.0;
-        for (int q = 0; q < p.C; ++q) {
-          double wc = (static_cast<double>(p.racc[(rb + q) * 2 + 0]) -
-                       rho * static_cast<double>(p.racc[(rb + q) * 2 + 1])) *
-                          kInvFixAcc / Sz +
-                      static_cast<double>(s_amb[q]) * kInvFixResidual;
-          wc = wc > 0.0 ? wc : 0.0;
-          if (cum + wc > t) {
-            pick = q;
-            t_in = t - cum;
-            break;
-          }
-          cum += wc;
-          t_in = t - cum;
-        }
-        t_fix = static_cast<long long>(t_in * 1152921504606846976.0);
-      } else {
-        resid = false;  // all-zero residual: draw from p_n
-      }
-    } else if (resid) {
-      // overflowed ambiguous list: the direct masses (2^60 units)
-      long long W = 0;
-      for (int q = 0; q < p.C; ++q) W += p.rmass[rb + q];
-      if (W == 0) {
-        resid = false;
-      } else {
-        const unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
-        long long cum = 0;
-        for (int q = 0; q < p.C; ++q) {
-          const long long nx = cum + p.rmass[rb + q];
-          if (nx > static_cast<long long>(t)) {
-            pick = q;
-            break;
-          }
-          cum = nx;
-        }
-        t_fix = static_cast<long long>(t) - cum;
-      }
+  // chunk weights in the units select_in_chunk sums: residual mass in 2^60
+  // (W_c = (A_c - rho B_c) / S_z plus the ambiguous part, or the direct
+  // masses when the ambiguous list overflowed), target mass a in 2^42
+  long long wq = 0;
+  if (tid < p.C) {
+    if (split) {
+      const double v = (static_cast<double>(ca) - s_acc[0] * static_cast<double>(cb)) * s_acc[1] +
+                       static_cast<double>(s_amb[tid]);
+      wq = v > 0.0 ? static_cast<long long>(v) : 0;
+    } else if (resid_row) {
+      wq = p.rmass[rb + tid];
+    } else {
+      wq = cz;
     }
-    if (!resid) {
-      // bonus draw, or the all-zero-residual fallback: target weights (2^42)
-      long long W = 0;
-      for (int q = 0; q < p.C; ++q) W += p.rnorm[(rb + q) * 2];
-      const unsigned long long t = scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]);
-      long long cum = 0;
-      pick = p.C - 1;
-      for (int q = 0; q < p.C; ++q) {
-        const long long nx = cum + p.rnorm[(rb + q) * 2];
-        if (nx > static_cast<long long>(t)) {
-          pick = q;
-          break;
-        }
-        cum = nx;
-      }
-      t_fix = static_cast<long long>(t) - cum;
-    }
-    s_chunk = pick | (resid ? 0 : 0x40000000);
-    s_target = t_fix;
+  }
+  long long W;
+  long long incl = block_scan_i64(wq, sm, &W);
+  bool resid = resid_row;
+  if (resid && W <= 0) {  // all-zero residual: draw from p_n
+    resid = false;
+    wq = tid < p.C ? cz : 0;
+    incl = block_scan_i64(wq, sm, &W);
+  }
+  const long long t =
+      static_cast<long long>(scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]));
+  if (tid == 0) {
+    s_chunk = p.C - 1;  // unreachable default: t < W always finds a chunk
+    s_target = 0;
   }
   __syncthreads();
-  const int q = s_chunk & 0xffff;
-  const bool resid = (s_chunk & 0x40000000) == 0;
+  if (wq > 0 && incl > t && incl - wq <= t) {  // exactly one thread
+    s_chunk = tid;
+    s_target = t - (incl - wq);
+  }
+  __syncthreads();
+  const int q = s_chunk;
   const long long target = s_target;
   const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
   int tok;
@@ -463,7 +443,7 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     tok = select_in_chunk<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual, target, sm, &s_pick);
   else
     tok = select_in_chunk<Tag, VEC, Q_NORM_Z>(zr, dr, clo, chi, p.E, cx, tab, kFixMass, target, sm, &s_pick);
-  if (threadIdx.x == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
+  if (tid == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
 }
 
 // Prepare the per-row draw state from a caller-supplied accept_len (used by

@@ -352,6 +352,38 @@ def test_full_size_qwen_batch(gpu_lib):
                   out["fork_tok"], out["fork_logit"])
 
 
+def test_residual_extremes_large_chunks(gpu_lib):
+    """Residual draws at the largest chunk sums and with overflowing
+    ambiguous-sign lists (bf16, B=64: chunks of ~15K elements).
+    Rows 0 mod 4: flat target (p uniform) against a peaked draft, so nearly
+    every element sits on the positive side of p - q.  Rows 1 mod 4: the draft
+    equals the target except at the draft token, a token of target
+    probability ~1e-4 raised by 0.25, so |p - q| is below 1e-3 (p + q) on
+    every other element.  u_acc = 0.999 rejects early."""
+    w = W.workload("qwen_b64", temp="1.0")
+    inp = W.make_inputs(w, device=DEV, seed=321)
+    Z, D, x = inp["Z"].clone(), inp["D"].clone(), inp["x"].clone()
+    Z[0::4] = 1.0
+    for b in range(1, w.B, 4):
+        for j in range(w.k):
+            lp = torch.log_softmax(Z[b, j].float(), dim=0)
+            v = int(torch.argmin((lp - np.log(1e-4)).abs()))
+            x[b, j] = v
+            D[b, j] = Z[b, j]
+            D[b, j, v] += 0.25
+    inp["Z"], inp["D"], inp["x"] = Z, D, x
+    inp["u_acc"] = torch.full_like(inp["u_acc"], 0.999)
+    out = run_verify(gpu_lib, inp, fork_f=w.f)
+    torch.cuda.synchronize()
+    bs = np.concatenate([np.arange(0, w.B, 4)[:8], np.arange(1, w.B, 4)[:8], [2, 3]])
+    ref = oracle_rows(inp, bs)
+    assert (ref["accept_len"][:16] < w.k).all()
+    rep = compare_verify(inp, out, bs, ref, Report())
+    assert not rep.failures, rep.failures[:5]
+    assert rep.sampled_mismatch == 0, rep.summary()
+    assert gpu_lib.get_device_error(out["ws"]) == 0
+
+
 def test_sampled_token_agreement_rate(gpu_lib):
     """>= 99.99% identical draws over 12288 stochastic rows, every mismatch
     traced to a uniform within 1e-6 of a CDF boundary."""
