@@ -296,7 +296,11 @@ SSD_API int ssd_spec_cache_depth(const ssd_spec_cache *cache);
  * launch stream (at most max_launches launches; later ones go unrecorded but
  * are still counted).  ssd_profile_end waits for the recorded events and
  * fills out[0 .. *n_out) with one entry per kernel name: launches and total
- * device time.  Events are created at begin and destroyed at end.
+ * device time.  Entries with launches == 0 are phases that span several
+ * launches: "stats_pass" is the statistics pass of a batched verify, whose
+ * target-row and draft-row kernels run concurrently on two internal streams,
+ * from the fork to the join on the caller's stream.  Events are created at
+ * begin and destroyed at end.
  */
 typedef struct {
     char name[40];

@@ -69,15 +69,20 @@ struct Profiler {
 };
 Profiler g_prof;
 
-// Brackets one kernel launch when profiling is on.
+// Brackets one kernel launch when profiling is on.  A phase scope
+// (launch = false) brackets several launches, possibly on other streams
+// joined back by events, and adds no launch to the count.
 struct ProfScope {
-  cudaStream_t s;
+  cudaStream_t s = nullptr;
   int rec = -1;
-  ProfScope(const char* name, cudaStream_t st) : s(st) {
+  ProfScope() = default;
+  ProfScope(const char* name, cudaStream_t st, bool launch = true) { begin(name, st, launch); }
+  void begin(const char* name, cudaStream_t st, bool launch = true) {
+    s = st;
     if (!g_prof.on) return;
     std::lock_guard<std::mutex> lk(g_prof.mu);
     int id = g_prof.kernel_id(name);
-    g_prof.counts[id] += 1;
+    if (launch) g_prof.counts[id] += 1;
     size_t used = g_prof.recs.size();
     if (static_cast<int>(used) >= g_prof.cap) return;
     ProfRecord r;
@@ -88,11 +93,15 @@ struct ProfScope {
     g_prof.recs.push_back(r);
     rec = static_cast<int>(used);
   }
-  ~ProfScope() {
+  void end() {
     if (rec < 0) return;
     std::lock_guard<std::mutex> lk(g_prof.mu);
     cudaEventRecord(g_prof.recs[rec].b, s);
+    rec = -1;
   }
+  ~ProfScope() { end(); }
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
 };
 
 inline cudaStream_t S(ssd_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -374,6 +383,8 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
     return enqueue_tail(c, q, c.B, vec, c.stream) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(ds->mu);
+  ProfScope pass;  // the concurrent statistics pass as one phase (one slice)
+  if (S == 1) pass.begin("stats_pass", c.stream, false);
   cudaError_t e = cudaEventRecord(ds->ev[0], c.stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->s1, ds->ev[0], 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->s2, ds->ev[0], 0);
@@ -386,6 +397,7 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
     if (e == cudaSuccess) e = cudaEventRecord(ds->ev[2 + 2 * i], ds->s2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[1 + 2 * i], 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[2 + 2 * i], 0);
+    pass.end();
     if (e == cudaSuccess) e = enqueue_tail(c, q, b1 - b0, vec, c.stream);
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;

@@ -34,10 +34,12 @@ struct StatsSmem {
 
 constexpr int kMaxF = 16;
 
-// Top-f scratch: the two best elements of every thread and the selection.
+// Top-f scratch: every thread's maximum, the warps' largest second values
+// and the selection.
 struct TopfScratch {
   float cv[kThreads];
   int ci[kThreads];
+  float w2[kWarps];
   float sv[kMaxF];
   int si[kMaxF];
   float bv[kWarps];
@@ -69,30 +71,49 @@ __device__ __forceinline__ void best_after(const typename Tag::Elem* row, int lo
   }
 }
 
+// First half of the top-f selection, before the block reduction of the
+// statistics (whose barrier publishes it): each thread posts its maximum as a
+// candidate (none if masked) and each warp the largest "second value" of its
+// threads -- m2, every element of a thread except its maximum is at most m2;
+// a thread that saw a NaN posts NaN, which sends the CTA to the exact path.
+__device__ __forceinline__ void topf_post(const ScanState& st, const int* msk, int M,
+                                          TopfScratch& ts) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool ok = st.idx != kIdxNone && !is_masked(st.idx, msk, M);
+  ts.cv[tid] = ok ? st.m : -INFINITY;
+  ts.ci[tid] = ok ? st.idx : kIdxNone;
+  float w2 = st.nan ? NAN : st.m2;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) w2 = max_nan(w2, __shfl_xor_sync(kFull, w2, o));
+  if (lane == 0) ts.w2[tid >> 5] = w2;
+}
+
 // Top f of the CTA's elements (logit descending, index ascending, masked
-// tokens skipped), certified: the candidates are the threads' maxima, and
-// every other element of a thread is at most that thread's second largest
-// value m2.  If every m2 is below the f-th pick nothing can be missing;
-// otherwise (rare; ties included) the exact selection is redone over [lo, hi)
-// by f rounds of a block-wide arg-max.
+// tokens and NaN skipped), certified: with M2 the largest second value of
+// any thread, every element that is not a thread maximum is at most M2, so
+// if at least f unmasked thread maxima exceed M2 the top f are thread
+// maxima and warp 0 picks them from the 256 posted candidates while the
+// other warps leave.  Otherwise (rare; ties included) the exact selection is
+// redone over [lo, hi) by f rounds of a block-wide arg-max.  Needs
+// topf_post and a barrier before it.
 template <typename Tag, bool VEC>
 __device__ void topf_select(const StatsParams& p, const ScanState& st,
                             const typename Tag::Elem* row, int lo, int hi, const int* msk,
                             TopEntry* out_top, int n_slots, TopfScratch& ts) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int f = p.f, M = p.M;
-  {
-    const bool ok = st.idx != kIdxNone && !is_masked(st.idx, msk, M);
-    ts.cv[tid] = ok ? st.m : -INFINITY;
-    ts.ci[tid] = ok ? st.idx : kIdxNone;
-  }
-  __syncthreads();
-  if (warp == 0) {
+  float M2 = ts.w2[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) M2 = max_nan(M2, ts.w2[w]);
+  const bool cand = ts.ci[tid] != kIdxNone && ts.cv[tid] > M2;  // false when M2 is NaN
+  if (__syncthreads_count(cand) >= f) {
+    if (warp != 0) return;
     float pv = INFINITY;
     int pi = -1;
     for (int r = 0; r < f; ++r) {
       float bv = -INFINITY;
       int bi = kIdxNone;
+#pragma unroll
       for (int q = lane; q < kThreads; q += 32) {
         const float v = ts.cv[q];
         const int i = ts.ci[q];
@@ -109,46 +130,44 @@ __device__ void topf_select(const StatsParams& p, const ScanState& st,
       pv = bv;
       pi = bi;
     }
+    __syncwarp();
+    // the group's list goes to its first chunk slot; the other slots of the
+    // group get empty entries, which rank last in the merge
+    for (int q = lane; q < n_slots * f; q += 32) {
+      const int slot = q / f, r = q % f;
+      out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
+      out_top[q].i = slot == 0 ? ts.si[r] : kIdxNone;
+    }
+    return;
   }
-  __syncthreads();
-  const float fv = ts.sv[f - 1];
-  const int fi = ts.si[f - 1];
-  // (a thread whose max is masked holds its best unmasked element at or
-  // below m2, so the same test covers it; with fewer than f picks the exact
-  // path always runs)
-  const bool flag = fi == kIdxNone || !(st.m2 < fv);
-  if (__syncthreads_or(flag)) {
-    float pv = INFINITY;
-    int pi = -1;
-    for (int r = 0; r < f; ++r) {
-      float bv;
-      int bi;
-      best_after<Tag, VEC>(row, lo, hi, pv, pi, msk, M, bv, bi);
-      warp_argmax(bv, bi);
-      if (lane == 0) {
-        ts.bv[warp] = bv;
-        ts.bi[warp] = bi;
-      }
-      __syncthreads();
-      bv = ts.bv[0];
-      bi = ts.bi[0];
-      for (int w = 1; w < kWarps; ++w)
-        if (ranks_before(ts.bv[w], ts.bi[w], bv, bi)) {
-          bv = ts.bv[w];
-          bi = ts.bi[w];
-        }
-      __syncthreads();
-      if (tid == 0) {
-        ts.sv[r] = bv;
-        ts.si[r] = bi;
-      }
-      pv = bv;
-      pi = bi;
+  float pv = INFINITY;
+  int pi = -1;
+  for (int r = 0; r < f; ++r) {
+    float bv;
+    int bi;
+    best_after<Tag, VEC>(row, lo, hi, pv, pi, msk, M, bv, bi);
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      ts.bv[warp] = bv;
+      ts.bi[warp] = bi;
     }
     __syncthreads();
+    bv = ts.bv[0];
+    bi = ts.bi[0];
+    for (int w = 1; w < kWarps; ++w)
+      if (ranks_before(ts.bv[w], ts.bi[w], bv, bi)) {
+        bv = ts.bv[w];
+        bi = ts.bi[w];
+      }
+    __syncthreads();
+    if (tid == 0) {
+      ts.sv[r] = bv;
+      ts.si[r] = bi;
+    }
+    pv = bv;
+    pi = bi;
   }
-  // the group's list goes to its first chunk slot; the other slots of the
-  // group get empty entries, which rank last in the merge
+  __syncthreads();
   for (int q = tid; q < n_slots * f; q += kThreads) {
     const int slot = q / f, r = q % f;
     out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
@@ -191,6 +210,7 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
       }
     }
   }
+  if constexpr (TOPF) topf_post(st, sm.mask, p.M, *ts);
   block_stats_write(st, c, DO_EXP, sm.m, sm.s, sm.i, sm.n, out_part);
   if constexpr (TOPF) topf_select<Tag, VEC>(p, st, row, lo, hi, sm.mask, out_top, n_slots, *ts);
 }
