@@ -138,6 +138,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(ms, world, device=None):
+    """The largest per-rank time; every rank receives it (an all-reduce MAX
+    over the default process group when world > 1)."""
+    if world == 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(B, world, ms_max, steps):
+    """Whole-job rows per second: every rank verifies B rows per step, and the
+    job takes as long as its slowest rank."""
+    return world * B / (ms_max / 1e3 / steps)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -252,12 +270,9 @@ def gpu_arm(args):
     prof = ssd.profile_end()
     clock = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     ms_step = ms_max / args.steps
-    value = world * w.B / (ms_max / 1e3 / args.steps)
+    value = job_throughput(w.B, world, ms_max, args.steps)
 
     # end to end through the public API with host buffers
     e2e = e2e_run(ssd, w, inp, step, dev, max(3, min(args.steps, 40)), world)

@@ -77,7 +77,7 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 #define SSD_DEVERR_BAD_LOGITS 0x2      /* NaN (or +inf / all -inf at T>0) */
 #define SSD_DEVERR_BAD_TOKEN 0x4       /* draft token outside [0, V): -2  */
 #define SSD_DEVERR_CACHE_FULL 0x8      /* insert found no free slot       */
-#define SSD_DEVERR_TIMEOUT 0x10        /* a bounded wait on a copy ran out */
+#define SSD_DEVERR_TIMEOUT 0x10        /* reserved: a bounded device wait ran out */
 
 /* Sentinels written to accept_len. */
 #define SSD_ROW_INVALID (-1)

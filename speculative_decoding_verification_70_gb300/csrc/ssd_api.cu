@@ -12,14 +12,10 @@
 #include "../../include/ssd.h"
 #include "ssd_layout.h"
 
-#ifndef SSD_TOPF_STAGED
-#define SSD_TOPF_STAGED 0
-#endif
 
 namespace ssd {
 cudaError_t launch_stats_rows(const StatsParams& p, int B, int dtype, bool vec, int r0, int rows,
                               bool topf, cudaStream_t s);
-cudaError_t launch_stats_topf(const StatsParams& p, int B, int dtype, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
@@ -187,13 +183,6 @@ cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaS
     return e;
   }
   ProfScope ps("stats_topf", s_topf);
-#if SSD_TOPF_STAGED
-  if (vec) {  // chunks staged into shared memory by bulk copies
-    StatsParams p = sp;
-    p.r0 = sp.Pz;
-    return launch_stats_topf(p, B, dtype, s_topf);
-  }
-#endif
   StatsParams pt = sp;
   pt.G = 1;
   while (pt.G < 4 && static_cast<long long>(B) * sp.Pdf * ((sp.C + 2 * pt.G - 1) / (2 * pt.G)) >= 2432)
@@ -344,7 +333,8 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   rp.rmass = reinterpret_cast<long long*>(wsp(c.ws, L.rmass)) + static_cast<size_t>(b0) * C;
   rp.racc = reinterpret_cast<long long*>(wsp(c.ws, L.racc)) + static_cast<size_t>(b0) * C * 2;
   rp.amb_cnt = reinterpret_cast<int*>(wsp(c.ws, L.amb_cnt)) + b0;
-  rp.amb_idx = reinterpret_cast<int*>(wsp(c.ws, L.amb_idx)) + static_cast<size_t>(b0) * kAmbCap;
+  rp.amb_cap = amb_cap(c.V);
+  rp.amb_idx = reinterpret_cast<int*>(wsp(c.ws, L.amb_idx)) + static_cast<size_t>(b0) * rp.amb_cap;
   rp.out_tok = fp.out_tok;
   fp.amb_cnt = rp.amb_cnt;
   return q;
@@ -560,6 +550,7 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
   rp.racc = reinterpret_cast<long long*>(wsp(ws, L.racc));
   rp.amb_cnt = reinterpret_cast<int*>(wsp(ws, L.amb_cnt));
   rp.amb_idx = reinterpret_cast<int*>(wsp(ws, L.amb_idx));
+  rp.amb_cap = amb_cap(V);
   rp.out_tok = out_tok;
   return cuda_status(run_residual(rp, B, dtype == SSD_BF16 ? 1 : 0, vec, S(stream)));
 }

@@ -8,7 +8,9 @@
 namespace ssd {
 
 constexpr int kMaxMask = 64;        // masked tokens per (b, position)
-constexpr int kAmbCap = 2048;       // ambiguous-sign elements kept per row (draw)
+constexpr int kAmbCap = 2048;       // ambiguous-sign elements kept per row (draw), at most
+                                    // V (amb_cap(V) below)
+constexpr int kMaxGridBatch = 65535;  // batch rows per launch (grid y / z limit)
 constexpr int kMaxChunkBytes = 32768;  // a chunk fits one shared-memory stage
 
 // Partial statistics of one chunk of one logit row.
@@ -68,6 +70,7 @@ struct StatsParams {
   int V, C, CH, R;     // R: rows per batch row
   int Rp;              // row pitch of part[] (>= R)
   int r0;              // first row of this launch
+  int b0;              // first batch row of this launch (grids hold <= 65535)
   int G;               // chunks per CTA in the plain statistics kernel
   PartStat* part;      // [B][Rp][C]
   TopEntry* topk;      // [B][Pdf][C][f]
@@ -109,13 +112,16 @@ struct ResidualParams {
   long long* rmass;    // [B][C]
   long long* racc;     // [B][C][2]
   int* amb_cnt;        // [B]
-  int* amb_idx;        // [B][kAmbCap]
+  int* amb_idx;        // [B][amb_cap]
+  int amb_cap;         // ambiguous elements kept per row
+  int b0;              // first batch row of this launch (grids hold <= 65535)
   int32_t* out_tok;    // [B][k+1]
 };
 
 struct SoftmaxParams {
   const void* L;
   int dtype, rows, V, C, CH;
+  int r0;              // first row of this launch (grids hold <= 65535 rows)
   const float* T;
   const PartStat* part;
   RowStat* rowstat;
@@ -199,6 +205,9 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Ambiguous-sign elements kept per row of the draw: a row holds at most V.
+inline int amb_cap(int V) { return V < kAmbCap ? V : kAmbCap; }
+
 inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   WsLayout L;
   L.B = B;
@@ -218,7 +227,7 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.rmass = off;                    off = align256(off + sizeof(long long) * B * C);
   L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * C);
   L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
-  L.amb_idx = off;                  off = align256(off + sizeof(int) * B * kAmbCap);
+  L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
   L.total = off;
   return L;

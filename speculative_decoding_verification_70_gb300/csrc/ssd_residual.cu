@@ -168,7 +168,7 @@ __device__ __forceinline__ void pass_element(float z, float d, int idx, bool res
                                              const RowCtx& cx, const float2* tab, float& sah,
                                              float& sal, float& sbh, float& sbl, float& ah,
                                              float& al, float& bh, float& bl, int* amb_cnt,
-                                             int* amb_idx) {
+                                             int* amb_idx, int amb_cap) {
   float xh, xl, a_h, a_l;
   arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
   exp2_df(xh, xl, tab, a_h, a_l);
@@ -189,7 +189,7 @@ __device__ __forceinline__ void pass_element(float z, float d, int idx, bool res
     df_acc(bh, bl, b_h, b_l);
   } else if (diff >= -lim && (a1 > 0.f || rb > 0.f)) {
     const int q = atomicAdd(amb_cnt, 1);
-    if (q < kAmbCap) amb_idx[q] = idx;
+    if (q < amb_cap) amb_idx[q] = idx;
   }
 }
 
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
-  const int c = blockIdx.x, b = blockIdx.y;
+  const int c = blockIdx.x, b = blockIdx.y + p.b0;
   BState bs;
   RowCtx cx;
   load_exp2_table(tab);
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
   const int hi = min(chi, lo + p.E);
   int* amb_cnt = p.amb_cnt + b;
-  int* amb_idx = p.amb_idx + static_cast<int64_t>(b) * kAmbCap;
+  int* amb_idx = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
   float sah = 0.f, sal = 0.f, sbh = 0.f, sbl = 0.f, ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
   constexpr int kV = Tag::kVec;
   int i = lo;
@@ -223,12 +223,12 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
 #pragma unroll
       for (int e = 0; e < kV; ++e)
         pass_element(z[e], resid ? d[e] : 0.f, i + e, resid, cx, tab, sah, sal, sbh, sbl, ah, al,
-                     bh, bl, amb_cnt, amb_idx);
+                     bh, bl, amb_cnt, amb_idx, p.amb_cap);
     }
   }
   for (; i < hi; ++i)
     pass_element(Tag::load1(zr + i), resid ? Tag::load1(dr + i) : 0.f, i, resid, cx, tab, sah,
-                 sal, sbh, sbl, ah, al, bh, bl, amb_cnt, amb_idx);
+                 sal, sbh, sbl, ah, al, bh, bl, amb_cnt, amb_idx, p.amb_cap);
   long long tz = block_sum_i64(df_to_fix(sah, sal, kFixMass), sm);
   long long td = 0, ta = 0, tb = 0;
   if (resid) {
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams 
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
-  const int c = blockIdx.x, b = blockIdx.y;
+  const int c = blockIdx.x, b = blockIdx.y + p.b0;
   // only rows whose ambiguous list overflowed need the direct mass
-  if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= kAmbCap) return;
+  if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= p.amb_cap) return;
   BState bs;
   RowCtx cx;
   load_exp2_table(tab);
@@ -388,9 +388,9 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
   const typename Tag::Elem *zr, *dr;
   row_ptrs<Tag>(p, b, bs.n, zr, dr);
   const int n_amb = resid_row ? p.amb_cnt[b] : 0;
-  const bool split = resid_row && n_amb <= kAmbCap;
+  const bool split = resid_row && n_amb <= p.amb_cap;
   if (split) {
-    const int* amb = p.amb_idx + static_cast<int64_t>(b) * kAmbCap;
+    const int* amb = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
     for (int q = tid; q < n_amb; q += kThreads) {
       const int i = amb[q];
       float wh, wl;
@@ -484,14 +484,27 @@ __global__ void residual_prep_kernel(PrepParams p) {
     }                                                                               \
   } while (0)
 
-cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
-  SSD_DISPATCH(residual_norm_kernel, dim3(p.C, B));
-  return cudaGetLastError();
+// grids (C, batch rows): at most 65535 batch rows per launch
+cudaError_t launch_residual_norm(const ResidualParams& p0, int B, int dtype, bool vec, cudaStream_t s) {
+  ResidualParams p = p0;
+  for (int b0 = 0; b0 < B; b0 += kMaxGridBatch) {
+    p.b0 = b0;
+    SSD_DISPATCH(residual_norm_kernel, dim3(p.C, B - b0 < kMaxGridBatch ? B - b0 : kMaxGridBatch));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-cudaError_t launch_residual_mass(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
-  SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B));
-  return cudaGetLastError();
+cudaError_t launch_residual_mass(const ResidualParams& p0, int B, int dtype, bool vec, cudaStream_t s) {
+  ResidualParams p = p0;
+  for (int b0 = 0; b0 < B; b0 += kMaxGridBatch) {
+    p.b0 = b0;
+    SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B - b0 < kMaxGridBatch ? B - b0 : kMaxGridBatch));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {

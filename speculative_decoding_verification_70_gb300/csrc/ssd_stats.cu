@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : 6)
   // for the group, written to the group's first partial; the others get the
   // identity record (m = -inf, s = 0, no index).
   const int G = p.G;
-  const int c = blockIdx.x * G, r = blockIdx.y + p.r0, b = blockIdx.z;
+  const int c = blockIdx.x * G, r = blockIdx.y + p.r0, b = blockIdx.z + p.b0;
   const int lo = c * p.CH;
   const int hi = min(p.V, lo + G * p.CH);
   const int n_slots = min(G, p.C - c);
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreads) softmax_finalize_kernel(SoftmaxParam
 // grid: (C, rows): p_v = 2^((z_v - m) c) / S, one-hot for greedy rows
 template <typename Tag>
 __global__ void __launch_bounds__(kThreads) softmax_probs_kernel(SoftmaxParams p) {
-  const int c = blockIdx.x, r = blockIdx.y;
+  const int c = blockIdx.x, r = blockIdx.y + p.r0;
   const int lo = c * p.CH, hi = min(p.V, lo + p.CH);
   const RowStat st = p.rowstat[r];
   const float T = p.T[r];
@@ -582,11 +582,17 @@ __global__ void __launch_bounds__(kThreads) softmax_probs_kernel(SoftmaxParams p
 // Launchers (host).
 // ---------------------------------------------------------------------------
 template <typename Tag, bool VEC>
-static cudaError_t launch_stats_t(const StatsParams& p, int B, int rows, bool topf, cudaStream_t s) {
-  dim3 grid((p.C + p.G - 1) / p.G, rows, B);
-  if (topf) stats_kernel<Tag, VEC, true><<<grid, kThreads, 0, s>>>(p);
-  else stats_kernel<Tag, VEC, false><<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+static cudaError_t launch_stats_t(const StatsParams& p0, int B, int rows, bool topf, cudaStream_t s) {
+  StatsParams p = p0;
+  for (int b0 = 0; b0 < B; b0 += kMaxGridBatch) {
+    p.b0 = b0;
+    dim3 grid((p.C + p.G - 1) / p.G, rows, B - b0 < kMaxGridBatch ? B - b0 : kMaxGridBatch);
+    if (topf) stats_kernel<Tag, VEC, true><<<grid, kThreads, 0, s>>>(p);
+    else stats_kernel<Tag, VEC, false><<<grid, kThreads, 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Rows [r0, r0 + rows) of every batch row; topf selects the variant that
@@ -613,11 +619,17 @@ cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s) {
-  dim3 grid(p.C, p.rows);
-  if (p.dtype == 1) softmax_probs_kernel<BF16Tag><<<grid, kThreads, 0, s>>>(p);
-  else softmax_probs_kernel<F32Tag><<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_softmax_probs(const SoftmaxParams& p0, cudaStream_t s) {
+  SoftmaxParams p = p0;
+  for (int r0 = 0; r0 < p0.rows; r0 += kMaxGridBatch) {
+    p.r0 = r0;
+    dim3 grid(p.C, p0.rows - r0 < kMaxGridBatch ? p0.rows - r0 : kMaxGridBatch);
+    if (p.dtype == 1) softmax_probs_kernel<BF16Tag><<<grid, kThreads, 0, s>>>(p);
+    else softmax_probs_kernel<F32Tag><<<grid, kThreads, 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace ssd

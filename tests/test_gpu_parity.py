@@ -73,6 +73,23 @@ def test_softmax_temp_parity(gpu_lib, V, dtype):
     assert err & gpu_lib.DEVERR_BAD_TEMPERATURE and err & gpu_lib.DEVERR_BAD_LOGITS
 
 
+def test_softmax_temp_more_rows_than_one_grid(gpu_lib):
+    """70000 rows: the launches loop over batches of 65535 grid rows."""
+    g = torch.Generator().manual_seed(70000)
+    rows, V = 70000, 24
+    z = torch.randn((rows, V), generator=g) * 2
+    T = torch.rand(rows, generator=g) + 0.5
+    T[::7] = 0.0
+    r = gpu_lib.ssd_softmax_temp(z.to(DEV), T.to(DEV))
+    assert torch.equal(r["row_argmax"].cpu().long(), torch.argmax(z, dim=1))
+    assert torch.equal(r["row_max"].cpu(), z.max(dim=1).values)
+    sel = np.r_[0:50, 65500:65600, rows - 50:rows]
+    ref = oracle.softmax_temp(z[sel], T[sel])
+    gp = to_np(r["probs"])[sel].astype(np.float64)
+    assert np.max(np.abs(gp - ref["probs"])) <= 1e-5
+    assert gpu_lib.get_device_error(r["ws"]) == 0
+
+
 # ---------------------------------------------------------------------------
 CASES = [
     ("tiny", {}, None, 0), ("tiny", {"B": 16}, None, 3),
