@@ -115,6 +115,7 @@ struct ResidualParams {
   int* amb_idx;        // [B][amb_cap]
   int amb_cap;         // ambiguous elements kept per row
   int b0;              // first batch row of this launch (grids hold <= 65535)
+  int B;               // batch rows of this call (row-strided kernels)
   int32_t* out_tok;    // [B][k+1]
 };
 

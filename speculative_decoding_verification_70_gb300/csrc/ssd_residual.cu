@@ -245,29 +245,36 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   }
 }
 
-// grid (C, B)
+// Direct per-chunk residual masses (2^60 units) of the rows whose ambiguous
+// list overflowed (p ~ q on more than amb_cap elements, e.g. bf16 drafts
+// that equal the target on many logits).  Grid (C, at most 128 row slots):
+// each CTA walks the batch rows slot, slot + 128, ..., so the launch costs a
+// few microseconds when no row overflowed.
+constexpr int kMassRowSlots = 128;
+
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams p) {
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
-  const int c = blockIdx.x, b = blockIdx.y + p.b0;
-  // only rows whose ambiguous list overflowed need the direct mass
-  if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= p.amb_cap) return;
-  BState bs;
-  RowCtx cx;
+  const int c = blockIdx.x;
   load_exp2_table(tab);
-  load_ctx(p, b, bs, cx, &s_cx, true);
-  const typename Tag::Elem *zr, *dr;
-  row_ptrs<Tag>(p, b, bs.n, zr, dr);
-  const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
-  const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
-  const int hi = min(chi, lo + p.E);
-  float h, l;
-  range_sum<Tag, VEC, Q_RESID>(zr, dr, lo, hi, cx, tab, h, l);
-  long long fw = df_to_fix(h, l, kFixResidual);
-  long long tw = block_sum_i64(fw, sm);
-  if (threadIdx.x == 0) p.rmass[static_cast<int64_t>(b) * p.C + c] = tw;
+  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+    if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= p.amb_cap) continue;
+    BState bs;
+    RowCtx cx;
+    load_ctx(p, b, bs, cx, &s_cx, true);  // holds a __syncthreads()
+    const typename Tag::Elem *zr, *dr;
+    row_ptrs<Tag>(p, b, bs.n, zr, dr);
+    const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
+    const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
+    const int hi = min(chi, lo + p.E);
+    float h, l;
+    range_sum<Tag, VEC, Q_RESID>(zr, dr, lo, hi, cx, tab, h, l);
+    long long fw = df_to_fix(h, l, kFixResidual);
+    long long tw = block_sum_i64(fw, sm);  // its barriers also retire s_cx
+    if (threadIdx.x == 0) p.rmass[static_cast<int64_t>(b) * p.C + c] = tw;
+  }
 }
 
 // floor(total * u) exactly, u a binary32 in [0, 1).
@@ -498,13 +505,9 @@ cudaError_t launch_residual_norm(const ResidualParams& p0, int B, int dtype, boo
 
 cudaError_t launch_residual_mass(const ResidualParams& p0, int B, int dtype, bool vec, cudaStream_t s) {
   ResidualParams p = p0;
-  for (int b0 = 0; b0 < B; b0 += kMaxGridBatch) {
-    p.b0 = b0;
-    SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B - b0 < kMaxGridBatch ? B - b0 : kMaxGridBatch));
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  p.B = B;
+  SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B < kMassRowSlots ? B : kMassRowSlots));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
