@@ -192,6 +192,44 @@ class Step:
         return o
 
 
+def b1_latency(ssd, W, dev, reps=300):
+    """Latency of the B = 1 SSD step (ssd_fork: k=7, f=3, V=128256 bf16,
+    T=1; verify + forked recovery + cache clear/insert/lookup), launched
+    eagerly and replayed as a captured CUDA graph; microseconds per step."""
+    import torch
+    w = W.workload("ssd_fork")
+    inp = W.make_inputs(w, device=dev, seed=W.default_seed("ssd_fork"))
+    step = Step(ssd, w, inp, dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    eager = timed(step)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    graph = timed(g.replay)
+    step.cache.close()
+    return {"workload": "ssd_fork: B=1 k=7 f=3 V=128256 bf16, T=1, verify+fork+cache step",
+            "eager_us": round(eager, 2), "graph_us": round(graph, 2)}
+
+
 def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
     """Time the oracle (as it stands, one host thread) on a bounded sample of
     the batch rows: verify_recover + forked_topf + the dict cache."""
@@ -313,6 +351,8 @@ def gpu_arm(args):
                        "l2": "inputs (%.2f GB per step) larger than L2" % (nbytes / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "gpu_launches": launches, "roofline": roof, "clocks": clock, "e2e": e2e}
+    if rank == 0 and world == 1:
+        line["latency_b1"] = b1_latency(ssd, W, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
     if rank == 0:

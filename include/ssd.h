@@ -94,6 +94,18 @@ SSD_API const char *ssd_status_string(ssd_status s);
 SSD_API int ssd_version(void);
 
 /*
+ * Streams, graphs, batch size.  Every call enqueues work on the caller's
+ * stream and returns: no device allocation, no host synchronisation (except
+ * the error-word reads, which say so).  A batched verify (B >= 32) runs its
+ * target-row and draft-row statistics on two internal streams forked from
+ * and joined back to the caller's stream by events; the streams and events
+ * are created on the first such call on a device.  Calls can therefore be
+ * captured into a CUDA graph (make one batched call on the device before
+ * capturing).  B may exceed 65535: kernels launch in grids of 65535 batch
+ * rows.
+ */
+
+/*
  * Workspace bytes for ssd_verify / ssd_verify_fork / ssd_sample_residual /
  * ssd_forked_recovery on batch B, draft length k, vocabulary V and fan-out
  * f (0 if no forked recovery).  Returns 0 for invalid sizes.
@@ -242,9 +254,12 @@ SSD_API ssd_status ssd_verify_fork(const void *Z, int64_t z_bstride, const void 
  * hits and misses).  An open-addressing table on the device mapping the key
  * (b, position, token) to `depth` draft tokens.  Keys compare exactly, so the
  * hash only decides slots, never results.  Inserts apply in input order (the
- * last duplicate wins, also across calls).  Probing is bounded by the
- * capacity: an insert that finds no slot is dropped and sets
- * SSD_DEVERR_CACHE_FULL.  Limits: b < 2^24, position < 256, token >= 0.
+ * last duplicate wins, also across calls).  The call order is counted on the
+ * device, so inserts into one cache must be ordered on one stream (or joined
+ * by events); an insert captured in a CUDA graph keeps the rule on every
+ * replay.  Probing is bounded by the capacity: an insert that finds no slot
+ * is dropped and sets SSD_DEVERR_CACHE_FULL.  Limits: b < 2^24,
+ * position < 256, token >= 0.
  */
 typedef struct ssd_spec_cache ssd_spec_cache;
 

@@ -34,7 +34,6 @@ using namespace ssd;
 
 struct ssd_spec_cache {
   CacheView view;
-  unsigned long long calls;
   int device;
 };
 
@@ -615,11 +614,18 @@ ssd_status ssd_spec_cache_create(int capacity, int depth, ssd_spec_cache** out) 
   cudaError_t e = cudaMalloc(&c->view.keys, kb);
   if (e == cudaSuccess) e = cudaMalloc(&c->view.winner, kb);
   if (e == cudaSuccess) e = cudaMalloc(&c->view.payload, pb);
-  if (e == cudaSuccess) e = cudaMalloc(&c->view.err, 16);
+  // one small block: the error word, the write kernel's ticket, the call counter
+  void* misc = nullptr;
+  if (e == cudaSuccess) e = cudaMalloc(&misc, 64);
+  if (e == cudaSuccess) {
+    c->view.err = static_cast<int*>(misc);
+    c->view.done = reinterpret_cast<unsigned*>(static_cast<char*>(misc) + 16);
+    c->view.calls = reinterpret_cast<unsigned long long*>(static_cast<char*>(misc) + 32);
+  }
   if (e == cudaSuccess) e = cudaMemset(c->view.keys, 0xff, kb);
   if (e == cudaSuccess) e = cudaMemset(c->view.winner, 0, kb);
   if (e == cudaSuccess) e = cudaMemset(c->view.payload, 0xff, pb);
-  if (e == cudaSuccess) e = cudaMemset(c->view.err, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(misc, 0, 64);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     ssd_spec_cache_destroy(c);
@@ -652,11 +658,9 @@ ssd_status ssd_spec_cache_insert(ssd_spec_cache* c, const int32_t* b, const int3
   if (!c || n < 0) return SSD_ERR_INVALID_ARG;
   if (n == 0) return SSD_OK;
   if (!b || !pos || !tok || !payload) return SSD_ERR_INVALID_ARG;
-  if (c->calls >= 0xffffffffull) return SSD_ERR_INVALID_ARG;
   InsertArgs a;
   memset(&a, 0, sizeof a);
   a.b = b; a.pos = pos; a.tok = tok; a.payload = payload; a.n = n;
-  a.seq = (++c->calls) << 32;
   return cuda_status(cache_insert(c->view, a, S(stream)));
 }
 
@@ -664,11 +668,9 @@ ssd_status ssd_spec_cache_insert_forks(ssd_spec_cache* c, const int32_t* fork_to
                                        int f, const int32_t* payload, ssd_stream_t stream) {
   if (!c || !fork_tok || !payload || B < 1 || P < 1 || P > 256 || f < 1) return SSD_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * P * f > 0x7fffffff) return SSD_ERR_INVALID_ARG;
-  if (c->calls >= 0xffffffffull) return SSD_ERR_INVALID_ARG;
   InsertArgs a;
   memset(&a, 0, sizeof a);
   a.fork_tok = fork_tok; a.P = P; a.f = f; a.payload = payload; a.n = B * P * f;
-  a.seq = (++c->calls) << 32;
   return cuda_status(cache_insert(c->view, a, S(stream)));
 }
 

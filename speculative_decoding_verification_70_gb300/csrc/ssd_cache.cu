@@ -16,7 +16,10 @@
 // (CAS the key into a slot, then atomicMax a 64-bit sequence number
 // call << 32 | input index into the slot's winner word) and write (the input
 // whose sequence number won copies its payload).  The last duplicate, in
-// input order and across calls, wins.
+// input order and across calls, wins.  The call number lives on the device:
+// both kernels read the count of finished inserts, and the write kernel's
+// last CTA (atomic ticket, no waiting) advances it, so an insert captured in
+// a CUDA graph draws a fresh call number on every replay.
 #include <stdint.h>
 
 #include "ssd_device.cuh"
@@ -70,9 +73,14 @@ __device__ __forceinline__ bool insert_key(const InsertArgs& a, int i, unsigned 
   return make_key(b, pos, tok, key);
 }
 
+__device__ __forceinline__ unsigned long long call_seq(const CacheView& c) {
+  return (__ldcg(c.calls) + 1ull) << 32;
+}
+
 __global__ void cache_claim_kernel(CacheView c, InsertArgs a) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= a.n) return;
+  const unsigned long long seq = call_seq(c);
   unsigned long long key;
   if (!insert_key(a, i, key)) return;
   const unsigned mask = static_cast<unsigned>(c.capacity - 1);
@@ -80,7 +88,7 @@ __global__ void cache_claim_kernel(CacheView c, InsertArgs a) {
   for (int probe = 0; probe < c.capacity; ++probe) {
     unsigned long long prev = atomicCAS(&c.keys[h], kEmptyKey, key);
     if (prev == kEmptyKey || prev == key) {
-      atomicMax(&c.winner[h], a.seq | static_cast<unsigned long long>(i));
+      atomicMax(&c.winner[h], seq | static_cast<unsigned long long>(i));
       return;
     }
     h = (h + 1) & mask;
@@ -90,15 +98,26 @@ __global__ void cache_claim_kernel(CacheView c, InsertArgs a) {
 
 __global__ void cache_write_kernel(CacheView c, InsertArgs a) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= a.n) return;
+  const unsigned long long seq = call_seq(c);  // read before this CTA's ticket
   unsigned long long key;
-  if (!insert_key(a, i, key)) return;
-  int s = find_slot(c, key);
-  if (s < 0) return;
-  if (c.winner[s] != (a.seq | static_cast<unsigned long long>(i))) return;
-  const int32_t* src = a.payload + static_cast<int64_t>(i) * c.depth;
-  int32_t* dst = c.payload + static_cast<int64_t>(s) * c.depth;
-  for (int d = 0; d < c.depth; ++d) dst[d] = src[d];
+  if (i < a.n && insert_key(a, i, key)) {
+    const int s = find_slot(c, key);
+    if (s >= 0 && c.winner[s] == (seq | static_cast<unsigned long long>(i))) {
+      const int32_t* src = a.payload + static_cast<int64_t>(i) * c.depth;
+      int32_t* dst = c.payload + static_cast<int64_t>(s) * c.depth;
+      for (int d = 0; d < c.depth; ++d) dst[d] = src[d];
+    }
+  }
+  // the last CTA to finish advances the call counter (every CTA has read it)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(c.done, 1u) == gridDim.x - 1) {
+      *c.done = 0u;
+      *c.calls = seq >> 32;
+      __threadfence();
+    }
+  }
 }
 
 __global__ void cache_lookup_kernel(CacheView c, LookupArgs a) {

@@ -149,7 +149,9 @@ struct CacheView {
   unsigned long long* keys;
   unsigned long long* winner;
   int32_t* payload;
-  int* err;
+  int* err;                  // device error word
+  unsigned long long* calls; // inserts completed so far (device counter)
+  unsigned* done;            // finished CTAs of the running insert's write kernel
   int capacity;
   int depth;
 };
@@ -162,7 +164,6 @@ struct InsertArgs {
   const int32_t* fork_tok;
   int P, f;
   int n;
-  unsigned long long seq;
 };
 
 struct LookupArgs {
