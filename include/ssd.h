@@ -250,6 +250,31 @@ SSD_API ssd_status ssd_verify_fork(const void *Z, int64_t z_bstride, const void 
                            size_t ws_bytes, ssd_stream_t stream);
 
 /*
+ * Variable fan-out ([SUM] get_forked_recovery_tokens_from_logits: selection
+ * by fan-out strategy).  As ssd_forked_recovery / ssd_verify_fork with
+ * F (<= SSD_MAX_F) in place of f, plus
+ *   fanout   : [P] int32 device array, f_j tokens kept at position j
+ *              (clamped to [0, F]).  fork_tok / fork_logit stay [B, P, F]:
+ *              slots f_j .. F-1 of position j hold (-1, -inf), which the
+ *              cache insert skips.  NULL keeps F everywhere.
+ *   ws       : sized with f = F.
+ */
+SSD_API ssd_status ssd_forked_recovery_fanout(const void *L, int64_t l_bstride,
+                                      ssd_dtype dtype, int B, int P, int V, int F,
+                                      const int32_t *fanout, const int32_t *mask,
+                                      int M, int32_t *fork_tok, float *fork_logit,
+                                      void *ws, size_t ws_bytes, ssd_stream_t stream);
+SSD_API ssd_status ssd_verify_fork_fanout(const void *Z, int64_t z_bstride,
+                                  const void *D, int64_t d_bstride, ssd_dtype dtype,
+                                  int B, int k, int V, const int32_t *x,
+                                  const float *T, const float *u_acc,
+                                  int32_t *accept_len, float *p_at_x, float *q_at_x,
+                                  const float *u_smp, int32_t *out_tok, int F,
+                                  const int32_t *fanout, const int32_t *mask, int M,
+                                  int32_t *fork_tok, float *fork_logit, void *ws,
+                                  size_t ws_bytes, ssd_stream_t stream);
+
+/*
  * Speculation cache ([SSD] roadmap: the speculation cache; [SUM] cache
  * hits and misses).  An open-addressing table on the device mapping the key
  * (b, position, token) to `depth` draft tokens.  Keys compare exactly, so the

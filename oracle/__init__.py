@@ -164,9 +164,15 @@ def verify_recover(Z, D, x, T, u_acc, u_smp, f64_uniforms: bool = False
     return {"accept_len": acc, "p_at_x": pax, "q_at_x": qax, "out_tok": out}
 
 
-def forked_topf(L, f: int, mask=None) -> Dict[str, np.ndarray]:
+def forked_topf(L, f: int, mask=None, fanout=None) -> Dict[str, np.ndarray]:
     """Top-f forked recovery tokens per (b, j) of L [B, P, V], skipping the
-    tokens listed in mask [B, P, M] (-1 = no entry)."""
+    tokens listed in mask [B, P, M] (-1 = no entry).
+
+    fanout [P] (variable fan-out, "tanishqkumar/ssd" summary, module notes:
+    forked recovery tokens selected by fan-out strategy): position j keeps
+    f_j = min(max(fanout[j], 0), f) tokens -- by definition the first f_j of
+    its top-f list, since the order is total -- and pads the rest with
+    (-1, -inf)."""
     l, dt = _logits(L)
     B, P, V = l.shape
     if mask is None:
@@ -178,6 +184,11 @@ def forked_topf(L, f: int, mask=None) -> Dict[str, np.ndarray]:
     _check(_load().oracle_forked_topf(_ptr(l), P * V, dt, B, P, V, f,
                                       _ptr(mask) if M > 0 else None, M,
                                       _ptr(tok), _ptr(lg)), "forked_topf")
+    if fanout is not None:
+        keep = np.clip(np.asarray(fanout, dtype=np.int64).reshape(P), 0, f)
+        drop = np.arange(f)[None, :] >= keep[:, None]          # [P, f]
+        tok[:, drop] = -1
+        lg[:, drop] = -np.inf
     return {"fork_tok": tok, "fork_logit": lg}
 
 

@@ -46,6 +46,10 @@ SIGNATURES = [
     ("ssd_forked_recovery", _I, [_P, _L, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _Z, _P]),
     ("ssd_verify_fork", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                              _P, _I, _P, _I, _P, _P, _P, _Z, _P]),
+    ("ssd_forked_recovery_fanout", _I, [_P, _L, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P,
+                                        _Z, _P]),
+    ("ssd_verify_fork_fanout", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _I, _P, _P, _I, _P, _P, _P, _Z, _P]),
     ("ssd_spec_cache_create", _I, [_I, _I, _P]),
     ("ssd_spec_cache_destroy", None, [_P]),
     ("ssd_spec_cache_clear", _I, [_P, _P]),
@@ -257,10 +261,12 @@ def ssd_sample_residual(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: to
 
 
 def ssd_forked_recovery(L: torch.Tensor, f: int, mask: Optional[torch.Tensor] = None, *,
+                        fanout: Optional[torch.Tensor] = None,
                         ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
                         stream=None) -> Dict[str, torch.Tensor]:
     """Top-f forked recovery tokens per (b, j) of L [B,P,V], skipping the
-    tokens in mask [B,P,M] (int32, -1 = none)."""
+    tokens in mask [B,P,M] (int32, -1 = none).  fanout [P] int32 (device)
+    keeps f_j <= f tokens at position j."""
     lib = load_library()
     B, P, V = L.shape
     dev = L.device
@@ -274,20 +280,30 @@ def ssd_forked_recovery(L: torch.Tensor, f: int, mask: Optional[torch.Tensor] = 
     if "fork_tok" not in out:
         out["fork_tok"] = torch.empty((B, P, f), dtype=torch.int32, device=dev)
         out["fork_logit"] = torch.empty((B, P, f), dtype=torch.float32, device=dev)
-    _check("ssd_forked_recovery", lib.ssd_forked_recovery(
-        _dev(L, "L"), P * V, _dtype_code(L), B, P, V, f, _opt(mask, "mask"), M,
-        _dev(out["fork_tok"], "fork_tok"), _dev(out["fork_logit"], "fork_logit"), wp, wn,
-        _stream(stream)))
+    if fanout is None:
+        _check("ssd_forked_recovery", lib.ssd_forked_recovery(
+            _dev(L, "L"), P * V, _dtype_code(L), B, P, V, f, _opt(mask, "mask"), M,
+            _dev(out["fork_tok"], "fork_tok"), _dev(out["fork_logit"], "fork_logit"), wp, wn,
+            _stream(stream)))
+    else:
+        _want(fanout, torch.int32, "fanout")
+        if fanout.numel() != P:
+            raise ValueError("fanout must hold P values")
+        _check("ssd_forked_recovery_fanout", lib.ssd_forked_recovery_fanout(
+            _dev(L, "L"), P * V, _dtype_code(L), B, P, V, f, _dev(fanout, "fanout"),
+            _opt(mask, "mask"), M, _dev(out["fork_tok"], "fork_tok"),
+            _dev(out["fork_logit"], "fork_logit"), wp, wn, _stream(stream)))
     out["ws"] = ws
     return out
 
 
 def ssd_verify_fork(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
                     u_acc: torch.Tensor, u_smp: Optional[torch.Tensor], f: int,
-                    mask: Optional[torch.Tensor] = None, *, ws: Optional[torch.Tensor] = None,
+                    mask: Optional[torch.Tensor] = None, *,
+                    fanout: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                     out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
     """ssd_verify plus the forked recovery over the SSD draft D [B,k+1,V] in
-    one pass over the logits."""
+    one pass over the logits (fanout [k+1] int32: f_j <= f forks at j)."""
     lib = load_library()
     B, kp1, V = Z.shape
     k = kp1 - 1
@@ -302,13 +318,20 @@ def ssd_verify_fork(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.
         ws = new_workspace(workspace_bytes(B, k, V, f), dev)
     wp, wn = _ws_ptr(ws)
     o = _verify_outputs(B, k, dev, out, u_smp is not None, f, kp1)
-    _check("ssd_verify_fork", lib.ssd_verify_fork(
-        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), kp1 * V, _dtype_code(Z), B, k, V,
-        _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
-        _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
-        _dev(o["out_tok"], "out_tok"), f, _opt(mask, "mask"), M,
-        _dev(o["fork_tok"], "fork_tok"), _dev(o["fork_logit"], "fork_logit"), wp, wn,
-        _stream(stream)))
+    head = (_dev(Z, "Z"), kp1 * V, _dev(D, "D"), kp1 * V, _dtype_code(Z), B, k, V,
+            _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
+            _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
+            _dev(o["out_tok"], "out_tok"), f)
+    tail = (_opt(mask, "mask"), M, _dev(o["fork_tok"], "fork_tok"),
+            _dev(o["fork_logit"], "fork_logit"), wp, wn, _stream(stream))
+    if fanout is None:
+        _check("ssd_verify_fork", lib.ssd_verify_fork(*head, *tail))
+    else:
+        _want(fanout, torch.int32, "fanout")
+        if fanout.numel() != kp1:
+            raise ValueError("fanout must hold k+1 values")
+        _check("ssd_verify_fork_fanout",
+               lib.ssd_verify_fork_fanout(*head, _dev(fanout, "fanout"), *tail))
     o["ws"] = ws
     return o
 

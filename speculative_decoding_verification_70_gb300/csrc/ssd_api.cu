@@ -127,6 +127,7 @@ struct VerifyCall {
   int32_t* accept_len; float* p_at_x; float* q_at_x;
   const float* u_smp; int32_t* out_tok;
   int f; const int32_t* mask; int M; int32_t* fork_tok; float* fork_logit;
+  const int32_t* fanout;  // [k+1] device, or null (f at every position)
   void* ws; size_t ws_bytes;
   cudaStream_t stream;
   bool single_stream;  // no internal streams (the no-allocation entry point)
@@ -318,6 +319,7 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   fp.out_tok = c.out_tok ? c.out_tok + static_cast<size_t>(b0) * (c.k + 1) : nullptr;
   fp.fork_tok = fork ? c.fork_tok + static_cast<size_t>(b0) * Pf * c.f : nullptr;
   fp.fork_logit = fork ? c.fork_logit + static_cast<size_t>(b0) * Pf * c.f : nullptr;
+  fp.fanout = fork ? c.fanout : nullptr;
   fp.part = part; fp.topk = topk;
   fp.rowstat = rowstat; fp.bstate = bstate; fp.err = err;
 
@@ -492,21 +494,35 @@ ssd_status ssd_verify(const void* Z, int64_t z_bstride, const void* D, int64_t d
   return run_verify(c, false);
 }
 
-ssd_status ssd_verify_fork(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
-                           ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
-                           const float* u_acc, int32_t* accept_len, float* p_at_x, float* q_at_x,
-                           const float* u_smp, int32_t* out_tok, int f, const int32_t* mask, int M,
-                           int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
-                           ssd_stream_t stream) {
+ssd_status ssd_verify_fork_fanout(const void* Z, int64_t z_bstride, const void* D,
+                                  int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                                  const int32_t* x, const float* T, const float* u_acc,
+                                  int32_t* accept_len, float* p_at_x, float* q_at_x,
+                                  const float* u_smp, int32_t* out_tok, int F,
+                                  const int32_t* fanout, const int32_t* mask, int M,
+                                  int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
+                                  ssd_stream_t stream) {
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
   c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
   c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
   c.u_smp = u_smp; c.out_tok = out_tok;
-  c.f = f; c.mask = mask; c.M = M; c.fork_tok = fork_tok; c.fork_logit = fork_logit;
+  c.f = F; c.mask = mask; c.M = M; c.fork_tok = fork_tok; c.fork_logit = fork_logit;
+  c.fanout = fanout;
   c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
   return run_verify(c, true);
+}
+
+ssd_status ssd_verify_fork(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                           ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
+                           const float* u_acc, int32_t* accept_len, float* p_at_x, float* q_at_x,
+                           const float* u_smp, int32_t* out_tok, int f, const int32_t* mask, int M,
+                           int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
+                           ssd_stream_t stream) {
+  return ssd_verify_fork_fanout(Z, z_bstride, D, d_bstride, dtype, B, k, V, x, T, u_acc,
+                                accept_len, p_at_x, q_at_x, u_smp, out_tok, f, nullptr, mask, M,
+                                fork_tok, fork_logit, ws, ws_bytes, stream);
 }
 
 ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
@@ -557,6 +573,15 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
 ssd_status ssd_forked_recovery(const void* L_, int64_t l_bstride, ssd_dtype dtype, int B, int P,
                                int V, int f, const int32_t* mask, int M, int32_t* fork_tok,
                                float* fork_logit, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  return ssd_forked_recovery_fanout(L_, l_bstride, dtype, B, P, V, f, nullptr, mask, M, fork_tok,
+                                    fork_logit, ws, ws_bytes, stream);
+}
+
+ssd_status ssd_forked_recovery_fanout(const void* L_, int64_t l_bstride, ssd_dtype dtype, int B,
+                                      int P, int V, int f, const int32_t* fanout,
+                                      const int32_t* mask, int M, int32_t* fork_tok,
+                                      float* fork_logit, void* ws, size_t ws_bytes,
+                                      ssd_stream_t stream) {
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!L_ || !fork_tok || !fork_logit || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || P < 1 || P > SSD_MAX_K + 1 || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -585,7 +610,7 @@ ssd_status ssd_forked_recovery(const void* L_, int64_t l_bstride, ssd_dtype dtyp
   fp.D = L_; fp.db = l_bstride; fp.Pds = 0; fp.Pdf = P;
   fp.dtype = dtype == SSD_BF16 ? 1 : 0;
   fp.B = B; fp.k = 0; fp.V = V; fp.C = L.ch.C; fp.R = P; fp.Rp = L.R; fp.f = f;
-  fp.fork_tok = fork_tok; fp.fork_logit = fork_logit;
+  fp.fork_tok = fork_tok; fp.fork_logit = fork_logit; fp.fanout = fanout;
   fp.part = sp.part; fp.topk = sp.topk;
   fp.rowstat = reinterpret_cast<RowStat*>(wsp(ws, L.rowstat));
   fp.bstate = reinterpret_cast<BState*>(wsp(ws, L.bstate));

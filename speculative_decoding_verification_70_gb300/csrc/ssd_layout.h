@@ -92,6 +92,7 @@ struct FinalizeParams {
   int32_t* out_tok;    // may be null
   int32_t* fork_tok;   // may be null
   float* fork_logit;
+  const int32_t* fanout;  // [Pdf] tokens kept per position (null: f everywhere)
   const PartStat* part;
   const TopEntry* topk;
   RowStat* rowstat;    // [B][Rp]

@@ -336,9 +336,10 @@ __device__ void merge_row(const PartStat* parts, int C, float c_hi, float c_lo, 
   rs.flags = (nan ? 1 : 0) | (bad ? 2 : 0);
 }
 
-// Top-f of one fork row from its C chunk lists (one warp).
-__device__ void merge_topf_row(const TopEntry* lists, int C, int f, bool nan, int32_t* tok_out,
-                               float* logit_out, int* heads) {
+// Top-f of one fork row from its C chunk lists (one warp).  Only the first
+// `keep` picks are written; slots keep .. f-1 get (token -1, logit -inf).
+__device__ void merge_topf_row(const TopEntry* lists, int C, int f, int keep, bool nan,
+                               int32_t* tok_out, float* logit_out, int* heads) {
   const int lane = threadIdx.x & 31;
   for (int q = lane; q < C; q += 32) heads[q] = 0;
   __syncwarp();
@@ -366,7 +367,10 @@ __device__ void merge_topf_row(const TopEntry* lists, int C, int f, bool nan, in
     if (bq >= 0 && (bq & 31) == lane) heads[bq] += 1;
     __syncwarp();
     if (lane == 0) {
-      if (nan) {
+      if (r >= keep) {
+        tok_out[r] = -1;
+        logit_out[r] = -INFINITY;
+      } else if (nan) {
         tok_out[r] = -1;
         logit_out[r] = NAN;
       } else if (bq < 0 || bi == kIdxNone) {
@@ -423,7 +427,9 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
     // forked top-f of draft row j
     if (!is_target && j < p.Pdf && p.fork_tok) {
       int64_t o = (static_cast<int64_t>(b) * p.Pdf + j) * p.f;
-      merge_topf_row(p.topk + (static_cast<int64_t>(b) * p.Pdf + j) * p.C * p.f, p.C, p.f,
+      // variable fan-out: f_j tokens at position j, clamped to [0, f]
+      const int keep = p.fanout ? min(max(__ldg(p.fanout + j), 0), p.f) : p.f;
+      merge_topf_row(p.topk + (static_cast<int64_t>(b) * p.Pdf + j) * p.C * p.f, p.C, p.f, keep,
                      (st.flags & 1) != 0, p.fork_tok + o, p.fork_logit + o, heads[warp]);
       if (lane == 0 && (st.flags & 1)) atomicOr(p.err, 0x2);
     }

@@ -169,6 +169,40 @@ def test_forked_recovery_ties_masks_nan(gpu_lib):
         compare_forks(ref, r["fork_tok"], r["fork_logit"], str(dtype))
 
 
+@pytest.mark.parametrize("name,over,fan", [
+    ("ssd_fork", {}, [3, 2, 2, 1, 1, 1, 0, 3]),
+    ("mixed512", {"B": 8}, [4, 4, 3, 3, 2, 2, 1, 0]),
+    ("qwen_b64", {"B": 5}, [0, 1, 2, 3, 1, 2]),
+])
+def test_variable_fanout(gpu_lib, name, over, fan):
+    """Per-position fan-out f_j: standalone and fused calls against the
+    oracle; padded slots are skipped by the cache insert."""
+    w = W.workload(name, **over)
+    inp = W.make_inputs(w, device=DEV, seed=W.default_seed(name) + 40)
+    fanout = torch.tensor(fan, dtype=torch.int32, device=DEV)
+    ref = oracle.forked_topf(inp["D"].cpu(), w.f, inp["mask"].cpu(), fanout=fan)
+    alone = gpu_lib.ssd_forked_recovery(inp["D"], w.f, inp["mask"], fanout=fanout)
+    compare_forks(ref, alone["fork_tok"], alone["fork_logit"], name)
+    fused = gpu_lib.ssd_verify_fork(inp["Z"], inp["D"], inp["x"], inp["T"], inp["u_acc"],
+                                    inp["u_smp"], w.f, inp["mask"], fanout=fanout)
+    compare_forks(ref, fused["fork_tok"], fused["fork_logit"], name)
+    plain = run_verify(gpu_lib, inp, fork_f=w.f)
+    for key in ("accept_len", "out_tok", "p_at_x", "q_at_x"):
+        assert torch.equal(fused[key], plain[key]), key
+    cache = gpu_lib.SpecCache(256 if w.B * (w.k + 1) * w.f < 128 else 4096, 2)
+    pay = torch.arange(w.B * (w.k + 1) * w.f * 2, dtype=torch.int32, device=DEV).reshape(-1, 2)
+    cache.insert_forks(fused["fork_tok"], pay)
+    bb = torch.arange(w.B, device=DEV, dtype=torch.int32).repeat_interleave((w.k + 1) * w.f)
+    pp = torch.arange(w.k + 1, device=DEV, dtype=torch.int32).repeat_interleave(w.f).repeat(w.B)
+    tt = fused["fork_tok"].reshape(-1)
+    valid = tt >= 0
+    look = cache.lookup(bb[valid].contiguous(), pp[valid].contiguous(), tt[valid].contiguous())
+    assert bool((look["hit"] == 1).all())
+    assert torch.equal(look["tok_out"], pay[valid])
+    assert cache.error() == 0
+    cache.close()
+
+
 def test_forked_recovery_constant_rows_use_exact_fallback(gpu_lib):
     """Rows whose logits are all equal put every element at the candidate
     bound, overflowing the candidate buffer: the exact fallback must still

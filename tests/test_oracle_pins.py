@@ -401,6 +401,21 @@ def test_topf_matches_full_sort():
             assert np.array_equal(r["fork_logit"][b, j], L[b, j, order].astype(np.float64))
 
 
+def test_topf_variable_fanout_is_a_prefix_of_the_full_sort():
+    rng = np.random.default_rng(12)
+    B, P, V, F = 3, 5, 40, 4
+    L = rng.integers(-6, 6, size=(B, P, V)).astype(np.float32)   # many ties
+    fan = [4, 0, 2, 7, -1]
+    r = oracle.forked_topf(L, F, fanout=fan)
+    for b in range(B):
+        for j in range(P):
+            keep = min(max(fan[j], 0), F)
+            order = sorted(range(V), key=lambda v: (-L[b, j, v], v))
+            assert r["fork_tok"][b, j, :keep].tolist() == order[:keep]
+            assert (r["fork_tok"][b, j, keep:] == -1).all()
+            assert np.isneginf(r["fork_logit"][b, j, keep:]).all()
+
+
 def test_topf_padding_and_nan():
     L = np.array([[[1.0, 2.0, 3.0], [1.0, np.nan, 0.0]]], dtype=np.float32)
     mask = np.array([[[0, 1], [-1, -1]]], dtype=np.int32)
