@@ -72,6 +72,12 @@ def _load():
     lib.oracle_forked_topf.argtypes = [P, i64, i32, i32, i32, i64, i32, P, i32,
                                        P, P]
     lib.oracle_forked_topf.restype = i32
+    lib.oracle_philox4x32_10.argtypes = [P, P, P]
+    lib.oracle_philox4x32_10.restype = None
+    u32 = ctypes.c_uint32
+    lib.oracle_draft_sample.argtypes = [P, i64, i32, i32, i32, i64, i32, i32, P, u32, u32, u32,
+                                        P, i64]
+    lib.oracle_draft_sample.restype = i32
     _lib = lib
     return lib
 
@@ -190,6 +196,32 @@ def forked_topf(L, f: int, mask=None, fanout=None) -> Dict[str, np.ndarray]:
         tok[:, drop] = -1
         lg[:, drop] = -np.inf
     return {"fork_tok": tok, "fork_logit": lg}
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 of a counter (4 x uint32) and key (2 x uint32)."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(4)
+    k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+    out = np.empty(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def draft_sample(D, T, seed: int, offset: int, row0: int = 0,
+                 rows: Optional[int] = None) -> np.ndarray:
+    """The drafter's tokens for rows [row0, row0 + rows) of D [B, Pd, V]:
+    Gumbel-max draws from softmax(D / T) with Philox4x32-10 uniforms
+    (counter (v / 4, row, b, offset), key = the 64-bit seed); argmax at
+    T == 0; -1 for invalid T or rows.  Returns x [B, rows] int32."""
+    d, dt = _logits(D)
+    B, Pd, V = d.shape
+    rows = Pd - row0 if rows is None else rows
+    T = np.ascontiguousarray(T, dtype=np.float32).reshape(B)
+    x = np.empty((B, rows), dtype=np.int32)
+    _check(_load().oracle_draft_sample(_ptr(d), Pd * V, dt, B, Pd, V, row0, rows, _ptr(T),
+                                       seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF,
+                                       offset & 0xFFFFFFFF, _ptr(x), rows), "draft_sample")
+    return x
 
 
 class SpecCacheOracle:

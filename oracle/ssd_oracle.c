@@ -42,6 +42,12 @@
  *   R7 sentinels: T < 0 or NaN -> accept_len -1; a draft token outside [0,V)
  *      -> accept_len -2; a NaN logit in any row read (or, for T > 0, a +inf
  *      logit or an all -inf row) -> accept_len -1.  Out tokens are then -1.
+ *   R8 draft-side sampling: the drafter's token at T > 0 is the Gumbel-max
+ *      draw argmax_v (z_v / T + G_v), G_v = -ln(-ln u_v), which is exactly a
+ *      draw from softmax(z / T); u_v comes from the counter-based generator
+ *      Philox4x32-10 (Salmon, Moraes, Dror & Shaw 2011) so that both sides
+ *      can regenerate it; ties go to the lowest index; T == 0 takes the
+ *      argmax; invalid T or rows give -1.
  */
 #include <math.h>
 #include <stdint.h>
@@ -430,5 +436,98 @@ int oracle_forked_topf(const void *L, int64_t l_bstride, int dtype, int B,
     }
     free(z);
     free(taken);
+    return ORACLE_OK;
+}
+
+
+/* ------------------------------------------------------------------------
+ * Draft-side sampling (reading R8).
+ * ------------------------------------------------------------------------ */
+
+/* Philox4x32-10, from its published definition (Salmon et al. 2011,
+ * "Parallel random numbers: as easy as 1, 2, 3"): ten rounds of
+ *   (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1,
+ *                        lo(M0 c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the key bumped by the Weyl
+ * constants (0x9E3779B9, 0xBB67AE85) before every round but the first. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniform of element v of draft row i of batch row b: word v mod 4 of
+ * Philox4x32-10 at counter (v / 4, i, b, offset), key (seed_lo, seed_hi),
+ * mapped to u = (w >> 8 + 1/2) / 2^24 in (0, 1).  Returns 1 - u, which is
+ * exact too. */
+static double draft_one_minus_u(uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, int b,
+                                int i, int64_t v)
+{
+    uint32_t ctr[4] = {(uint32_t)(v >> 2), (uint32_t)i, (uint32_t)b, offset};
+    uint32_t key[2] = {seed_lo, seed_hi};
+    uint32_t out[4];
+    oracle_philox4x32_10(ctr, key, out);
+    uint32_t w = out[v & 3] >> 8;
+    return ((double)(16777215u - w) + 0.5) / 16777216.0;
+}
+
+/* x[b * x_bstride + (i - row0)] for draft rows i in [row0, row0 + rows) of
+ * D [B][Pd][V] (batch stride d_bstride). */
+int oracle_draft_sample(const void *D, int64_t d_bstride, int dtype, int B, int Pd, int64_t V,
+                        int row0, int rows, const float *T, uint32_t seed_lo, uint32_t seed_hi,
+                        uint32_t offset, int32_t *x, int64_t x_bstride)
+{
+    if (!D || !T || !x || B < 0 || Pd < 1 || V < 1 || row0 < 0 || rows < 0 ||
+        row0 + rows > Pd)
+        return ORACLE_BAD_ARG;
+    double *z = (double *)malloc((size_t)V * sizeof(double));
+    if (!z)
+        return ORACLE_NO_MEMORY;
+    for (int b = 0; b < B; ++b) {
+        const double Tb = (double)T[b];
+        const int t_bad = isnan(Tb) || Tb < 0.0;
+        const int greedy = !(Tb > 0.0);
+        for (int i = row0; i < row0 + rows; ++i) {
+            int32_t *xo = x + (int64_t)b * x_bstride + (i - row0);
+            load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)i * V, V, z);
+            if (t_bad || !row_is_valid(z, V, greedy)) {
+                *xo = -1;
+                continue;
+            }
+            if (greedy) {
+                *xo = (int32_t)argmax_lowest(z, V);
+                continue;
+            }
+            int64_t best = -1;
+            double best_y = -INFINITY;
+            for (int64_t v = 0; v < V; ++v) {
+                if (z[v] == -INFINITY)
+                    continue;
+                /* E = -ln u = -log1p(-(1 - u)), G = -ln E */
+                double e = -log1p(-draft_one_minus_u(seed_lo, seed_hi, offset, b, i, v));
+                double y = z[v] / Tb - log(e);
+                if (best < 0 || y > best_y) {
+                    best = v;
+                    best_y = y;
+                }
+            }
+            *xo = (int32_t)best;
+        }
+    }
+    free(z);
     return ORACLE_OK;
 }
