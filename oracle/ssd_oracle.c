@@ -472,8 +472,8 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
 
 /* The uniform of element v of draft row i of batch row b: word v mod 4 of
  * Philox4x32-10 at counter (v / 4, i, b, offset), key (seed_lo, seed_hi),
- * mapped to u = (w >> 8 + 1/2) / 2^24 in (0, 1).  Returns 1 - u, which is
- * exact too. */
+ * mapped to u = (w >> 9 + 1/2) / 2^23 in (0, 1) -- 23 bits, so that u and
+ * 1 - u are exact in binary32 as well as here.  Returns 1 - u. */
 static double draft_one_minus_u(uint32_t seed_lo, uint32_t seed_hi, uint32_t offset, int b,
                                 int i, int64_t v)
 {
@@ -481,8 +481,8 @@ static double draft_one_minus_u(uint32_t seed_lo, uint32_t seed_hi, uint32_t off
     uint32_t key[2] = {seed_lo, seed_hi};
     uint32_t out[4];
     oracle_philox4x32_10(ctr, key, out);
-    uint32_t w = out[v & 3] >> 8;
-    return ((double)(16777215u - w) + 0.5) / 16777216.0;
+    uint32_t w = out[v & 3] >> 9;
+    return ((double)(8388607u - w) + 0.5) / 8388608.0;
 }
 
 /* x[b * x_bstride + (i - row0)] for draft rows i in [row0, row0 + rows) of
