@@ -230,6 +230,47 @@ def b1_latency(ssd, W, dev, reps=300):
             "eager_us": round(eager, 2), "graph_us": round(graph, 2)}
 
 
+def draft_pipeline(ssd, w, inp, dev, reps=50):
+    """The drafter's side fused with the verify (the next step of the hot
+    path): ssd_draft_sample over the k+1 SSD draft rows (Gumbel-max tokens,
+    the draft rows' statistics and the f forks with the drafted token masked)
+    followed by ssd_verify_drafted, which streams only the target rows.
+    Milliseconds per call, CUDA events, same workload."""
+    import torch
+    ws = ssd.new_workspace(ssd.workspace_bytes(w.B, w.k, w.V, w.f + 1), dev)
+    dout, vout = {}, {}
+    x = torch.empty((w.B, w.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def draft():
+        ssd.ssd_draft_sample(inp["D"], inp["T"], w.k, 1234, 0, f=w.f, ws=ws, out=dout)
+
+    def verify():
+        x.copy_(dout["x"][:, : w.k])
+        ssd.ssd_verify(inp["Z"], inp["D"], x, inp["T"], inp["u_acc"], inp["u_smp"],
+                       drafted=True, ws=ws, out=vout)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    draft()
+    t_d = timed(draft)
+    t_v = timed(verify)
+    row = w.B * (w.k + 1) * w.V * 4
+    return {"draft_sample_ms": round(t_d, 4), "verify_drafted_ms": round(t_v, 4),
+            "draft_sample_gbs": round(row / (t_d / 1e3) / 1e9, 1),
+            "verify_drafted_stream_gbs": round(row / (t_v / 1e3) / 1e9, 1)}
+
+
 def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
     """Time the oracle (as it stands, one host thread) on a bounded sample of
     the batch rows: verify_recover + forked_topf + the dict cache."""
@@ -353,6 +394,7 @@ def gpu_arm(args):
             "gpu_launches": launches, "roofline": roof, "clocks": clock, "e2e": e2e}
     if rank == 0 and world == 1:
         line["latency_b1"] = b1_latency(ssd, W, dev)
+        line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
     if rank == 0:

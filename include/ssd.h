@@ -275,6 +275,53 @@ SSD_API ssd_status ssd_verify_fork_fanout(const void *Z, int64_t z_bstride,
                                   size_t ws_bytes, ssd_stream_t stream);
 
 /*
+ * ssd_draft_sample -- the drafter's tokens, drawn on the GPU ([SUM] sampler:
+ * greedy at temperature 0, stochastic otherwise; [SPS] the small model
+ * proposes the draft), fused with the draft rows' statistics so that a later
+ * ssd_verify_drafted reads only the target rows.
+ *   D        : draft logits [B, >= row0+rows, V], batch stride d_bstride.
+ *   k        : the verify call's draft length (sizes and places the
+ *              statistics in ws); rows [row0, row0+rows) with
+ *              row0 + rows <= k + 1 (row k: SSD's next-round token).
+ *   T        : [B] fp32; the verify call must use the same temperatures.
+ *   seed, offset : the draw of element v of row i of batch row b uses word
+ *              v mod 4 of Philox4x32-10 (Salmon et al. 2011) at counter
+ *              (v / 4, i, b, offset) under key (seed low, seed high 32 bits)
+ *              and u = ((w >> 9) + 1/2) / 2^23.
+ *   x_out    : x_out[b * x_bstride + (i - row0)] = the token: T > 0 the
+ *              Gumbel-max draw argmax_v (z_v / T - ln(-ln u_v)) (an exact
+ *              draw from softmax(z / T); ties to the lowest index); T == 0
+ *              the argmax; -1 for T < 0 / NaN or an invalid row (device
+ *              error word set).
+ *   f, fork_tok, fork_logit : f >= 1 also writes [B, rows, f] forks: the f
+ *              largest logits of each row other than its drafted token (SSD
+ *              forked recovery with the drafter's token masked); f == 0
+ *              writes none (pointers may be NULL).  f + 1 <= SSD_MAX_F.
+ *   ws       : ssd_workspace_bytes(B, k, V, f > 0 ? f + 1 : 0) bytes; the
+ *              same workspace goes to ssd_verify_drafted.
+ */
+SSD_API ssd_status ssd_draft_sample(const void *D, int64_t d_bstride, ssd_dtype dtype, int B,
+                            int k, int V, int row0, int rows, const float *T,
+                            uint64_t seed, uint32_t offset, int32_t *x_out,
+                            int64_t x_bstride, int f, int32_t *fork_tok,
+                            float *fork_logit, void *ws, size_t ws_bytes,
+                            ssd_stream_t stream);
+
+/*
+ * ssd_verify_drafted -- ssd_verify whose draft rows 0..k-1 were already
+ * summarised into ws by ssd_draft_sample calls (same B, k, V, T and ws):
+ * the streaming pass reads only the k+1 target rows; D is still read at the
+ * draft tokens and, for the recovery draw, at row n.  Arguments and results
+ * as ssd_verify.
+ */
+SSD_API ssd_status ssd_verify_drafted(const void *Z, int64_t z_bstride, const void *D,
+                              int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                              const int32_t *x, const float *T, const float *u_acc,
+                              int32_t *accept_len, float *p_at_x, float *q_at_x,
+                              const float *u_smp, int32_t *out_tok, void *ws,
+                              size_t ws_bytes, ssd_stream_t stream);
+
+/*
  * Speculation cache ([SSD] roadmap: the speculation cache; [SUM] cache
  * hits and misses).  An open-addressing table on the device mapping the key
  * (b, position, token) to `depth` draft tokens.  Keys compare exactly, so the

@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     profile_end,
     selftest_exp2,
     softmax_workspace_bytes,
+    ssd_draft_sample,
     ssd_forked_recovery,
     ssd_sample_residual,
     ssd_softmax_temp,

@@ -50,6 +50,10 @@ SIGNATURES = [
                                         _Z, _P]),
     ("ssd_verify_fork_fanout", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _I, _P, _P, _I, _P, _P, _P, _Z, _P]),
+    ("ssd_draft_sample", _I, [_P, _L, _I, _I, _I, _I, _I, _I, _P, ctypes.c_uint64,
+                              ctypes.c_uint32, _P, _L, _I, _P, _P, _P, _Z, _P]),
+    ("ssd_verify_drafted", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                _P, _P, _Z, _P]),
     ("ssd_spec_cache_create", _I, [_I, _I, _P]),
     ("ssd_spec_cache_destroy", None, [_P]),
     ("ssd_spec_cache_clear", _I, [_P, _P]),
@@ -211,11 +215,12 @@ def _verify_outputs(B, k, dev, out, sample: bool, f: int = 0, P: int = 0):
 
 def ssd_verify(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
                u_acc: torch.Tensor, u_smp: Optional[torch.Tensor] = None, *,
-               ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
-               stream=None) -> Dict[str, torch.Tensor]:
+               drafted: bool = False, ws: Optional[torch.Tensor] = None,
+               out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
     """Acceptance, first-reject prefix and (if u_smp is given) the recovery or
     bonus draw.  Z [B,k+1,V], D [B,>=k,V] (same dtype), x [B,k] int32,
-    T [B], u_acc [B,k], u_smp [B] float32."""
+    T [B], u_acc [B,k], u_smp [B] float32.  drafted: the draft rows'
+    statistics are already in ws (ssd_draft_sample with the same ws)."""
     lib = load_library()
     B, kp1, V = Z.shape
     k = kp1 - 1
@@ -228,11 +233,14 @@ def ssd_verify(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tenso
     for t, n in ((T, "T"), (u_acc, "u_acc")):
         _want(t, torch.float32, n)
     dev = Z.device
+    if drafted and ws is None:
+        raise ValueError("drafted=True needs the workspace of ssd_draft_sample")
     if ws is None:
         ws = new_workspace(workspace_bytes(B, k, V, 0), dev)
     wp, wn = _ws_ptr(ws)
     o = _verify_outputs(B, k, dev, out, u_smp is not None)
-    _check("ssd_verify", lib.ssd_verify(
+    fn = lib.ssd_verify_drafted if drafted else lib.ssd_verify
+    _check("ssd_verify_drafted" if drafted else "ssd_verify", fn(
         _dev(Z, "Z"), kp1 * V, _dev(D, "D"), D.shape[1] * V, _dtype_code(Z), B, k, V,
         _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
         _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
@@ -334,6 +342,37 @@ def ssd_verify_fork(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.
                lib.ssd_verify_fork_fanout(*head, _dev(fanout, "fanout"), *tail))
     o["ws"] = ws
     return o
+
+
+def ssd_draft_sample(D: torch.Tensor, T: torch.Tensor, k: int, seed: int, offset: int, *,
+                     row0: int = 0, rows: Optional[int] = None, f: int = 0,
+                     ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                     stream=None) -> Dict[str, torch.Tensor]:
+    """Draw the drafter's tokens for rows [row0, row0 + rows) of D [B, Pd, V]
+    (Gumbel-max with Philox4x32-10 uniforms; argmax at T == 0) and keep the
+    rows' statistics in ws for ssd_verify(..., drafted=True).  With f > 0
+    also the f forks per row (top-f logits other than the drafted token)."""
+    lib = load_library()
+    B, Pd, V = D.shape
+    rows = Pd - row0 if rows is None else rows
+    _want(T, torch.float32, "T")
+    dev = D.device
+    if ws is None:
+        ws = new_workspace(workspace_bytes(B, k, V, f + 1 if f > 0 else 0), dev)
+    wp, wn = _ws_ptr(ws)
+    out = {} if out is None else out
+    if "x" not in out:
+        out["x"] = torch.empty((B, rows), dtype=torch.int32, device=dev)
+        if f > 0:
+            out["fork_tok"] = torch.empty((B, rows, f), dtype=torch.int32, device=dev)
+            out["fork_logit"] = torch.empty((B, rows, f), dtype=torch.float32, device=dev)
+    _check("ssd_draft_sample", lib.ssd_draft_sample(
+        _dev(D, "D"), Pd * V, _dtype_code(D), B, k, V, row0, rows, _dev(T, "T"),
+        seed & 0xFFFFFFFFFFFFFFFF, offset & 0xFFFFFFFF, _dev(out["x"], "x"), rows, f,
+        _opt(out.get("fork_tok"), "fork_tok"), _opt(out.get("fork_logit"), "fork_logit"),
+        wp, wn, _stream(stream)))
+    out["ws"] = ws
+    return out
 
 
 class SpecCache:

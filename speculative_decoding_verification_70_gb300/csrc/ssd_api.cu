@@ -17,6 +17,9 @@ namespace ssd {
 cudaError_t launch_stats_rows(const StatsParams& p, int B, int dtype, bool vec, int r0, int rows,
                               bool topf, cudaStream_t s);
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
+cudaError_t launch_draft(const StatsParams& p, int B, int dtype, bool vec, int rows, bool topf,
+                         cudaStream_t s);
+cudaError_t launch_draft_finalize(const DraftParams& p, cudaStream_t s);
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
@@ -128,6 +131,7 @@ struct VerifyCall {
   const float* u_smp; int32_t* out_tok;
   int f; const int32_t* mask; int M; int32_t* fork_tok; float* fork_logit;
   const int32_t* fanout;  // [k+1] device, or null (f at every position)
+  bool drafted;           // draft rows' statistics already in ws (ssd_draft_sample)
   void* ws; size_t ws_bytes;
   cudaStream_t stream;
   bool single_stream;  // no internal streams (the no-allocation entry point)
@@ -296,7 +300,7 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   StatsParams& sp = q.sp;
   memset(&sp, 0, sizeof sp);
   sp.Z = Zb; sp.zb = c.zb; sp.Pz = c.k + 1;
-  sp.D = Db; sp.db = c.db; sp.Pds = c.k; sp.Pdf = fork ? Pf : 0;
+  sp.D = Db; sp.db = c.db; sp.Pds = c.drafted ? 0 : c.k; sp.Pdf = fork ? Pf : 0;
   sp.T = c.T + b0;
   sp.mask = fork && c.M > 0 ? c.mask + static_cast<size_t>(b0) * Pf * c.M : nullptr;
   sp.M = fork ? c.M : 0; sp.f = fork ? c.f : 0;
@@ -308,9 +312,10 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   FinalizeParams& fp = q.fp;
   memset(&fp, 0, sizeof fp);
   fp.Z = Zb; fp.zb = c.zb; fp.Pz = sp.Pz;
-  fp.D = Db; fp.db = c.db; fp.Pds = sp.Pds; fp.Pdf = sp.Pdf;
+  fp.D = Db; fp.db = c.db; fp.Pds = c.k; fp.Pdf = sp.Pdf;
   fp.dtype = c.dt == SSD_BF16 ? 1 : 0;
-  fp.B = Bs; fp.k = c.k; fp.V = c.V; fp.C = L.ch.C; fp.R = sp.R; fp.Rp = L.R; fp.f = sp.f;
+  fp.B = Bs; fp.k = c.k; fp.V = c.V; fp.C = L.ch.C; fp.Rp = L.R; fp.f = sp.f;
+  fp.R = sp.Pz + (sp.Pdf > c.k ? sp.Pdf : c.k);
   fp.T = c.T + b0; fp.x = c.x + static_cast<size_t>(b0) * c.k;
   fp.u_acc = c.u_acc + static_cast<size_t>(b0) * c.k;
   fp.accept_len = c.accept_len + b0;
@@ -492,6 +497,74 @@ ssd_status ssd_verify(const void* Z, int64_t z_bstride, const void* D, int64_t d
   c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
   c.u_smp = u_smp; c.out_tok = out_tok; c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
   return run_verify(c, false);
+}
+
+ssd_status ssd_verify_drafted(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                              ssd_dtype dtype, int B, int k, int V, const int32_t* x,
+                              const float* T, const float* u_acc, int32_t* accept_len,
+                              float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
+                              void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
+  c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
+  c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
+  c.u_smp = u_smp; c.out_tok = out_tok; c.drafted = true;
+  c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
+  return run_verify(c, false);
+}
+
+ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, int B, int k,
+                            int V, int row0, int rows, const float* T, uint64_t seed,
+                            uint32_t offset, int32_t* x_out, int64_t x_bstride, int f,
+                            int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
+                            ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!D || !T || !x_out || !ws) return SSD_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (row0 < 0 || rows < 1 || row0 + rows > k + 1) return SSD_ERR_INVALID_ARG;
+  if (d_bstride < static_cast<int64_t>(row0 + rows) * V) return SSD_ERR_INVALID_ARG;
+  if (B > 1 && x_bstride < rows) return SSD_ERR_INVALID_ARG;
+  if (f < 0 || f + 1 > SSD_MAX_F || f + 1 >= V) return SSD_ERR_INVALID_ARG;
+  if (f > 0 && (!fork_tok || !fork_logit)) return SSD_ERR_INVALID_ARG;
+  if (!aligned(D, esize(dtype)) || !aligned(ws, 256)) return SSD_ERR_INVALID_ARG;
+  const WsLayout L = make_layout(B, k, V, f > 0 ? f + 1 : 0, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(D, d_bstride, V, dtype);
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.D = D; sp.db = d_bstride;
+  sp.Pz = k + 1;  // draft row i's partials sit at row Pz + i of the verify layout
+  sp.T = T;
+  sp.f = f > 0 ? f + 1 : 0;
+  sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = L.R; sp.Rp = L.R; sp.r0 = row0;
+  sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  sp.topk = reinterpret_cast<TopEntry*>(wsp(ws, L.topk));
+  sp.gpart = reinterpret_cast<GumbelPart*>(wsp(ws, L.gpart));
+  sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  sp.seed_lo = static_cast<uint32_t>(seed);
+  sp.seed_hi = static_cast<uint32_t>(seed >> 32);
+  sp.offset = offset;
+  sp.Pf = L.Pf;
+  sp.G = 1;
+  while (sp.G < 4 && static_cast<long long>(B) * rows * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
+    sp.G *= 2;
+  const int dt = dtype == SSD_BF16 ? 1 : 0;
+  cudaError_t e;
+  {
+    ProfScope ps("draft_stats", S(stream));
+    e = launch_draft(sp, B, dt, vec, rows, f > 0, S(stream));
+  }
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  DraftParams dp;
+  memset(&dp, 0, sizeof dp);
+  dp.B = B; dp.V = V; dp.C = L.ch.C; dp.Rp = L.R; dp.Pz = k + 1; dp.Pf = L.Pf;
+  dp.row0 = row0; dp.rows = rows; dp.T = T;
+  dp.part = sp.part; dp.gpart = sp.gpart; dp.topk = sp.topk; dp.f = f;
+  dp.x_out = x_out; dp.x_bstride = x_bstride; dp.fork_tok = fork_tok; dp.fork_logit = fork_logit;
+  dp.err = sp.err;
+  ProfScope ps("draft_finalize", S(stream));
+  return cuda_status(launch_draft_finalize(dp, S(stream)));
 }
 
 ssd_status ssd_verify_fork_fanout(const void* Z, int64_t z_bstride, const void* D,

@@ -26,6 +26,12 @@ struct TopEntry {
   int i;  // 0x7fffffff marks an empty slot
 };
 
+// Best Gumbel-perturbed logit of a chunk (draft-side sampling).
+struct GumbelPart {
+  float y;    // max over the chunk of z / T - ln(-ln u)
+  int idx;    // lowest index attaining it (0x7fffffff: none)
+};
+
 // Merged statistics of one logit row.
 struct RowStat {
   double S;    // sum over the row of 2^((z - m) * c)
@@ -51,7 +57,7 @@ struct Chunking {
 
 // Workspace of the verify / fork / residual calls.
 struct WsLayout {
-  size_t err, part, topk, rowstat, bstate, rnorm, rmass, racc, amb_cnt, amb_idx, total;
+  size_t err, part, topk, rowstat, bstate, rnorm, rmass, racc, amb_cnt, amb_idx, gpart, total;
   int B, R, Pf, f;
   Chunking ch;
 };
@@ -75,6 +81,10 @@ struct StatsParams {
   PartStat* part;      // [B][Rp][C]
   TopEntry* topk;      // [B][Pdf][C][f]
   int* err;            // device error word
+  // draft-side sampling (draft_kernel only)
+  GumbelPart* gpart;   // [B][Pf][C]
+  uint32_t seed_lo, seed_hi, offset;
+  int Pf;              // row pitch of gpart[] and topk[] (k + 1)
 };
 
 struct FinalizeParams {
@@ -118,6 +128,21 @@ struct ResidualParams {
   int b0;              // first batch row of this launch (grids hold <= 65535)
   int B;               // batch rows of this call (row-strided kernels)
   int32_t* out_tok;    // [B][k+1]
+};
+
+// Merge of the draft-side sampling pass: one warp per (b, draft row).
+struct DraftParams {
+  int B, V, C, Rp, Pz, Pf, row0, rows;
+  const float* T;
+  const PartStat* part;      // [B][Rp][C], draft row i at Pz + i
+  const GumbelPart* gpart;   // [B][Pf][C]
+  const TopEntry* topk;      // [B][Pf][C][F1], F1 = f + 1
+  int f;                     // forks kept per row (0: none)
+  int32_t* x_out;            // [b * x_bstride + (i - row0)]
+  int64_t x_bstride;
+  int32_t* fork_tok;         // [B][rows][f]
+  float* fork_logit;
+  int* err;
 };
 
 struct SoftmaxParams {
@@ -231,6 +256,7 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * C);
   L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
+  L.gpart = off;                    off = align256(off + sizeof(GumbelPart) * B * L.Pf * C);
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
   L.total = off;
   return L;
@@ -251,6 +277,7 @@ inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
   L.topk = off;
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * rows);
   L.bstate = off; L.rnorm = off; L.rmass = off; L.racc = off; L.amb_cnt = off; L.amb_idx = off;
+  L.gpart = off;
   L.total = off;
   return L;
 }

@@ -29,8 +29,78 @@ namespace ssd {
 struct StatsSmem {
   float m[kWarps], s[kWarps];
   int i[kWarps], n[kWarps];
+  float gy[kWarps];
+  int gi[kWarps];
   int mask[kMaxMask];
 };
+
+// ---------------------------------------------------------------------------
+// Draft-side sampling: Gumbel-max draws argmax_v (z_v / T - ln(-ln u_v)),
+// an exact draw from softmax(z / T) (the Gumbel-max trick), with u_v from
+// the counter-based generator Philox4x32-10 (Salmon, Moraes, Dror & Shaw
+// 2011): element v of draft row i of batch row b takes word v mod 4 of the
+// generator at counter (v / 4, i, b, offset) under key (seed_lo, seed_hi),
+// and u = (w >> 9 + 1/2) / 2^23 (23 bits: u and 1 - u are exact floats).
+// ---------------------------------------------------------------------------
+struct GumbelArgs {
+  uint32_t k0, k1, row, b, offset;
+  float invT;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// z / T + G for one element: G = -ln(E), E = -ln u = -log1p(-(1 - u)).
+__device__ __forceinline__ float gumbel_key(float z, float invT, uint32_t w) {
+  const float one_minus_u = (static_cast<float>(8388607u - (w >> 9)) + 0.5f) * 1.1920928955078125e-7f;
+  const float e = -log1pf(-one_minus_u);
+  return fmaf(z, invT, -logf(e));
+}
+
+// Fold the kv elements z[0..kv) starting at index `base` into the thread's
+// best (gy, gi); elements arrive in increasing index order, so a strict
+// compare keeps the lowest index on ties.
+template <int KV>
+__device__ __forceinline__ void gumbel_vector(const GumbelArgs& g, const float (&z)[8], int base,
+                                              float& gy, int& gi) {
+  if (KV == 1) {
+    const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(base) >> 2, g.row, g.b, g.offset),
+                                  g.k0, g.k1);
+    const int q = base & 3;
+    const uint32_t word = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
+    const float y = gumbel_key(z[0], g.invT, word);
+    if (y > gy) {
+      gy = y;
+      gi = base;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < KV / 4; ++h) {
+      const uint4 w = philox4x32_10(
+          make_uint4((static_cast<uint32_t>(base) >> 2) + h, g.row, g.b, g.offset), g.k0, g.k1);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float y = gumbel_key(z[4 * h + e], g.invT, ws[e]);
+        if (y > gy) {
+          gy = y;
+          gi = base + 4 * h + e;
+        }
+      }
+    }
+  }
+}
 
 constexpr int kMaxF = 16;
 
@@ -175,15 +245,18 @@ __device__ void topf_select(const StatsParams& p, const ScanState& st,
   }
 }
 
-template <typename Tag, bool VEC, bool DO_EXP, bool TOPF>
+template <typename Tag, bool VEC, bool DO_EXP, bool TOPF, bool GUMBEL = false>
 __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row, int lo, int hi,
                             float c, PartStat* out_part, TopEntry* out_top, int n_slots,
-                            StatsSmem& sm, TopfScratch* ts) {
+                            StatsSmem& sm, TopfScratch* ts, const GumbelArgs* ga = nullptr,
+                            GumbelPart* out_g = nullptr) {
   constexpr int kV = VEC ? Tag::kVec : 1;
   constexpr int U = 4;
   const int tid = threadIdx.x;
   ScanState st;
   scan_init(st);
+  float gy = -INFINITY;
+  int gi = kIdxNone;
   const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
   for (int vb = v0 + tid; vb < v1; vb += kThreads * U) {
     typename Tag::Raw raw[U];
@@ -207,11 +280,32 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
 #pragma unroll
         for (int e = 1; e < kV; ++e) m = max_nan(m, z[e]);
         scan_vector<DO_EXP, TOPF>(st, z, kV, m, vi * kV, c);
+        if constexpr (GUMBEL) gumbel_vector<kV>(*ga, z, vi * kV, gy, gi);
       }
     }
   }
+  if constexpr (GUMBEL) {
+    warp_argmax(gy, gi);
+    if ((tid & 31) == 0) {
+      sm.gy[tid >> 5] = gy;
+      sm.gi[tid >> 5] = gi;
+    }
+  }
   if constexpr (TOPF) topf_post(st, sm.mask, p.M, *ts);
-  block_stats_write(st, c, DO_EXP, sm.m, sm.s, sm.i, sm.n, out_part);
+  block_stats_write(st, c, DO_EXP, sm.m, sm.s, sm.i, sm.n, out_part);  // holds a barrier
+  if constexpr (GUMBEL) {
+    if (tid == 0) {
+      GumbelPart g;
+      g.y = sm.gy[0];
+      g.idx = sm.gi[0];
+      for (int w = 1; w < kWarps; ++w)
+        if (ranks_before(sm.gy[w], sm.gi[w], g.y, g.idx)) {
+          g.y = sm.gy[w];
+          g.idx = sm.gi[w];
+        }
+      *out_g = g;
+    }
+  }
   if constexpr (TOPF) topf_select<Tag, VEC>(p, st, row, lo, hi, sm.mask, out_top, n_slots, *ts);
 }
 
@@ -279,6 +373,177 @@ __global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : 6)
     stats_chunk<Tag, VEC, true, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm, nullptr);
   else
     stats_chunk<Tag, VEC, false, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm, nullptr);
+}
+
+// Draft-side sampling pass.  grid: (chunk groups, draft rows of this call,
+// batch rows).  Each CTA streams G chunks of draft row i = blockIdx.y + r0
+// once and writes, into the verify workspace, the row's partial statistics
+// (slot Pz + i, so a later ssd_verify_drafted skips these rows), the best
+// Gumbel-perturbed logit (T > 0 rows) and, with HAS_TOPF, a top-(f+1) list
+// (the forks with the drafted token masked are taken from it at the merge).
+template <typename Tag, bool VEC, bool HAS_TOPF>
+__global__ void __launch_bounds__(kThreads, SSD_TOPF_MIN_BLOCKS) draft_kernel(StatsParams p) {
+  using Elem = typename Tag::Elem;
+  const int G = p.G;
+  const int c = blockIdx.x * G, i = blockIdx.y + p.r0, b = blockIdx.z + p.b0;
+  const int lo = c * p.CH;
+  const int hi = min(p.V, lo + G * p.CH);
+  const int n_slots = min(G, p.C - c);
+  __shared__ StatsSmem sm;
+  __shared__ float2 s_c;
+  const Elem* row = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db +
+                    static_cast<int64_t>(i) * p.V;
+  const float T = p.T[b];
+  const bool do_exp = T > 0.f;  // NaN and T <= 0: statistics without exponentials
+  float cf = 0.f;
+  if (do_exp) cf = cta_temp_coeff(T, &s_c).x;
+  PartStat* out_part = p.part + (static_cast<int64_t>(b) * p.Rp + p.Pz + i) * p.C + c;
+  GumbelPart* out_g = p.gpart + (static_cast<int64_t>(b) * p.Pf + i) * p.C + c;
+  if (threadIdx.x < n_slots) {
+    GumbelPart none;
+    none.y = -INFINITY;
+    none.idx = kIdxNone;
+    if (threadIdx.x > 0 || !do_exp) out_g[threadIdx.x] = none;
+    if (threadIdx.x > 0) {
+      PartStat id;
+      id.m = -INFINITY;
+      id.s = 0.f;
+      id.idx = kIdxNone;
+      id.flags = 0;
+      out_part[threadIdx.x] = id;
+    }
+  }
+  GumbelArgs ga;
+  ga.k0 = p.seed_lo;
+  ga.k1 = p.seed_hi;
+  ga.row = static_cast<uint32_t>(i);
+  ga.b = static_cast<uint32_t>(b);
+  ga.offset = p.offset;
+  ga.invT = do_exp ? 1.0f / T : 0.f;
+  if constexpr (HAS_TOPF) {
+    __shared__ TopfScratch ts;  // no masked tokens (M == 0)
+    TopEntry* out_top = p.topk + ((static_cast<int64_t>(b) * p.Pf + i) * p.C + c) * p.f;
+    if (do_exp)
+      stats_chunk<Tag, VEC, true, true, true>(p, row, lo, hi, cf, out_part, out_top, n_slots, sm,
+                                              &ts, &ga, out_g);
+    else
+      stats_chunk<Tag, VEC, false, true, false>(p, row, lo, hi, cf, out_part, out_top, n_slots, sm,
+                                                &ts);
+    return;
+  }
+  if (do_exp)
+    stats_chunk<Tag, VEC, true, false, true>(p, row, lo, hi, cf, out_part, nullptr, 0, sm, nullptr,
+                                             &ga, out_g);
+  else
+    stats_chunk<Tag, VEC, false, false, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm,
+                                               nullptr);
+}
+
+// Merge of the draft pass, one warp per (b, draft row): the drafted token
+// (T > 0: the best Gumbel-perturbed logit over the chunks; T == 0: the
+// argmax; -1 for an invalid temperature or row) and, when f > 0, the f best
+// logits of the row other than the drafted token (the SSD forks with the
+// drafter's own token masked), from the chunks' top-(f+1) lists.
+__global__ void __launch_bounds__(kThreads) draft_finalize_kernel(DraftParams p) {
+  __shared__ int heads[kWarps][256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long w = static_cast<long long>(blockIdx.x) * kWarps + warp;
+  if (w >= static_cast<long long>(p.B) * p.rows) return;  // whole warp
+  const int b = static_cast<int>(w / p.rows), r = static_cast<int>(w % p.rows), i = p.row0 + r;
+  const float T = p.T[b];
+  const bool t_bad = isnan(T) || T < 0.f;
+  const bool greedy = !(T > 0.f);
+  // maximum, lowest argmax and NaN flag of the row
+  const PartStat* parts = p.part + (static_cast<int64_t>(b) * p.Rp + p.Pz + i) * p.C;
+  float m = -INFINITY;
+  int idx = kIdxNone, nan = 0;
+  for (int q = lane; q < p.C; q += 32) {
+    const PartStat ps = parts[q];
+    nan |= ps.flags & 1;
+    if (ranks_before(ps.m, ps.idx, m, idx)) {
+      m = ps.m;
+      idx = ps.idx;
+    }
+  }
+  warp_argmax(m, idx);
+  nan = __any_sync(kFull, nan);
+  const bool bad = t_bad || nan || (!greedy && (m == INFINITY || m == -INFINITY));
+  int x = -1;
+  if (!bad && greedy) {
+    x = idx == kIdxNone ? -1 : idx;
+  } else if (!bad) {
+    const GumbelPart* gp = p.gpart + (static_cast<int64_t>(b) * p.Pf + i) * p.C;
+    float gy = -INFINITY;
+    int gi = kIdxNone;
+    for (int q = lane; q < p.C; q += 32) {
+      const GumbelPart g = gp[q];
+      if (ranks_before(g.y, g.idx, gy, gi)) {
+        gy = g.y;
+        gi = g.idx;
+      }
+    }
+    warp_argmax(gy, gi);
+    x = gi == kIdxNone ? -1 : gi;
+  }
+  if (lane == 0) {
+    p.x_out[static_cast<int64_t>(b) * p.x_bstride + r] = x;
+    int e = 0;
+    if (t_bad) e |= 0x1;
+    else if (bad) e |= 0x2;
+    if (e) atomicOr(p.err, e);
+  }
+  if (p.f <= 0) return;
+  // forks: merge the chunks' top-(f+1) lists, skipping the drafted token
+  const int F1 = p.f + 1;
+  const TopEntry* lists = p.topk + (static_cast<int64_t>(b) * p.Pf + i) * p.C * F1;
+  int32_t* tok_out = p.fork_tok + (static_cast<int64_t>(b) * p.rows + r) * p.f;
+  float* logit_out = p.fork_logit + (static_cast<int64_t>(b) * p.rows + r) * p.f;
+  int* hd = heads[warp];
+  for (int q = lane; q < p.C; q += 32) hd[q] = 0;
+  __syncwarp();
+  int out_n = 0;
+  for (int round = 0; round < F1 && out_n < p.f; ++round) {
+    float bv = -INFINITY;
+    int bi = kIdxNone, bq = -1;
+    for (int q = lane; q < p.C; q += 32) {
+      const int h = hd[q];
+      if (h < F1) {
+        const TopEntry e = lists[q * F1 + h];
+        if (bq < 0 || ranks_before(e.v, e.i, bv, bi)) {
+          bv = e.v;
+          bi = e.i;
+          bq = q;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, o);
+      const int oi = __shfl_xor_sync(kFull, bi, o);
+      const int oq = __shfl_xor_sync(kFull, bq, o);
+      const bool take = (oq >= 0) && (bq < 0 || ranks_before(ov, oi, bv, bi) ||
+                                      (ov == bv && oi == bi && oq < bq));
+      if (take) {
+        bv = ov;
+        bi = oi;
+        bq = oq;
+      }
+    }
+    if (bq < 0 || bi == kIdxNone) break;  // lists exhausted
+    if (lane == (bq & 31)) hd[bq] += 1;
+    __syncwarp();
+    if (bi == x) continue;  // the drafted token is masked
+    if (lane == 0) {
+      tok_out[out_n] = nan ? -1 : bi;
+      logit_out[out_n] = nan ? NAN : bv;
+    }
+    ++out_n;
+  }
+  if (lane == 0)
+    for (int q = out_n; q < p.f; ++q) {
+      tok_out[q] = -1;
+      logit_out[q] = nan ? NAN : -INFINITY;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -613,6 +878,37 @@ cudaError_t launch_stats_rows(const StatsParams& p0, int B, int dtype, bool vec,
                : launch_stats_t<BF16Tag, false>(p, B, rows, topf, s);
   return vec ? launch_stats_t<F32Tag, true>(p, B, rows, topf, s)
              : launch_stats_t<F32Tag, false>(p, B, rows, topf, s);
+}
+
+template <typename Tag, bool VEC>
+static cudaError_t launch_draft_t(const StatsParams& p0, int B, int rows, bool topf, cudaStream_t s) {
+  StatsParams p = p0;
+  for (int b0 = 0; b0 < B; b0 += kMaxGridBatch) {
+    p.b0 = b0;
+    dim3 grid((p.C + p.G - 1) / p.G, rows, B - b0 < kMaxGridBatch ? B - b0 : kMaxGridBatch);
+    if (topf) draft_kernel<Tag, VEC, true><<<grid, kThreads, 0, s>>>(p);
+    else draft_kernel<Tag, VEC, false><<<grid, kThreads, 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Draft rows [p.r0, p.r0 + rows) of every batch row.
+cudaError_t launch_draft(const StatsParams& p, int B, int dtype, bool vec, int rows, bool topf,
+                         cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (dtype == 1)
+    return vec ? launch_draft_t<BF16Tag, true>(p, B, rows, topf, s)
+               : launch_draft_t<BF16Tag, false>(p, B, rows, topf, s);
+  return vec ? launch_draft_t<F32Tag, true>(p, B, rows, topf, s)
+             : launch_draft_t<F32Tag, false>(p, B, rows, topf, s);
+}
+
+cudaError_t launch_draft_finalize(const DraftParams& p, cudaStream_t s) {
+  const long long warps = static_cast<long long>(p.B) * p.rows;
+  draft_finalize_kernel<<<static_cast<unsigned>((warps + kWarps - 1) / kWarps), kThreads, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {

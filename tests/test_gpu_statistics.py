@@ -105,3 +105,20 @@ def test_gpu_tokens_match_oracle_on_a_million_rows(million):
     dp = np.abs(ref["p_at_x"] - got["p_at_x"].numpy()).max()
     dq = np.abs(ref["q_at_x"] - got["q_at_x"].numpy()).max()
     assert dp <= 1e-5 and dq <= 1e-5
+
+
+def test_gpu_draft_sampler_law_on_a_million_rows(gpu_lib):
+    """The drafter's Gumbel-max draws follow softmax(z / T): 10^6 rows of the
+    same logits (distinct batch rows, so distinct Philox counters), one call;
+    every row also equals the oracle's draw."""
+    V, N, T = 8, 1_000_000, 0.9
+    z = torch.tensor([0.4, -0.7, 1.9, 0.0, 1.2, -2.5, 0.9, 0.1])
+    D = z.reshape(1, 1, V).expand(N, 1, V).contiguous()
+    Tv = torch.full((N,), T)
+    out = gpu_lib.ssd_draft_sample(D.cuda(), Tv.cuda(), 1, 0xABCDEF, 2)
+    torch.cuda.synchronize()
+    x = out["x"][:, 0].cpu().numpy()
+    p = _softmax64(z.numpy()[None], T)[0]
+    assert scipy_stats.chisquare(np.bincount(x, minlength=V), p * N).pvalue > 1e-3
+    ref = oracle.draft_sample(D, Tv, 0xABCDEF, 2)[:, 0]
+    assert (ref != x).sum() <= 1e-4 * N
