@@ -61,11 +61,29 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// z / T + G for one element: G = -ln(E), E = -ln u = -log1p(-(1 - u)).
+__device__ __forceinline__ float lg2_fast(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// z / T + G for one element: G = -ln(E), E = -ln u.  E is taken from the
+// series v + v^2/2 + ... + v^5/5 of -ln(1 - v), v = 1 - u, when v < 1/16
+// (truncation below v^6/6 relative, < 1e-8), else as -ln 2 * log2(u); both
+// logarithms use the MUFU log2 (absolute error ~2^-22 in log2), so G is off
+// by at most ~2e-6 -- a token can differ from an exact computation only when
+// two perturbed logits tie that closely.
 __device__ __forceinline__ float gumbel_key(float z, float invT, uint32_t w) {
-  const float one_minus_u = (static_cast<float>(8388607u - (w >> 9)) + 0.5f) * 1.1920928955078125e-7f;
-  const float e = -log1pf(-one_minus_u);
-  return fmaf(z, invT, -logf(e));
+  const uint32_t m = w >> 9;
+  const float v = (static_cast<float>(8388607u - m) + 0.5f) * 1.1920928955078125e-7f;  // 1 - u
+  constexpr float kLn2 = 0.693147180559945309f;
+  const float u = (static_cast<float>(m) + 0.5f) * 1.1920928955078125e-7f;
+  float s = fmaf(v, 0.2f, 0.25f);
+  s = fmaf(v, s, 0.333333333f);
+  s = fmaf(v, s, 0.5f);
+  s = fmaf(v, s, 1.0f);
+  const float e = v < 0.0625f ? v * s : -kLn2 * lg2_fast(u);
+  return fmaf(z, invT, -kLn2 * lg2_fast(e));
 }
 
 // Fold the kv elements z[0..kv) starting at index `base` into the thread's
