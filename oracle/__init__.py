@@ -72,6 +72,9 @@ def _load():
     lib.oracle_forked_topf.argtypes = [P, i64, i32, i32, i32, i64, i32, P, i32,
                                        P, P]
     lib.oracle_forked_topf.restype = i32
+    lib.oracle_verify_recover_filtered.argtypes = [P, i64, P, i64, i32, i32, i32, i64, P, P,
+                                                   i32, P, P, P, i32, P, P, P, P]
+    lib.oracle_verify_recover_filtered.restype = i32
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox4x32_10.restype = None
     u32 = ctypes.c_uint32
@@ -167,6 +170,36 @@ def verify_recover(Z, D, x, T, u_acc, u_smp, f64_uniforms: bool = False
         _ptr(z), kp1 * V, _ptr(d), Pd * V, dt, B, k, V, _ptr(x), _ptr(T),
         _ptr(u_acc), _ptr(u_smp), _ptr(acc), _ptr(pax), _ptr(qax), _ptr(out)),
         "verify_recover")
+    return {"accept_len": acc, "p_at_x": pax, "q_at_x": qax, "out_tok": out}
+
+
+def verify_recover_filtered(Z, D, x, T, K: int, top_p, u_acc, u_smp,
+                            f64_uniforms: bool = False) -> Dict[str, np.ndarray]:
+    """verify_recover over top-k / top-p filtered target and draft
+    distributions (same K and top_p for both; top_p [B] or None): the tokens
+    ordered by (logit desc, index asc), the first K kept, then the shortest
+    prefix holding >= top_p of their mass, renormalised."""
+    z, dt = _logits(Z)
+    d, dt2 = _logits(D)
+    if dt != dt2:
+        raise TypeError("Z and D must share a dtype")
+    B, kp1, V = z.shape
+    k = kp1 - 1
+    Pd = d.shape[1]
+    x = np.ascontiguousarray(x, dtype=np.int32).reshape(B, k)
+    T = np.ascontiguousarray(T, dtype=np.float32).reshape(B)
+    tp = None if top_p is None else np.ascontiguousarray(top_p, dtype=np.float32).reshape(B)
+    udt = np.float64 if f64_uniforms else np.float32
+    u_acc = np.ascontiguousarray(u_acc, dtype=udt).reshape(B, k)
+    u_smp = np.ascontiguousarray(u_smp, dtype=udt).reshape(B)
+    acc = np.empty(B, dtype=np.int32)
+    pax = np.empty((B, k), dtype=np.float64)
+    qax = np.empty((B, k), dtype=np.float64)
+    out = np.empty((B, k + 1), dtype=np.int32)
+    _check(_load().oracle_verify_recover_filtered(
+        _ptr(z), kp1 * V, _ptr(d), Pd * V, dt, B, k, V, _ptr(x), _ptr(T), K, _ptr(tp),
+        _ptr(u_acc), _ptr(u_smp), int(f64_uniforms), _ptr(acc), _ptr(pax), _ptr(qax),
+        _ptr(out)), "verify_recover_filtered")
     return {"accept_len": acc, "p_at_x": pax, "q_at_x": qax, "out_tok": out}
 
 

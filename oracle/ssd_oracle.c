@@ -42,6 +42,12 @@
  *   R7 sentinels: T < 0 or NaN -> accept_len -1; a draft token outside [0,V)
  *      -> accept_len -2; a NaN logit in any row read (or, for T > 0, a +inf
  *      logit or an all -inf row) -> accept_len -1.  Out tokens are then -1.
+ *   R9 top-k / top-p filtered distributions (both the target's and the
+ *      draft's, with the same K and top_p): order the tokens by (logit
+ *      descending, index ascending); keep the first K; then keep the shortest
+ *      prefix of those whose probability mass is >= top_p times their mass;
+ *      renormalise over what is kept.  Acceptance, the residual and the bonus
+ *      draw then use the filtered p and q; greedy rows are unchanged.
  *   R8 draft-side sampling: the drafter's token at T > 0 is the Gumbel-max
  *      draw argmax_v (z_v / T + G_v), G_v = -ln(-ln u_v), which is exactly a
  *      draw from softmax(z / T); u_v comes from the counter-based generator
@@ -194,8 +200,52 @@ int oracle_softmax_temp(const void *logits, int dtype, int rows, int64_t V,
     return ORACLE_OK;
 }
 
+/* Top-k / top-p filter of one row's probabilities p (reading R9), in
+ * place: the first K tokens in (z descending, index ascending) order, then
+ * the shortest prefix of them holding >= top_p of their mass, renormalised;
+ * every other token gets 0.  `sel` is scratch for K indices and `taken` for
+ * V flags. */
+static void filter_topk_topp(const double *z, double *p, int64_t V, int K, double top_p,
+                             int64_t *sel, char *taken)
+{
+    memset(taken, 0, (size_t)V);
+    int n = 0;
+    for (; n < K; ++n) {
+        int64_t best = -1;
+        for (int64_t v = 0; v < V; ++v)
+            if (!taken[v] && (best < 0 || z[v] > z[best]))
+                best = v;
+        if (best < 0)
+            break;
+        taken[best] = 1;
+        sel[n] = best;
+    }
+    double mass = 0.0;
+    for (int j = 0; j < n; ++j)
+        mass += p[sel[j]];
+    int keep = n;
+    if (top_p < 1.0) {
+        double c = 0.0;
+        for (int j = 0; j < n; ++j) {
+            c += p[sel[j]];
+            if (c >= top_p * mass) {
+                keep = j + 1;
+                break;
+            }
+        }
+    }
+    double kept = 0.0;
+    for (int j = 0; j < keep; ++j)
+        kept += p[sel[j]];
+    memset(taken, 0, (size_t)V);
+    for (int j = 0; j < keep; ++j)
+        taken[sel[j]] = 1;
+    for (int64_t v = 0; v < V; ++v)
+        p[v] = taken[v] ? p[v] / kept : 0.0;
+}
+
 /*
- * oracle_verify_recover_f64: one verify-and-recover step for B batch rows,
+ * verify_core / oracle_verify_recover_f64: one verify-and-recover step for B batch rows,
  * with the uniforms in double precision (the core; the binary32 entry point
  * below widens its uniforms and calls this).
  *
@@ -210,15 +260,14 @@ int oracle_softmax_temp(const void *logits, int dtype, int rows, int64_t V,
  * position, first rejection n, then one draw from the residual (n < k) or
  * from the target's last row (n == k).
  */
-int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
-                              int64_t d_bstride, int dtype, int B, int k,
-                              int64_t V, const int32_t *x, const float *T,
-                              const double *u_acc, const double *u_smp,
-                              int32_t *accept_len, double *p_at_x,
-                              double *q_at_x, int32_t *out_tok)
+/* The core; K == 0 filters nothing (R9 otherwise, top_p may be NULL). */
+static int verify_core(const void *Z, int64_t z_bstride, const void *D, int64_t d_bstride,
+                       int dtype, int B, int k, int64_t V, const int32_t *x, const float *T,
+                       int K, const float *top_p, const double *u_acc, const double *u_smp,
+                       int32_t *accept_len, double *p_at_x, double *q_at_x, int32_t *out_tok)
 {
     if (!Z || !D || !x || !T || !u_acc || !u_smp || !accept_len || !out_tok ||
-        B < 0 || k < 1 || V < 1)
+        B < 0 || k < 1 || V < 1 || K < 0)
         return ORACLE_BAD_ARG;
     double *zrow = (double *)malloc((size_t)V * sizeof(double));
     double *drow = (double *)malloc((size_t)V * sizeof(double));
@@ -226,13 +275,17 @@ int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
     double *q = (double *)malloc((size_t)V * sizeof(double));
     double *w = (double *)malloc((size_t)V * sizeof(double));
     int *accepted = (int *)malloc((size_t)k * sizeof(int));
-    if (!zrow || !drow || !p || !q || !w || !accepted) {
-        free(zrow); free(drow); free(p); free(q); free(w); free(accepted);
+    int64_t *sel = (int64_t *)malloc((size_t)(K > 0 ? K : 1) * sizeof(int64_t));
+    char *taken = (char *)malloc((size_t)V);
+    if (!zrow || !drow || !p || !q || !w || !accepted || !sel || !taken) {
+        free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(sel);
+        free(taken);
         return ORACLE_NO_MEMORY;
     }
 
     for (int b = 0; b < B; ++b) {
         double t = (double)T[b];
+        const double pb = top_p ? (double)top_p[b] : 1.0;
         int32_t *out = out_tok + (int64_t)b * (k + 1);
         for (int j = 0; j <= k; ++j)
             out[j] = -1;
@@ -285,6 +338,10 @@ int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
                 double m, S;
                 softmax_temp(zrow, V, t, p, &m, &S);
                 softmax_temp(drow, V, t, q, &m, &S);
+                if (K > 0) {
+                    filter_topk_topp(zrow, p, V, K, pb, sel, taken);
+                    filter_topk_topp(drow, q, V, K, pb, sel, taken);
+                }
                 pi = p[xi];
                 qi = q[xi];
                 /* R2: accept with probability min(1, p/q) against u. */
@@ -315,9 +372,13 @@ int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
         } else {
             double m, S;
             softmax_temp(zrow, V, t, p, &m, &S);
+            if (K > 0)
+                filter_topk_topp(zrow, p, V, K, pb, sel, taken);
             if (n < k) {
                 load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)n * V, V, drow);
                 softmax_temp(drow, V, t, q, &m, &S);
+                if (K > 0)
+                    filter_topk_topp(drow, q, V, K, pb, sel, taken);
                 double total = 0.0;
                 for (int64_t v = 0; v < V; ++v) {
                     double d = p[v] - q[v];
@@ -340,8 +401,50 @@ int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
         out[n] = (int32_t)tok;
     }
 
-    free(zrow); free(drow); free(p); free(q); free(w); free(accepted);
+    free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(sel); free(taken);
     return ORACLE_OK;
+}
+
+int oracle_verify_recover_f64(const void *Z, int64_t z_bstride, const void *D,
+                              int64_t d_bstride, int dtype, int B, int k,
+                              int64_t V, const int32_t *x, const float *T,
+                              const double *u_acc, const double *u_smp,
+                              int32_t *accept_len, double *p_at_x,
+                              double *q_at_x, int32_t *out_tok)
+{
+    return verify_core(Z, z_bstride, D, d_bstride, dtype, B, k, V, x, T, 0, NULL, u_acc,
+                       u_smp, accept_len, p_at_x, q_at_x, out_tok);
+}
+
+/* The step over top-k / top-p filtered distributions (R9), binary32 or
+ * double uniforms (f64 != 0). */
+int oracle_verify_recover_filtered(const void *Z, int64_t z_bstride, const void *D,
+                                   int64_t d_bstride, int dtype, int B, int k, int64_t V,
+                                   const int32_t *x, const float *T, int K, const float *top_p,
+                                   const void *u_acc, const void *u_smp, int f64,
+                                   int32_t *accept_len, double *p_at_x, double *q_at_x,
+                                   int32_t *out_tok)
+{
+    if (K < 1 || !u_acc || !u_smp)
+        return ORACLE_BAD_ARG;
+    if (f64)
+        return verify_core(Z, z_bstride, D, d_bstride, dtype, B, k, V, x, T, K, top_p,
+                           (const double *)u_acc, (const double *)u_smp, accept_len, p_at_x,
+                           q_at_x, out_tok);
+    double *ua = (double *)malloc((size_t)(B > 0 ? B : 1) * (size_t)k * sizeof(double));
+    double *us = (double *)malloc((size_t)(B > 0 ? B : 1) * sizeof(double));
+    if (!ua || !us) {
+        free(ua); free(us);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t j = 0; j < (int64_t)B * k; ++j)
+        ua[j] = (double)((const float *)u_acc)[j];
+    for (int b = 0; b < B; ++b)
+        us[b] = (double)((const float *)u_smp)[b];
+    int rc = verify_core(Z, z_bstride, D, d_bstride, dtype, B, k, V, x, T, K, top_p, ua, us,
+                         accept_len, p_at_x, q_at_x, out_tok);
+    free(ua); free(us);
+    return rc;
 }
 
 /* The same step with binary32 uniforms, as the GPU library takes them. */

@@ -153,15 +153,31 @@ def _split(pred):
     return m, (t_pt if m > 0 else None), (f_pt if m < 1 else None)
 
 
-def enumerate_output_distribution(Z, D, T):
+def enumerate_output_distribution(Z, D, T, call=None, filt=None):
     """Exact law of the 3-token sequence produced by the oracle (one verify
     round, then completion from the target rows), draft tokens drawn from q.
     Acceptance probabilities are the measures of the accepting uniforms and
     token laws come from the break points of the oracle's draw as a function
-    of u_smp, all located by bisection on the oracle itself."""
+    of u_smp, all located by bisection on the oracle itself.  `call` replaces
+    the oracle entry point and `filt(z_row, p_row)` the distributions (for
+    the filtered step)."""
+    global _call
     V = Z.shape[1]
     p = softmax_ref(Z.astype(np.float64), T)
     q = softmax_ref(D.astype(np.float64), T)
+    if filt is not None:
+        p = np.stack([filt(Z[i], p[i]) for i in range(p.shape[0])])
+        q = np.stack([filt(D[i], q[i]) for i in range(q.shape[0])])
+    saved = _call
+    if call is not None:
+        _call = call
+    try:
+        return _enumerate(Z, D, T, V, p, q)
+    finally:
+        _call = saved
+
+
+def _enumerate(Z, D, T, V, p, q):
     law = np.zeros((V,) * 3)
     for x0, x1 in itertools.product(range(V), repeat=2):
         wx = q[0, x0] * q[1, x1]
@@ -194,6 +210,73 @@ def test_exactness_by_enumeration(seed, T):
     target = np.einsum("i,j,k->ijk", p[0], p[1], p[2])
     assert abs(law.sum() - 1.0) < 1e-12
     assert np.max(np.abs(law - target)) < 1e-12
+
+
+def _filter_ref(z, p, K, top_p):
+    """R9 written out independently: order by (logit desc, index asc), keep the
+    first K, then the shortest prefix holding >= top_p of their mass."""
+    order = sorted(range(len(z)), key=lambda v: (-float(z[v]), v))[:K]
+    mass = sum(p[v] for v in order)
+    keep, c = [], 0.0
+    for v in order:
+        keep.append(v)
+        c += p[v]
+        if c >= top_p * mass:
+            break
+    out = np.zeros_like(p)
+    kept = sum(p[v] for v in keep)
+    for v in keep:
+        out[v] = p[v] / kept
+    return out
+
+
+@pytest.mark.parametrize("K,top_p", [(3, 1.0), (4, 0.7), (2, 0.5)])
+def test_filtered_exactness_by_enumeration(K, top_p):
+    """Over top-k / top-p filtered distributions the step reproduces the
+    filtered target law exactly (V = 5, k = 2)."""
+    rng = np.random.default_rng(7 + K)
+    T = float(np.float32(0.9))
+    Z = (rng.standard_normal((3, 5)) * 1.5).astype(np.float32)
+    D = (Z[:2] + rng.standard_normal((2, 5))).astype(np.float32)
+
+    def call(Z_, D_, x, T_, ua, us):
+        r = oracle.verify_recover_filtered(Z_[None], D_[None], np.asarray(x, np.int32)[None], [T_],
+                                           K, [top_p], np.asarray(ua, np.float64)[None], [us],
+                                           f64_uniforms=True)
+        return int(r["accept_len"][0]), [int(t) for t in r["out_tok"][0]]
+
+    filt = lambda z, p: _filter_ref(z, p, K, top_p)
+    law, p, q = enumerate_output_distribution(Z, D, T, call=call, filt=filt)
+    target = np.einsum("i,j,k->ijk", p[0], p[1], p[2])
+    assert abs(law.sum() - 1.0) < 1e-12
+    assert np.max(np.abs(law - target)) < 1e-12
+    assert (p > 0).sum(axis=1).max() <= K
+
+
+def test_filtered_reduces_to_unfiltered_and_probabilities():
+    rng = np.random.default_rng(5)
+    B, k, V = 6, 3, 12
+    Z = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    D = (Z[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    x = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    T = np.array([1.0, 0.7, 0.0, 1.3, 0.9, 0.5], np.float32)
+    ua = rng.random((B, k)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    plain = oracle.verify_recover(Z, D, x, T, ua, us)
+    full = oracle.verify_recover_filtered(Z, D, x, T, V, None, ua, us)
+    for key in ("accept_len", "out_tok"):
+        assert np.array_equal(plain[key], full[key])
+    assert np.allclose(plain["p_at_x"], full["p_at_x"], atol=1e-15, equal_nan=True)
+    K, tp = 4, np.full(B, 0.8, np.float32)
+    r = oracle.verify_recover_filtered(Z, D, x, T, K, tp, ua, us)
+    for b in range(B):
+        if T[b] == 0:
+            continue
+        for i in range(k):
+            if i > 0 and r["accept_len"][b] < i:
+                break
+            p = _filter_ref(Z[b, i], softmax_ref(Z[b, i].astype(np.float64)[None], T[b])[0], K, 0.8)
+            assert abs(r["p_at_x"][b, i] - p[x[b, i]]) < 1e-12
 
 
 def test_exactness_detects_a_wrong_residual():
