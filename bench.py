@@ -271,6 +271,37 @@ def draft_pipeline(ssd, w, inp, dev, reps=50):
             "verify_drafted_stream_gbs": round(row / (t_v / 1e3) / 1e9, 1)}
 
 
+def topk_verify(ssd, w, inp, dev, K=32, top_p=0.9, reps=50):
+    """Verify over top-K / top-p filtered distributions on the same workload
+    (one pass over the 2k+1 rows, no exponentials in it; the rest on at most
+    K candidates per row).  Milliseconds per call and the pass's GB/s."""
+    import torch
+    D = inp["D"][:, : w.k].contiguous()
+    tp = torch.full((w.B,), top_p, dtype=torch.float32, device=dev)
+    out = {}
+    ws = ssd.new_workspace(ssd.load_library().ssd_topk_workspace_bytes(w.B, w.k, w.V, K), dev)
+
+    def call():
+        ssd.ssd_verify_topk(inp["Z"], D, inp["x"], inp["T"], K, tp, inp["u_acc"], inp["u_smp"],
+                            ws=ws, out=out)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = w.B * (2 * w.k + 1) * w.V * 4
+    return {"K": K, "top_p": top_p, "ms": round(ms, 4),
+            "rows_per_s": round(w.B / (ms / 1e3), 1),
+            "stream_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+
+
 def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
     """Time the oracle (as it stands, one host thread) on a bounded sample of
     the batch rows: verify_recover + forked_topf + the dict cache."""
@@ -395,6 +426,7 @@ def gpu_arm(args):
     if rank == 0 and world == 1:
         line["latency_b1"] = b1_latency(ssd, W, dev)
         line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)
+        line["topk_verify"] = topk_verify(ssd, w, inp, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
     if rank == 0:

@@ -322,6 +322,29 @@ SSD_API ssd_status ssd_verify_drafted(const void *Z, int64_t z_bstride, const vo
                               size_t ws_bytes, ssd_stream_t stream);
 
 /*
+ * ssd_verify_topk -- ssd_verify over top-k / top-p filtered distributions:
+ * the target rows and the draft rows are filtered alike (order the tokens by
+ * logit descending, index ascending; keep the first K; keep the shortest
+ * prefix of those holding >= top_p[b] of their probability mass;
+ * renormalise), and acceptance, the residual and the bonus draw use the
+ * filtered p and q.  Greedy rows (T == 0) are unaffected.  One pass over the
+ * 2k+1 rows keeps per-chunk top-K lists (no exponentials); the rest works
+ * on at most K candidates per row, in extended precision.
+ *   K        : 1 <= K <= 32 (and K <= V).
+ *   top_p    : [B] fp32 device array, or NULL for 1 (no cut).
+ *   other arguments and results as ssd_verify (the draft tokens x must have
+ *   been drawn from the filtered draft distribution for exactness).
+ *   ws       : ssd_topk_workspace_bytes(B, k, V, K) bytes.
+ */
+SSD_API size_t ssd_topk_workspace_bytes(int B, int k, int V, int K);
+SSD_API ssd_status ssd_verify_topk(const void *Z, int64_t z_bstride, const void *D,
+                           int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                           const int32_t *x, const float *T, int K, const float *top_p,
+                           const float *u_acc, int32_t *accept_len, float *p_at_x,
+                           float *q_at_x, const float *u_smp, int32_t *out_tok, void *ws,
+                           size_t ws_bytes, ssd_stream_t stream);
+
+/*
  * Speculation cache ([SSD] roadmap: the speculation cache; [SUM] cache
  * hits and misses).  An open-addressing table on the device mapping the key
  * (b, position, token) to `depth` draft tokens.  Keys compare exactly, so the

@@ -54,6 +54,9 @@ SIGNATURES = [
                               ctypes.c_uint32, _P, _L, _I, _P, _P, _P, _Z, _P]),
     ("ssd_verify_drafted", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P, _Z, _P]),
+    ("ssd_topk_workspace_bytes", _Z, [_I, _I, _I, _I]),
+    ("ssd_verify_topk", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
+                             _P, _P, _P, _Z, _P]),
     ("ssd_spec_cache_create", _I, [_I, _I, _P]),
     ("ssd_spec_cache_destroy", None, [_P]),
     ("ssd_spec_cache_clear", _I, [_P, _P]),
@@ -373,6 +376,40 @@ def ssd_draft_sample(D: torch.Tensor, T: torch.Tensor, k: int, seed: int, offset
         wp, wn, _stream(stream)))
     out["ws"] = ws
     return out
+
+
+def ssd_verify_topk(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
+                    K: int, top_p: Optional[torch.Tensor], u_acc: torch.Tensor,
+                    u_smp: Optional[torch.Tensor] = None, *, ws: Optional[torch.Tensor] = None,
+                    out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """ssd_verify over top-K / top-p filtered target and draft distributions
+    (K <= 32; top_p [B] float32 or None)."""
+    lib = load_library()
+    B, kp1, V = Z.shape
+    k = kp1 - 1
+    if D.dim() != 3 or D.shape[0] != B or D.shape[2] != V or D.shape[1] < k:
+        raise ValueError("D must be [B, >=k, V]")
+    if Z.dtype != D.dtype:
+        raise TypeError("Z and D must share a dtype")
+    _want(x, torch.int32, "x")
+    if top_p is not None:
+        _want(top_p, torch.float32, "top_p")
+    dev = Z.device
+    if ws is None:
+        n = lib.ssd_topk_workspace_bytes(B, k, V, K)
+        if n == 0:
+            raise SSDError("ssd_topk_workspace_bytes", 1)
+        ws = new_workspace(n, dev)
+    wp, wn = _ws_ptr(ws)
+    o = _verify_outputs(B, k, dev, out, u_smp is not None)
+    _check("ssd_verify_topk", lib.ssd_verify_topk(
+        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), D.shape[1] * V, _dtype_code(Z), B, k, V,
+        _dev(x, "x"), _dev(T, "T"), K, _opt(top_p, "top_p"), _dev(u_acc, "u_acc"),
+        _dev(o["accept_len"], "accept_len"), _dev(o["p_at_x"], "p_at_x"),
+        _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"), _dev(o["out_tok"], "out_tok"),
+        wp, wn, _stream(stream)))
+    o["ws"] = ws
+    return o
 
 
 class SpecCache:

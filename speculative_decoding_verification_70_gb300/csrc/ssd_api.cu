@@ -20,6 +20,8 @@ cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s);
 cudaError_t launch_draft(const StatsParams& p, int B, int dtype, bool vec, int rows, bool topf,
                          cudaStream_t s);
 cudaError_t launch_draft_finalize(const DraftParams& p, cudaStream_t s);
+cudaError_t launch_topk_verify(const TopkParams& p, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_topk_finalize(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
@@ -565,6 +567,52 @@ ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, i
   dp.err = sp.err;
   ProfScope ps("draft_finalize", S(stream));
   return cuda_status(launch_draft_finalize(dp, S(stream)));
+}
+
+size_t ssd_topk_workspace_bytes(int B, int k, int V, int K) {
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || K < 1 || K > kMaxTopK || K > V) return 0;
+  return make_topk_layout(B, k, V, K).total;
+}
+
+ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                           ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
+                           int K, const float* top_p, const float* u_acc, int32_t* accept_len,
+                           float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
+                           void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!Z || !D || !x || !T || !u_acc || !accept_len || !ws) return SSD_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (K < 1 || K > kMaxTopK || K > V) return SSD_ERR_INVALID_ARG;
+  if ((p_at_x == nullptr) != (q_at_x == nullptr)) return SSD_ERR_INVALID_ARG;
+  if (u_smp && !out_tok) return SSD_ERR_INVALID_ARG;
+  if (z_bstride < static_cast<int64_t>(k + 1) * V || d_bstride < static_cast<int64_t>(k) * V)
+    return SSD_ERR_INVALID_ARG;
+  if (!aligned(Z, esize(dtype)) || !aligned(D, esize(dtype)) || !aligned(ws, 256))
+    return SSD_ERR_INVALID_ARG;
+  const TopkLayout L = make_topk_layout(B, k, V, K, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(Z, z_bstride, V, dtype) && vec_ok(D, d_bstride, V, dtype);
+  TopkParams tp;
+  memset(&tp, 0, sizeof tp);
+  tp.Z = Z; tp.zb = z_bstride; tp.D = D; tp.db = d_bstride;
+  tp.dtype = dtype == SSD_BF16 ? 1 : 0;
+  tp.B = B; tp.k = k; tp.V = V; tp.C = L.ch.C; tp.CH = L.ch.CH; tp.R = L.R; tp.K = K;
+  tp.G = 1;
+  while (tp.G < 4 && static_cast<long long>(B) * L.R * ((tp.C + 2 * tp.G - 1) / (2 * tp.G)) >= 2432)
+    tp.G *= 2;
+  tp.T = T; tp.top_p = top_p; tp.x = x; tp.u_acc = u_acc; tp.u_smp = u_smp;
+  tp.accept_len = accept_len; tp.p_at_x = p_at_x; tp.q_at_x = q_at_x; tp.out_tok = out_tok;
+  tp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  tp.lists = reinterpret_cast<TopEntry*>(wsp(ws, L.lists));
+  tp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  cudaError_t e;
+  {
+    ProfScope ps("topk_pass", S(stream));
+    e = launch_topk_verify(tp, tp.dtype, vec, S(stream));
+  }
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  ProfScope ps("topk_finalize", S(stream));
+  return cuda_status(launch_topk_finalize(tp, S(stream)));
 }
 
 ssd_status ssd_verify_fork_fanout(const void* Z, int64_t z_bstride, const void* D,

@@ -130,6 +130,37 @@ struct ResidualParams {
   int32_t* out_tok;    // [B][k+1]
 };
 
+// Top-k / top-p filtered verify (ssd_verify_topk).
+constexpr int kMaxTopK = 32;
+
+struct TopkLayout {
+  size_t err, part, lists, total;
+  int R;          // rows per batch row: k+1 target, k draft
+  Chunking ch;
+};
+
+struct TopkParams {
+  const void* Z; int64_t zb;
+  const void* D; int64_t db;
+  int dtype;           // 0 f32, 1 bf16
+  int B, k, V, C, CH, R, K, G;
+  int b0;              // first batch row of this launch
+  const float* T;
+  const float* top_p;  // [B] or null (1)
+  const int32_t* x;
+  const float* u_acc;
+  const float* u_smp;  // may be null (no draw)
+  int32_t* accept_len;
+  float* p_at_x;
+  float* q_at_x;
+  int32_t* out_tok;
+  PartStat* part;      // [B][R][C]
+  TopEntry* lists;     // [B][R][C][K]
+  int* err;
+};
+
+inline TopkLayout make_topk_layout(int B, int k, int V, int K, int esize = 4);
+
 // Merge of the draft-side sampling pass: one warp per (b, draft row).
 struct DraftParams {
   int B, V, C, Rp, Pz, Pf, row0, rows;
@@ -258,6 +289,19 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
   L.gpart = off;                    off = align256(off + sizeof(GumbelPart) * B * L.Pf * C);
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
+  L.total = off;
+  return L;
+}
+
+inline TopkLayout make_topk_layout(int B, int k, int V, int K, int esize) {
+  TopkLayout L;
+  L.R = 2 * k + 1;
+  L.ch = make_chunking(B, 2 * (k + 1), V, esize);
+  const size_t C = static_cast<size_t>(L.ch.C);
+  size_t off = 0;
+  L.err = off;                      off = align256(off + 16);
+  L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
+  L.lists = off;                    off = align256(off + sizeof(TopEntry) * B * L.R * C * K);
   L.total = off;
   return L;
 }
