@@ -21,6 +21,9 @@ cudaError_t launch_draft(const StatsParams& p, int B, int dtype, bool vec, int r
                          cudaStream_t s);
 cudaError_t launch_draft_finalize(const DraftParams& p, cudaStream_t s);
 cudaError_t launch_topk_verify(const TopkParams& p, int dtype, bool vec, cudaStream_t s);
+#ifndef SSD_TOPK_MAX_GROUP
+#define SSD_TOPK_MAX_GROUP 32
+#endif
 cudaError_t launch_topk_finalize(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
@@ -597,8 +600,11 @@ ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int6
   tp.Z = Z; tp.zb = z_bstride; tp.D = D; tp.db = d_bstride;
   tp.dtype = dtype == SSD_BF16 ? 1 : 0;
   tp.B = B; tp.k = k; tp.V = V; tp.C = L.ch.C; tp.CH = L.ch.CH; tp.R = L.R; tp.K = K;
+  // chunk groups up to a whole row per CTA while the grid keeps ~16 CTAs per
+  // SM: the end-of-CTA selection (K rounds) is then paid once per row
   tp.G = 1;
-  while (tp.G < 4 && static_cast<long long>(B) * L.R * ((tp.C + 2 * tp.G - 1) / (2 * tp.G)) >= 2432)
+  while (tp.G < SSD_TOPK_MAX_GROUP && tp.G < tp.C &&
+         static_cast<long long>(B) * L.R * ((tp.C + 2 * tp.G - 1) / (2 * tp.G)) >= 2432)
     tp.G *= 2;
   tp.T = T; tp.top_p = top_p; tp.x = x; tp.u_acc = u_acc; tp.u_smp = u_smp;
   tp.accept_len = accept_len; tp.p_at_x = p_at_x; tp.q_at_x = q_at_x; tp.out_tok = out_tok;
