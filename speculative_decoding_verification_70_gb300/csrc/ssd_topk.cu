@@ -32,7 +32,14 @@ namespace {
 
 constexpr int kPer = 4;  // candidates kept by each thread
 
+constexpr int kSecond = 256;  // entries of the second-chance buffer
+
 struct PassSmem {
+  float lv[kMaxTopK];          // the candidates' top K (sorted)
+  int li[kMaxTopK];
+  float xv[kSecond];           // second chance: elements of overflowing threads
+  int xi[kSecond];
+  int nx;
   float wl[kWarps][kMaxTopK];  // each warp's sorted top K
   int wi[kWarps][kMaxTopK];
   float w5[kWarps];
@@ -212,8 +219,9 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
   // certified: every element outside the candidates is <= M5, and at least K
   // candidates exceed it (or nothing finite lies outside the candidates)
   const bool certified = sm.cnt >= p.K || M5 == -INFINITY;
-  if (certified) {
-    // each warp: the K best of its 128 candidates (four per lane, registers)
+  // the K best candidates: each warp ranks its 128 (four per lane, in
+  // registers), then warp 0 merges the eight sorted lists
+  {
     float t[kPer];
     int ix[kPer];
 #pragma unroll
@@ -247,9 +255,10 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
           }
       }
     }
-    __syncthreads();
-    if (warp != 0) return;
-    // warp 0: merge the eight sorted lists (lane w < 8 holds list w's head)
+  }
+  if (tid == 0) sm.nx = 0;
+  __syncthreads();
+  if (warp == 0) {
     int head = 0;
     for (int rr = 0; rr < p.K; ++rr) {
       float hv = -INFINITY;
@@ -263,13 +272,76 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
       warp_argmax(wv, wi);
       if (wi != kIdxNone && wi == hi2) ++head;
       if (lane == 0) {
-        out_list[rr].v = wv;
-        out_list[rr].i = wi;
+        sm.lv[rr] = wv;
+        sm.li[rr] = wi;
       }
+    }
+  }
+  __syncthreads();
+  if (certified) {
+    for (int q = tid; q < p.K; q += kThreads) {
+      out_list[q].v = sm.lv[q];
+      out_list[q].i = sm.li[q];
     }
     return;
   }
-  // rare: K rounds of a block-wide arg-max over the group's elements
+  // Second chance (rare; e.g. several of a row's top logits in one vector).
+  // With tau the candidates' K-th best, every element of the true top K
+  // that is not a candidate ranks before tau and lies in a thread whose
+  // fifth value b5 is >= tau: those threads re-read their own elements and
+  // add the ones ranking before tau; the top K of the candidates' list and
+  // these extras is exact.
+  const float tv = sm.lv[p.K - 1];
+  const int ti = sm.li[p.K - 1];
+  bool second = ti != kIdxNone;
+  if (second && st.b5 >= tv) {
+    for (int v = v0 + tid; v < v1; v += kThreads) {
+      float z[8];
+      if (VEC) Tag::loadv_cached(row + static_cast<int64_t>(v) * kV, z);
+      else z[0] = Tag::load1(row + v);
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        const int idx = v * kV + e;
+        const bool own = idx == st.i[0] || idx == st.i[1] || idx == st.i[2] || idx == st.i[3];
+        if (!own && z[e] > -INFINITY && ranks_before(z[e], idx, tv, ti)) {
+          const int q = atomicAdd(&sm.nx, 1);
+          if (q < kSecond) {
+            sm.xv[q] = z[e];
+            sm.xi[q] = idx;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int nx = sm.nx;
+  if (second && nx <= kSecond) {
+    if (warp != 0) return;
+    float pv = INFINITY;
+    int pi = -1;
+    for (int rr = 0; rr < p.K; ++rr) {
+      float bv = -INFINITY;
+      int bi = kIdxNone;
+      for (int q = lane; q < p.K + nx; q += 32) {
+        const float ev = q < p.K ? sm.lv[q] : sm.xv[q - p.K];
+        const int ei = q < p.K ? sm.li[q] : sm.xi[q - p.K];
+        if (ei != kIdxNone && ranks_before(pv, pi, ev, ei) && ranks_before(ev, ei, bv, bi)) {
+          bv = ev;
+          bi = ei;
+        }
+      }
+      warp_argmax(bv, bi);
+      if (lane == 0) {
+        out_list[rr].v = bi == kIdxNone ? -INFINITY : bv;
+        out_list[rr].i = bi;
+      }
+      pv = bv;
+      pi = bi;
+    }
+    return;
+  }
+  // last resort (the list was short or the buffer overflowed): K rounds of
+  // a block-wide arg-max over the group's elements
   float pv = INFINITY;
   int pi = -1;
   for (int rr = 0; rr < p.K; ++rr) {

@@ -109,3 +109,61 @@ def test_verify_topk_full_vocab_equals_plain_verify(gpu_lib):
     assert torch.equal(a["accept_len"], b["accept_len"])
     assert torch.equal(a["out_tok"], b["out_tok"])
     assert torch.allclose(a["p_at_x"], b["p_at_x"], atol=1e-6)
+
+
+def test_verify_topk_clustered_top_logits(gpu_lib):
+    """Top logits packed into one thread's vectors: certification from the
+    threads' top-4 lists fails and the pass takes its second chance (row 0:
+    six top logits at indices 0-3, 1024, 2048) or, when one thread holds
+    hundreds of them, its last resort (row 1: every index = 0..3 mod 1024)."""
+    B, k, V, K = 4, 2, 151936, 32
+    g = torch.Generator().manual_seed(9)
+    Z = torch.randn((B, k + 1, V), generator=g)
+    D = torch.randn((B, k, V), generator=g)
+    hot0 = torch.tensor([0, 1, 2, 3, 1024, 2048])
+    idx = torch.arange(V)
+    hot1 = idx[(idx % 1024) < 4]
+    for t in (Z, D):
+        t[0, :, hot0] = 20.0 + torch.arange(len(hot0)).float() * 0.01
+        t[1, :, hot1] = 10.0 + torch.rand((t.shape[1], len(hot1)), generator=g)
+    x = torch.stack([hot0[:k], hot1[5:5 + k], torch.tensor([7, 9]), torch.tensor([11, 13])]).int()
+    T = torch.tensor([1.0, 0.8, 1.0, 0.6])
+    ua = torch.rand((B, k), generator=g)
+    us = torch.rand(B, generator=g)
+    inp = {"Z": Z, "D": D, "T": T, "u_acc": ua, "u_smp": us}
+    for tp in (None, 0.7):
+        top_p = None if tp is None else torch.full((B,), tp)
+        out = gpu_lib.ssd_verify_topk(Z.to(DEV), D.to(DEV), x.to(DEV), T.to(DEV), K,
+                                      None if top_p is None else top_p.to(DEV), ua.to(DEV),
+                                      us.to(DEV))
+        torch.cuda.synchronize()
+        _check(inp, x, K, top_p, out)
+        assert gpu_lib.get_device_error(out["ws"]) == 0
+
+
+def test_verify_topk_last_resort(gpu_lib):
+    """B = 512 makes a CTA cover a whole row (593 elements per thread); in
+    row 3 one thread holds all 596 top logits (every index = 0..3 mod 1024),
+    more than the second-chance buffer takes, so the exact K-round re-scan
+    runs.  Rows 3 and 100 are compared with the oracle."""
+    B, k, V, K = 512, 2, 151936, 32
+    g = torch.Generator(device=DEV).manual_seed(4)
+    Z = torch.randn((B, k + 1, V), generator=g, device=DEV)
+    D = torch.randn((B, k, V), generator=g, device=DEV)
+    idx = torch.arange(V, device=DEV)
+    hot = idx[(idx % 1024) < 4]
+    Z[3, :, hot] = 10.0 + torch.rand((k + 1, len(hot)), generator=g, device=DEV)
+    D[3, :, hot] = 10.0 + torch.rand((k, len(hot)), generator=g, device=DEV)
+    x = torch.randint(0, V, (B, k), generator=g, device=DEV, dtype=torch.int32)
+    x[3] = hot[:k].int()
+    T = torch.full((B,), 0.9, device=DEV)
+    ua = torch.rand((B, k), generator=g, device=DEV)
+    us = torch.rand(B, generator=g, device=DEV)
+    out = gpu_lib.ssd_verify_topk(Z, D, x, T, K, None, ua, us)
+    torch.cuda.synchronize()
+    rows = [3, 100]
+    sub = {"Z": Z[rows].cpu(), "D": D[rows].cpu(), "T": T[rows].cpu(), "u_acc": ua[rows].cpu(),
+           "u_smp": us[rows].cpu()}
+    got = {key: out[key][rows] for key in ("accept_len", "out_tok", "p_at_x", "q_at_x")}
+    _check(sub, x[rows].cpu(), K, None, got)
+    assert gpu_lib.get_device_error(out["ws"]) == 0
