@@ -124,9 +124,14 @@ constexpr int kMaxF = 16;
 
 // Top-f scratch: every thread's maximum, the warps' largest second values
 // and the selection.
+constexpr int kTopfSecond = 256;  // entries of the second-chance buffer
+
 struct TopfScratch {
   float cv[kThreads];
   int ci[kThreads];
+  float xv[kTopfSecond];           // second chance: elements of overflowing threads
+  int xi[kTopfSecond];
+  int nx;
   float w2[kWarps];
   float sv[kMaxF];
   int si[kMaxF];
@@ -177,25 +182,31 @@ __device__ __forceinline__ void topf_post(const ScanState& st, const int* msk, i
 }
 
 // Top f of the CTA's elements (logit descending, index ascending, masked
-// tokens and NaN skipped), certified: with M2 the largest second value of
-// any thread, every element that is not a thread maximum is at most M2, so
-// if at least f unmasked thread maxima exceed M2 the top f are thread
-// maxima and warp 0 picks them from the 256 posted candidates while the
-// other warps leave.  Otherwise (rare; ties included) the exact selection is
-// redone over [lo, hi) by f rounds of a block-wide arg-max.  Needs
+// tokens and NaN skipped).  Warp 0 picks the f best of the 256 posted thread
+// maxima.  Certified: with M2 the largest second value of any thread, every
+// element that is not a thread maximum is at most M2, so if at least f
+// unmasked maxima exceed M2 the picks are exact.  Otherwise (a few percent
+// of CTAs; e.g. several top logits in one vector) a second chance: with tau
+// the f-th pick, every missing element ranks before tau and sits in a thread
+// whose second value is >= tau, so only those threads re-read their own
+// elements and add the ones ranking before tau; the f best of the picks and
+// these extras are exact.  A NaN, fewer than f picks or an overflowing
+// buffer take the last resort: f rounds of a block-wide arg-max.  Needs
 // topf_post and a barrier before it.
 template <typename Tag, bool VEC>
 __device__ void topf_select(const StatsParams& p, const ScanState& st,
                             const typename Tag::Elem* row, int lo, int hi, const int* msk,
                             TopEntry* out_top, int n_slots, TopfScratch& ts) {
+  constexpr int kV = VEC ? Tag::kVec : 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int f = p.f, M = p.M;
   float M2 = ts.w2[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) M2 = max_nan(M2, ts.w2[w]);
   const bool cand = ts.ci[tid] != kIdxNone && ts.cv[tid] > M2;  // false when M2 is NaN
-  if (__syncthreads_count(cand) >= f) {
-    if (warp != 0) return;
+  if (tid == 0) ts.nx = 0;
+  const bool certified = __syncthreads_count(cand) >= f;
+  if (warp == 0) {
     float pv = INFINITY;
     int pi = -1;
     for (int r = 0; r < f; ++r) {
@@ -218,9 +229,12 @@ __device__ void topf_select(const StatsParams& p, const ScanState& st,
       pv = bv;
       pi = bi;
     }
+  }
+  // the group's list goes to its first chunk slot; the other slots of the
+  // group get empty entries, which rank last in the merge
+  if (certified) {
+    if (warp != 0) return;
     __syncwarp();
-    // the group's list goes to its first chunk slot; the other slots of the
-    // group get empty entries, which rank last in the merge
     for (int q = lane; q < n_slots * f; q += 32) {
       const int slot = q / f, r = q % f;
       out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
@@ -228,6 +242,71 @@ __device__ void topf_select(const StatsParams& p, const ScanState& st,
     }
     return;
   }
+  __syncthreads();
+  const float tv = ts.sv[f - 1];
+  const int ti = ts.si[f - 1];
+  const bool second = ti != kIdxNone && M2 == M2;
+  if (second && st.m2 >= tv) {
+    const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
+    for (int v = v0 + tid; v < v1; v += kThreads) {
+      float z[8];
+      if (VEC) Tag::loadv_cached(row + static_cast<int64_t>(v) * kV, z);
+      else z[0] = Tag::load1(row + v);
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        const int idx = v * kV + e;
+        if (idx != ts.ci[tid] && z[e] == z[e] && ranks_before(z[e], idx, tv, ti) &&
+            !is_masked(idx, msk, M)) {
+          const int q = atomicAdd(&ts.nx, 1);
+          if (q < kTopfSecond) {
+            ts.xv[q] = z[e];
+            ts.xi[q] = idx;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int nx = ts.nx;
+  if (second && nx <= kTopfSecond) {
+    if (warp != 0) return;
+    float pv = INFINITY;
+    int pi = -1;
+    float keep_v = -INFINITY;
+    int keep_i = kIdxNone;
+    for (int r = 0; r < f; ++r) {
+      float bv = -INFINITY;
+      int bi = kIdxNone;
+      for (int q = lane; q < f + nx; q += 32) {
+        const float v = q < f ? ts.sv[q] : ts.xv[q - f];
+        const int i = q < f ? ts.si[q] : ts.xi[q - f];
+        if (i != kIdxNone && ranks_before(pv, pi, v, i) && ranks_before(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+        }
+      }
+      warp_argmax(bv, bi);
+      if (lane == r) {
+        keep_v = bv;
+        keep_i = bi;
+      }
+      pv = bv;
+      pi = bi;
+    }
+    __syncwarp();
+    if (lane < f) {
+      ts.sv[lane] = keep_i == kIdxNone ? -INFINITY : keep_v;
+      ts.si[lane] = keep_i;
+    }
+    __syncwarp();
+    for (int q = lane; q < n_slots * f; q += 32) {
+      const int slot = q / f, r = q % f;
+      out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
+      out_top[q].i = slot == 0 ? ts.si[r] : kIdxNone;
+    }
+    return;
+  }
+  // last resort: f rounds of a block-wide arg-max over [lo, hi)
   float pv = INFINITY;
   int pi = -1;
   for (int r = 0; r < f; ++r) {
