@@ -155,3 +155,54 @@ def test_oracle_and_cuda_path_share_no_code():
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "speculative_decoding_verification_70_gb300" not in text, f
             assert "ssd.h" not in text, f
+
+
+def test_next_rows_reject_bad_arguments_on_host(lib):
+    """Draft-side sampling, the drafted verify, the filtered verify and the
+    fan-out calls refuse bad arguments before touching CUDA."""
+    INVALID, DTYPE, WS = 1, 2, 6
+    P = 1 << 20
+    big = 1 << 30
+    # ssd_draft_sample(D, d_bstride, dt, B, k, V, row0, rows, T, seed, offset, x, x_bstride,
+    #                  f, fork_tok, fork_logit, ws, ws_bytes, stream)
+    ok = dict(D=P, db=8 * 1000, dt=0, B=2, k=7, V=1000, row0=0, rows=8, T=P, seed=1, off=0,
+              x=P, xb=8, f=0, ft=None, fl=None, ws=P, wsb=big)
+
+    def draft(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.ssd_draft_sample(a["D"], a["db"], a["dt"], a["B"], a["k"], a["V"], a["row0"],
+                                    a["rows"], a["T"], a["seed"], a["off"], a["x"], a["xb"],
+                                    a["f"], a["ft"], a["fl"], a["ws"], a["wsb"], None)
+    assert draft(D=None) == INVALID
+    assert draft(dt=5) == DTYPE
+    assert draft(rows=9) == INVALID                  # row0 + rows > k + 1
+    assert draft(row0=-1) == INVALID
+    assert draft(db=100) == INVALID                  # stride below the rows read
+    assert draft(xb=3) == INVALID                    # x row stride below rows
+    assert draft(f=16) == INVALID                    # f + 1 > 16
+    assert draft(f=2) == INVALID                     # forks without outputs
+    assert draft(wsb=16) == WS
+    assert draft(D=P + 2) == INVALID                 # misaligned
+    # ssd_verify_topk(Z, zb, D, db, dt, B, k, V, x, T, K, top_p, u_acc, acc, p, q, us, out,
+    #                 ws, wsb, stream)
+
+    def topk(K=8, **kw):
+        a = dict(Z=P, zb=3 * 1000, D=P, db=2 * 1000, B=2, k=2, V=1000, ws=P, wsb=big)
+        a.update(kw)
+        return lib.ssd_verify_topk(a["Z"], a["zb"], a["D"], a["db"], 0, a["B"], a["k"], a["V"],
+                                   P, P, K, None, P, P, None, None, None, None, a["ws"],
+                                   a["wsb"], None)
+    assert topk(K=0) == INVALID
+    assert topk(K=33) == INVALID                     # K <= 32
+    assert topk(K=8, V=4) == INVALID                 # K > V
+    assert topk(K=8, zb=10) == INVALID
+    assert topk(K=8, wsb=16) == WS
+    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 33) == 0
+    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 32) > 0
+    # the drafted verify checks like ssd_verify
+    assert lib.ssd_verify_drafted(None, 3000, P, 2000, 0, 2, 2, 1000, P, P, P, P, None, None,
+                                  None, None, P, big, None) == INVALID
+    # fan-out: F as f
+    assert lib.ssd_forked_recovery_fanout(P, 8 * 40, 0, 1, 2, 40, 17, P, None, 0, P, P, P, big,
+                                          None) == INVALID
