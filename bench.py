@@ -2,10 +2,11 @@
 
 One step = the whole hot path on one batch of the large-batch mixed-sampling
 workload (B=512, k=7, f=4, V=151936, fp32 logits, T=0 on half the rows and
-U(0.5,1.2) on the rest): ssd_verify_fork (row statistics, acceptance,
-first-reject prefix, recovery/bonus draw, forked top-f) followed by the
-speculation-cache step (clear, insert the forked recovery tokens, look up each
-row's realised outcome).  The metric is verified batch rows per second; the
+U(0.5,1.2) on the rest): one SSD round through ssd_verify_fork_cache (row
+statistics, acceptance, first-reject prefix, recovery/bonus draw, forked
+top-f, then the speculation-cache step: clear, insert the forked recovery
+tokens -- on a side stream during the draw -- and look up each row's
+realised outcome).  The metric is verified batch rows per second; the
 roofline object reports the achieved HBM bandwidth of the dominant unit, the
 streaming statistics pass (its two kernels run concurrently on two streams and
 are timed together from the fork to the join).
@@ -183,12 +184,13 @@ class Step:
         self.look = None
 
     def __call__(self):
+        # one SSD round: verify + forks, the forks into the (cleared) cache on
+        # a side stream during the recovery draw, the outcome looked up
         i = self.inp
-        o = self.ssd.ssd_verify_fork(i["Z"], i["D"], i["x"], i["T"], i["u_acc"], i["u_smp"],
-                                     self.w.f, i["mask"], ws=self.ws, out=self.out)
-        self.cache.clear()
-        self.cache.insert_forks(o["fork_tok"], self.payload)
-        self.look = self.cache.lookup_outcome(o["accept_len"], o["out_tok"], out=self.look)
+        o = self.ssd.ssd_verify_fork_cache(i["Z"], i["D"], i["x"], i["T"], i["u_acc"],
+                                           i["u_smp"], self.w.f, i["mask"], self.cache,
+                                           self.payload, ws=self.ws, out=self.out)
+        self.look = o
         return o
 
 

@@ -364,6 +364,28 @@ SSD_API ssd_status ssd_spec_cache_create(int capacity, int depth, ssd_spec_cache
 SSD_API void ssd_spec_cache_destroy(ssd_spec_cache *cache);
 SSD_API ssd_status ssd_spec_cache_clear(ssd_spec_cache *cache, ssd_stream_t stream);
 
+/*
+ * ssd_verify_fork_cache -- one SSD round step ([SSD] the drafter keeps
+ * speculations for the likely verification outcomes; a correct guess is
+ * returned at once): ssd_verify_fork, then (after clearing the cache when
+ * clear != 0) the forks go into `cache` keyed (b, position, fork token) with
+ * payload rows payload[((b*(k+1) + j)*f + r) * depth ..], and each row's
+ * realised outcome (accept_len[b], out_tok[b, accept_len[b]]) is looked up:
+ * hit[b] in {0, 1}, tok_out[b, 0..depth) (-1 on a miss).  With B >= 32 the
+ * clear and the insert run on an internal stream while the recovery draw
+ * runs.  Arguments otherwise as ssd_verify_fork (out_tok required); the
+ * cache must live on the current device.
+ */
+SSD_API ssd_status ssd_verify_fork_cache(const void *Z, int64_t z_bstride, const void *D,
+                                 int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                                 const int32_t *x, const float *T, const float *u_acc,
+                                 int32_t *accept_len, float *p_at_x, float *q_at_x,
+                                 const float *u_smp, int32_t *out_tok, int f,
+                                 const int32_t *mask, int M, int32_t *fork_tok,
+                                 float *fork_logit, ssd_spec_cache *cache, int clear,
+                                 const int32_t *payload, int32_t *hit, int32_t *tok_out,
+                                 void *ws, size_t ws_bytes, ssd_stream_t stream);
+
 /* n keys (b[i], pos[i], tok[i]) -> payload[i*depth .. +depth). */
 SSD_API ssd_status ssd_spec_cache_insert(ssd_spec_cache *cache, const int32_t *b,
                                  const int32_t *pos, const int32_t *tok,

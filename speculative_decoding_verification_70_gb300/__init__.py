@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     ssd_softmax_temp,
     ssd_verify,
     ssd_verify_fork,
+    ssd_verify_fork_cache,
     ssd_verify_topk,
     workspace_bytes,
 )

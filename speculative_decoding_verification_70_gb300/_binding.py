@@ -57,6 +57,8 @@ SIGNATURES = [
     ("ssd_topk_workspace_bytes", _Z, [_I, _I, _I, _I]),
     ("ssd_verify_topk", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
                              _P, _P, _P, _Z, _P]),
+    ("ssd_verify_fork_cache", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P]),
     ("ssd_spec_cache_create", _I, [_I, _I, _P]),
     ("ssd_spec_cache_destroy", None, [_P]),
     ("ssd_spec_cache_clear", _I, [_P, _P]),
@@ -306,6 +308,48 @@ def ssd_forked_recovery(L: torch.Tensor, f: int, mask: Optional[torch.Tensor] = 
             _dev(out["fork_logit"], "fork_logit"), wp, wn, _stream(stream)))
     out["ws"] = ws
     return out
+
+
+def ssd_verify_fork_cache(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,
+                          u_acc: torch.Tensor, u_smp: Optional[torch.Tensor], f: int,
+                          mask: Optional[torch.Tensor], cache: "SpecCache",
+                          payload: torch.Tensor, *, clear: bool = True,
+                          ws: Optional[torch.Tensor] = None, out: Optional[dict] = None,
+                          stream=None) -> Dict[str, torch.Tensor]:
+    """One SSD round step: ssd_verify_fork, the forks inserted into `cache`
+    (cleared first when clear) with payload [B*(k+1)*f, depth], and each
+    row's realised outcome looked up: out["hit"] [B], out["tok_out"]
+    [B, depth]."""
+    lib = load_library()
+    B, kp1, V = Z.shape
+    k = kp1 - 1
+    if tuple(D.shape) != (B, kp1, V):
+        raise ValueError("D must be [B, k+1, V] for the fused call")
+    if Z.dtype != D.dtype:
+        raise TypeError("Z and D must share a dtype")
+    _want(x, torch.int32, "x")
+    _want(payload, torch.int32, "payload")
+    if tuple(payload.shape) != (B * kp1 * f, cache.depth):
+        raise ValueError("payload must be [B*(k+1)*f, depth]")
+    M = 0 if mask is None else mask.shape[2]
+    dev = Z.device
+    if ws is None:
+        ws = new_workspace(workspace_bytes(B, k, V, f), dev)
+    wp, wn = _ws_ptr(ws)
+    o = _verify_outputs(B, k, dev, out, True, f, kp1)
+    if "hit" not in o:
+        o["hit"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["tok_out"] = torch.empty((B, cache.depth), dtype=torch.int32, device=dev)
+    _check("ssd_verify_fork_cache", lib.ssd_verify_fork_cache(
+        _dev(Z, "Z"), kp1 * V, _dev(D, "D"), kp1 * V, _dtype_code(Z), B, k, V,
+        _dev(x, "x"), _dev(T, "T"), _dev(u_acc, "u_acc"), _dev(o["accept_len"], "accept_len"),
+        _dev(o["p_at_x"], "p_at_x"), _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"),
+        _dev(o["out_tok"], "out_tok"), f, _opt(mask, "mask"), M,
+        _dev(o["fork_tok"], "fork_tok"), _dev(o["fork_logit"], "fork_logit"), cache._h,
+        int(clear), _dev(payload, "payload"), _dev(o["hit"], "hit"),
+        _dev(o["tok_out"], "tok_out"), wp, wn, _stream(stream)))
+    o["ws"] = ws
+    return o
 
 
 def ssd_verify_fork(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.Tensor,

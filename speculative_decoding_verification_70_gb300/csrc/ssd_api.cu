@@ -137,6 +137,10 @@ struct VerifyCall {
   int f; const int32_t* mask; int M; int32_t* fork_tok; float* fork_logit;
   const int32_t* fanout;  // [k+1] device, or null (f at every position)
   bool drafted;           // draft rows' statistics already in ws (ssd_draft_sample)
+  // SSD round step (ssd_verify_fork_cache): clear + insert the forks, then
+  // look up each row's realised outcome
+  const CacheView* cache; bool cache_clear; const int32_t* payload;
+  int32_t* hit; int32_t* tok_out;
   void* ws; size_t ws_bytes;
   cudaStream_t stream;
   bool single_stream;  // no internal streams (the no-allocation entry point)
@@ -241,7 +245,7 @@ struct DevStreams {
   bool ready = false;
   bool failed = false;
   cudaStream_t s1 = nullptr, s2 = nullptr;
-  cudaEvent_t ev[1 + 2 * kMaxSlices] = {};
+  cudaEvent_t ev[3 + 2 * kMaxSlices] = {};  // fork, per-slice joins, cache step
 };
 DevStreams g_streams[kMaxDevs];
 
@@ -352,15 +356,59 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
 }
 
 // finalize + (optional) draw of one slice on stream s
+// The cache step of an SSD round: (clear,) insert the forks of all B rows.
+cudaError_t cache_forks(const VerifyCall& c, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (c.cache_clear) {
+    const size_t kb = sizeof(unsigned long long) * c.cache->capacity;
+    e = cudaMemsetAsync(c.cache->keys, 0xff, kb, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c.cache->winner, 0, kb, s);
+  }
+  if (e != cudaSuccess) return e;
+  InsertArgs a;
+  memset(&a, 0, sizeof a);
+  a.fork_tok = c.fork_tok; a.P = c.k + 1; a.f = c.f; a.payload = c.payload;
+  a.n = c.B * (c.k + 1) * c.f;
+  return cache_insert(*c.cache, a, s);
+}
+
+cudaError_t cache_lookup_outcome(const VerifyCall& c, cudaStream_t s) {
+  LookupArgs a;
+  memset(&a, 0, sizeof a);
+  a.accept_len = c.accept_len; a.out_tok = c.out_tok; a.k = c.k; a.n = c.B;
+  a.hit = c.hit; a.tok_out = c.tok_out;
+  ProfScope ps("cache_lookup", s);
+  return launch_cache_lookup(*c.cache, a, s);
+}
+
+// finalize + (optional) draw of one slice on stream s.  With a cache step
+// and a side stream, the last slice's forks go into the cache on the side
+// stream while the draw runs (side waits on the finalize, s on the insert
+// before the lookup).
 cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool vec,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool last = true, cudaStream_t side = nullptr,
+                         cudaEvent_t ev_fin = nullptr, cudaEvent_t ev_ins = nullptr) {
   cudaError_t e;
   {
     ProfScope ps("finalize", s);
     e = launch_finalize(q.fp, s);
   }
-  if (e != cudaSuccess || !c.u_smp) return e;
-  return run_residual(q.rp, Bs, q.fp.dtype, vec, s);
+  if (e != cudaSuccess) return e;
+  const bool cache = c.cache && last;
+  const bool overlap = cache && side && ev_fin && ev_ins;
+  if (overlap) {
+    e = cudaEventRecord(ev_fin, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ev_fin, 0);
+    if (e == cudaSuccess) e = cache_forks(c, side);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_ins, side);
+    if (e != cudaSuccess) return e;
+  }
+  if (c.u_smp) e = run_residual(q.rp, Bs, q.fp.dtype, vec, s);
+  if (e != cudaSuccess || !cache) return e;
+  if (overlap) e = cudaStreamWaitEvent(s, ev_ins, 0);
+  else e = cache_forks(c, s);
+  if (e == cudaSuccess) e = cache_lookup_outcome(c, s);
+  return e;
 }
 
 // Schedule: for B >= 32 the batch is cut into S slices.  The target-row and
@@ -399,7 +447,9 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[1 + 2 * i], 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[2 + 2 * i], 0);
     pass.end();
-    if (e == cudaSuccess) e = enqueue_tail(c, q, b1 - b0, vec, c.stream);
+    if (e == cudaSuccess)
+      e = enqueue_tail(c, q, b1 - b0, vec, c.stream, i == S - 1, ds->s2, ds->ev[1 + 2 * kMaxSlices],
+                       ds->ev[2 + 2 * kMaxSlices]);
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
@@ -637,6 +687,30 @@ ssd_status ssd_verify_fork_fanout(const void* Z, int64_t z_bstride, const void* 
   c.u_smp = u_smp; c.out_tok = out_tok;
   c.f = F; c.mask = mask; c.M = M; c.fork_tok = fork_tok; c.fork_logit = fork_logit;
   c.fanout = fanout;
+  c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
+  return run_verify(c, true);
+}
+
+ssd_status ssd_verify_fork_cache(const void* Z, int64_t z_bstride, const void* D,
+                                 int64_t d_bstride, ssd_dtype dtype, int B, int k, int V,
+                                 const int32_t* x, const float* T, const float* u_acc,
+                                 int32_t* accept_len, float* p_at_x, float* q_at_x,
+                                 const float* u_smp, int32_t* out_tok, int f, const int32_t* mask,
+                                 int M, int32_t* fork_tok, float* fork_logit,
+                                 ssd_spec_cache* cache, int clear, const int32_t* payload,
+                                 int32_t* hit, int32_t* tok_out, void* ws, size_t ws_bytes,
+                                 ssd_stream_t stream) {
+  if (!cache || !payload || !hit || !tok_out || !out_tok) return SSD_ERR_INVALID_ARG;
+  if (k + 1 > 256 || static_cast<int64_t>(B) * (k + 1) * f > 0x7fffffff) return SSD_ERR_INVALID_ARG;
+  VerifyCall c;
+  memset(&c, 0, sizeof c);
+  c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
+  c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
+  c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
+  c.u_smp = u_smp; c.out_tok = out_tok;
+  c.f = f; c.mask = mask; c.M = M; c.fork_tok = fork_tok; c.fork_logit = fork_logit;
+  c.cache = &cache->view; c.cache_clear = clear != 0; c.payload = payload;
+  c.hit = hit; c.tok_out = tok_out;
   c.ws = ws; c.ws_bytes = ws_bytes; c.stream = S(stream);
   return run_verify(c, true);
 }

@@ -259,6 +259,35 @@ def test_spec_cache_ssd_workload(gpu_lib):
     assert int(got["hit"].sum()) == 0
 
 
+@pytest.mark.parametrize("name,over", [("ssd_fork", {}), ("mixed512", {"B": 64}),
+                                       ("qwen_b64", {})])
+def test_fused_round_step_equals_separate_calls(gpu_lib, name, over):
+    """ssd_verify_fork_cache (the forks inserted on a side stream while the
+    draw runs, for B >= 32) gives what the separate calls give."""
+    w = W.workload(name, **over)
+    inp = W.make_inputs(w, device=DEV, seed=W.default_seed(name) + 55)
+    depth = 5
+    n = w.B * (w.k + 1) * w.f
+    cap = 1 << max(6, (2 * n - 1).bit_length())
+    pay = torch.arange(n * depth, dtype=torch.int32, device=DEV).reshape(n, depth)
+    c1, c2 = gpu_lib.SpecCache(cap, depth), gpu_lib.SpecCache(cap, depth)
+    for rep in range(2):  # the second round also checks the clear
+        fused = gpu_lib.ssd_verify_fork_cache(inp["Z"], inp["D"], inp["x"], inp["T"], inp["u_acc"],
+                                              inp["u_smp"], w.f, inp["mask"], c1, pay + rep)
+        sep = run_verify(gpu_lib, inp, fork_f=w.f)
+        c2.clear()
+        c2.insert_forks(sep["fork_tok"], pay + rep)
+        look = c2.lookup_outcome(sep["accept_len"], sep["out_tok"])
+        torch.cuda.synchronize()
+        for key in ("accept_len", "out_tok", "p_at_x", "q_at_x", "fork_tok", "fork_logit"):
+            assert torch.equal(fused[key], sep[key]), key
+        assert torch.equal(fused["hit"], look["hit"])
+        assert torch.equal(fused["tok_out"], look["tok_out"])
+    assert c1.error() == 0
+    c1.close()
+    c2.close()
+
+
 def test_spec_cache_duplicates_and_overflow(gpu_lib):
     cache = gpu_lib.SpecCache(8, 2)
     b = torch.tensor([0, 0, 0, 1], dtype=torch.int32, device=DEV)
