@@ -320,25 +320,42 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
     __syncthreads();
     return chi - 1;
   }
-  if (tid == pick) {
-    // walk the thread's range with the same double-float accumulation
-    const long long base = incl - own;
-    float ah = 0.f, al = 0.f;
-    int last_pos = -1;
-    for (int i = lo; i < hi; ++i) {
-      float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
-      float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
-      float wh, wl;
-      weight<Q>(z, d, cx, tab, wh, wl);
-      if (wh > 0.f) last_pos = i;
-      df_acc(ah, al, wh, wl);
-      if (base + df_to_fix(ah, al, scale) > target) {
-        tok = i;
-        break;
+  // warp 0 walks the picked thread's range: per-element weights in fixed
+  // point, an int64 scan over the lanes, the first element whose cumulative
+  // mass passes the target (per-element rounding moves the cumulative by at
+  // most a few units of 2^-60 against the thread's own total)
+  __shared__ long long s_base;
+  if (tid == pick) s_base = incl - own;
+  __syncthreads();
+  if (tid < 32) {
+    const int plo = min(chi, clo + pick * E), phi = min(chi, plo + E);
+    const long long base = s_base;
+    long long carry = 0;
+    int last_pos = -1, found = -1;
+    for (int off = plo; off < phi && found < 0; off += 32) {
+      const int i = off + tid;
+      long long wf = 0;
+      if (i < phi) {
+        const float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
+        const float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
+        float wh, wl;
+        weight<Q>(z, d, cx, tab, wh, wl);
+        wf = df_to_fix(wh, wl, scale);
       }
+      long long c = wf;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(kFull, c, o);
+        if (tid >= o) c += y;
+      }
+      const unsigned over = __ballot_sync(kFull, i < phi && base + carry + c > target);
+      const unsigned posm = __ballot_sync(kFull, i < phi && wf > 0);
+      if (posm) last_pos = off + 31 - __clz(posm);
+      if (over) found = off + __ffs(over) - 1;
+      carry += __shfl_sync(kFull, c, 31);
     }
-    if (tok < 0) tok = last_pos >= 0 ? last_pos : hi - 1;  // rounding guard
-    *s_pick = -1 - tok;
+    if (tid == 0) tok = found >= 0 ? found : (last_pos >= 0 ? last_pos : phi - 1);  // rounding guard
+    if (tid == 0) *s_pick = -1 - tok;
   }
   __syncthreads();
   return -1 - *s_pick;
