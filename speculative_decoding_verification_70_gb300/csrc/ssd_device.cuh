@@ -125,15 +125,14 @@ __device__ __forceinline__ void arg_df(float z, float m, float c_hi, float c_lo,
   xl = __fmaf_rn(dl, c_hi, xl);
 }
 
-// 2^(xh + xl) for xh <= 0 as a float pair (hi, lo), relative error ~1e-9.
-// Method: J = round(64 xh) (one add of 1.5 * 2^23 gives both the rounded
-// float and the integer), x = J/64 + g with |g| <= 1/128 (exact) plus xl;
-// 2^x = 2^(J >> 6) * 2^((J & 63)/64) * (1 + P(g)) with the table 2^(j/64)
-// held as float pairs and P the degree-4 Taylor polynomial of 2^g - 1
-// (truncation < 4e-14).  Results below 2^-125 (relative to the row maximum
-// 1) return 0.  `tab` is a shared-memory copy of kExp2Tab.  The pair is
-// not normalised: hi is the scaled table value alone and lo carries the
-// polynomial part (up to 0.55% of hi), so callers use hi + lo, never hi alone.
+// 2^(xh + xl) for xh <= 0 as a normalised float pair (hi, lo: |lo| <= half
+// an ulp of hi), relative error ~1e-9.  Method: J = round(64 xh) (one add
+// of 1.5 * 2^23 gives both the rounded float and the integer), x = J/64 + g
+// with |g| <= 1/128 (exact) plus xl; 2^x = 2^(J >> 6) * 2^((J & 63)/64) *
+// (1 + P(g)) with the table 2^(j/64) held as float pairs and P the degree-3
+// Taylor polynomial of 2^g - 1 (truncation < 4e-11, below the float
+// rounding of P).  Results below 2^-125 (relative to the row maximum 1)
+// return 0.  `tab` is a shared-memory copy of kExp2Tab.
 __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, float& hi,
                                         float& lo) {
   if (!(xh > -125.0f)) {
@@ -147,16 +146,18 @@ __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, f
   const int J = __float_as_int(tj) - 0x4B400000;
   float g = __fmaf_rn(Jf, -0.015625f, xh);     // exact, |g| <= 1/128
   g = __fadd_rn(g, xl);
-  float P = __fmaf_rn(g, SSD_EXP2_C4, SSD_EXP2_C3);
-  P = __fmaf_rn(g, P, SSD_EXP2_C2);
+  float P = __fmaf_rn(g, SSD_EXP2_C3, SSD_EXP2_C2);
   P = __fmaf_rn(g, P, SSD_LN2_LO);
   P = __fmul_rn(g, P);
   P = __fmaf_rn(g, SSD_LN2_HI, P);             // 2^g - 1
   const float2 t = tab[J & 63];
   const float l = __fmaf_rn(t.x, P, __fmaf_rn(t.y, P, t.y));
   const float scale = __int_as_float(((J >> 6) + 127) << 23);  // J >> 6 in [-126, 0]
-  hi = __fmul_rn(t.x, scale);
-  lo = __fmul_rn(l, scale);
+  // renormalise (|l| < 0.6% of t.x: Fast2Sum is exact)
+  const float s = __fadd_rn(t.x, l);
+  const float e = __fsub_rn(l, __fsub_rn(s, t.x));
+  hi = __fmul_rn(s, scale);
+  lo = __fmul_rn(e, scale);
 }
 
 // Copy the exp2 table to shared memory (call before the first exp2_df; a
@@ -182,6 +183,16 @@ __device__ __forceinline__ void df_sub(float ah, float al, float bh, float bl, f
   e = __fadd_rn(e, __fsub_rn(al, bl));
   sh = __fadd_rn(s, e);
   sl = __fsub_rn(e, __fsub_rn(sh, s));
+}
+
+// Compensated sum of non-negative values: acc += vh with the exact error
+// of that add (Fast2Sum after ordering the two) and vl added to comp; the
+// pair (acc, comp) carries the sum to O(n u^2).  vh, vl: a normalised pair.
+__device__ __forceinline__ void comp_acc(float& acc, float& comp, float vh, float vl) {
+  const float big = fmaxf(acc, vh), small = fminf(acc, vh);
+  const float t = __fadd_rn(big, small);
+  comp = __fadd_rn(comp, __fadd_rn(__fadd_rn(__fsub_rn(big, t), small), vl));
+  acc = t;
 }
 
 // acc += v (double-float, renormalised)

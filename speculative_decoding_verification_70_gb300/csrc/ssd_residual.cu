@@ -9,8 +9,9 @@
 // The draw decides an integer from sums over ~10^5 tiny weights, so fp32
 // would move CDF boundaries across the dense tail of the distribution and
 // change ~1e-3 of the draws.  Here every weight is evaluated in double-float
-// (exp2_df, ~1e-9 relative), each thread sums a contiguous index range in
-// double-float, and everything above a thread is exact 64-bit fixed point,
+// (exp2_df, ~1e-9 relative), each thread sums a contiguous index range with
+// compensation (error O(n u^2)), and everything above a thread is exact
+// 64-bit fixed point,
 // so every level of the three-level select (chunk, thread, element) sees the
 // same totals.
 //
@@ -172,22 +173,20 @@ __device__ __forceinline__ void pass_element(float z, float d, int idx, bool res
   float xh, xl, a_h, a_l;
   arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
   exp2_df(xh, xl, tab, a_h, a_l);
-  df_acc(sah, sal, a_h, a_l);
+  comp_acc(sah, sal, a_h, a_l);
   if (!resid) return;
   float b_h, b_l;
   arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
   exp2_df(xh, xl, tab, b_h, b_l);
-  df_acc(sbh, sbl, b_h, b_l);
-  // exp2_df's pair is not normalised (lo holds up to 0.55% of hi), so the
-  // split compares the rounded sums, good to ~1e-7 against the 1e-3 margin
-  const float a1 = __fadd_rn(a_h, a_l);
-  const float rb = cx.rho * __fadd_rn(b_h, b_l);
-  const float diff = a1 - rb;
-  const float lim = kSignMargin * fmaxf(a1, rb);
+  comp_acc(sbh, sbl, b_h, b_l);
+  // the pairs are normalised: hi alone is good to 2^-24 against the margin
+  const float rb = cx.rho * b_h;
+  const float diff = a_h - rb;
+  const float lim = kSignMargin * fmaxf(a_h, rb);
   if (diff > lim) {
-    df_acc(ah, al, a_h, a_l);
-    df_acc(bh, bl, b_h, b_l);
-  } else if (diff >= -lim && (a1 > 0.f || rb > 0.f)) {
+    comp_acc(ah, al, a_h, a_l);
+    comp_acc(bh, bl, b_h, b_l);
+  } else if (diff >= -lim && (a_h > 0.f || rb > 0.f)) {
     const int q = atomicAdd(amb_cnt, 1);
     if (q < amb_cap) amb_idx[q] = idx;
   }
