@@ -44,9 +44,12 @@ struct RowStat {
 enum ResidualMode : int { kModeNone = 0, kModeResidual = 1, kModeTarget = 2 };
 
 struct BState {
-  int n;      // accepted prefix length (or sentinel)
-  int mode;   // ResidualMode
-  int pad0, pad1;
+  int n;        // accepted prefix length (or sentinel)
+  int mode;     // ResidualMode
+  float c_hi;   // log2(e) / T as a float pair (0 for greedy rows)
+  float c_lo;
+  float rho;    // S_z / S_d of rows n from the streaming statistics (residual mode)
+  int pad0, pad1, pad2;
 };
 
 struct Chunking {

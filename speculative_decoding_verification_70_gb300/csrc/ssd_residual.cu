@@ -134,16 +134,12 @@ __device__ __forceinline__ bool load_ctx(const ResidualParams& p, int b, BState&
   if (bs.mode == kModeNone) return false;
   if (threadIdx.x == 0) {
     RowCtx c;
-    const RowStat rz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n];
-    c.mz = rz.m;
-    c.md = 0.f;
-    c.rho = 1.f;
-    if (bs.mode == kModeResidual) {
-      const RowStat rd = p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n];
-      c.md = rd.m;
-      c.rho = static_cast<float>(rz.S / rd.S);
-    }
-    temp_coeff(p.T[b], c.c_hi, c.c_lo);
+    c.mz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n].m;
+    c.md = (bs.mode == kModeResidual) ? p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m
+                                      : 0.f;
+    c.rho = bs.rho;  // from the streaming statistics, set with the draw state
+    c.c_hi = bs.c_hi;
+    c.c_lo = bs.c_lo;
     c.iz_hi = c.iz_lo = c.id_hi = c.id_lo = 0.f;
     if (with_inverses) norm_inverses(p, b, c);
     *s_cx = c;
@@ -397,7 +393,8 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     c.mz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n].m;
     c.md = resid_row ? p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m : 0.f;
     c.rho = 1.f;
-    temp_coeff(p.T[b], c.c_hi, c.c_lo);
+    c.c_hi = bs.c_hi;
+    c.c_lo = bs.c_lo;
     const double Sz = static_cast<double>(sz) * kInvFixMass;
     const double Sd = static_cast<double>(sd) * kInvFixMass;
     split_double(1.0 / Sz, c.iz_hi, c.iz_lo);
@@ -482,7 +479,15 @@ __global__ void residual_prep_kernel(PrepParams p) {
   bs.n = n;
   bs.mode = (n < 0 || n > p.k || greedy || isnan(T)) ? kModeNone
                                                        : (n < p.k ? kModeResidual : kModeTarget);
-  bs.pad0 = bs.pad1 = 0;
+  bs.c_hi = bs.c_lo = 0.f;
+  bs.rho = 1.f;
+  if (bs.mode != kModeNone) {
+    temp_coeff(T, bs.c_hi, bs.c_lo);
+    if (bs.mode == kModeResidual)
+      bs.rho = static_cast<float>(p.rowstat[static_cast<int64_t>(b) * p.R + n].S /
+                                  p.rowstat[static_cast<int64_t>(b) * p.R + p.k + 1 + n].S);
+  }
+  bs.pad0 = bs.pad1 = bs.pad2 = 0;
   p.bstate[b] = bs;
   p.amb_cnt[b] = 0;
   int32_t* o = p.out_tok + static_cast<int64_t>(b) * (p.k + 1);

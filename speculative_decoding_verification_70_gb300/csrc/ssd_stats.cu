@@ -648,9 +648,11 @@ __global__ void __launch_bounds__(kThreads) draft_finalize_kernel(DraftParams p)
 // ---------------------------------------------------------------------------
 
 // Merge the C partial records of one row (one warp).  S is accumulated in
-// double with extended-precision rescaling factors.
+// double-float (products s * 2^((m_c - m) c) with extended-precision
+// rescaling factors) and returned as the pair (sh, sl) and, in rs.S, as a
+// double (one conversion per row: the FP64 pipe is narrow).
 __device__ void merge_row(const PartStat* parts, int C, float c_hi, float c_lo, bool do_exp,
-                          const float2* tab, RowStat& rs) {
+                          const float2* tab, RowStat& rs, float& sh, float& sl) {
   const int lane = threadIdx.x & 31;
   float m = -INFINITY;
   int idx = kIdxNone, nan = 0;
@@ -672,29 +674,35 @@ __device__ void merge_row(const PartStat* parts, int C, float c_hi, float c_lo, 
       idx = i2;
     }
   }
-  double S = 0.0;
+  sh = 0.f;
+  sl = 0.f;
   if (do_exp) {
     for (int q = lane; q < C; q += 32) {
       PartStat ps = parts[q];
-      double fct;
-      if (ps.m == m) {
-        fct = 1.0;
-      } else {
-        float xh, xl, eh, el;
+      float fh = 1.f, fl = 0.f;
+      if (ps.m != m) {
+        float xh, xl;
         arg_df(ps.m, m, c_hi, c_lo, xh, xl);
-        exp2_df(xh, xl, tab, eh, el);
-        fct = static_cast<double>(eh) + static_cast<double>(el);
+        exp2_df(xh, xl, tab, fh, fl);
       }
-      S += static_cast<double>(ps.s) * fct;
+      float ph, pl;
+      df_mul(ps.s, 0.f, fh, fl, ph, pl);
+      df_acc(sh, sl, ph, pl);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(kFull, sh, o);
+      const float ol = __shfl_xor_sync(kFull, sl, o);
+      df_acc(sh, sl, oh, ol);
+    }
+  } else {
+    sh = 1.f;
   }
   rs.m = m;
   rs.argmax = idx;
-  rs.S = do_exp ? S : 1.0;
+  rs.S = static_cast<double>(sh) + static_cast<double>(sl);
   int bad = nan;
-  if (do_exp && !(S > 0.0 && S < INFINITY)) bad = 1;  // +inf, NaN or all -inf at T > 0
+  if (do_exp && !(sh > 0.f && sh < INFINITY)) bad = 1;  // +inf, NaN or all -inf at T > 0
   rs.flags = (nan ? 1 : 0) | (bad ? 2 : 0);
 }
 
@@ -758,6 +766,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float2 tab[64];
   __shared__ RowStat rs[2 * (32 + 1)];
+  __shared__ float2 rsum[2 * (32 + 1)];  // each row's S as a float pair
   __shared__ int heads[kWarps][256];
   load_exp2_table(tab);
   __syncthreads();
@@ -781,9 +790,12 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
     bool need_stats = is_target || j < p.Pds;
     bool do_exp = need_stats && !greedy && !t_bad;
     RowStat st;
-    merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c_hi, c_lo, do_exp, tab, st);
+    float sh, sl;
+    merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c_hi, c_lo, do_exp, tab, st,
+              sh, sl);
     if (lane == 0) {
       rs[r] = st;
+      rsum[r] = make_float2(sh, sl);
       p.rowstat[static_cast<int64_t>(b) * p.Rp + r] = st;
     }
     // forked top-f of draft row j
@@ -830,17 +842,21 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
     } else {
       float zx = logit_at(p.Z, p.dtype, static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(lane) * p.V + xi);
       float dx = logit_at(p.D, p.dtype, static_cast<int64_t>(b) * p.db + static_cast<int64_t>(lane) * p.V + xi);
-      float xh, xl, eh, el;
+      float xh, xl, ezh, ezl, edh, edl;
       arg_df(zx, tz.m, c_hi, c_lo, xh, xl);
-      exp2_df(xh, xl, tab, eh, el);
-      double pd = (static_cast<double>(eh) + static_cast<double>(el)) / tz.S;
+      exp2_df(xh, xl, tab, ezh, ezl);
       arg_df(dx, td.m, c_hi, c_lo, xh, xl);
-      exp2_df(xh, xl, tab, eh, el);
-      double qd = (static_cast<double>(eh) + static_cast<double>(el)) / td.S;
-      float u = p.u_acc[static_cast<int64_t>(b) * k + lane];
-      acc = (qd == 0.0) ? (pd > 0.0) : (static_cast<double>(u) < pd / qd);
-      pv = static_cast<float>(pd);
-      qv = static_cast<float>(qd);
+      exp2_df(xh, xl, tab, edh, edl);
+      const float2 Sz = rsum[lane], Sd = rsum[p.Pz + lane];
+      const float u = p.u_acc[static_cast<int64_t>(b) * k + lane];
+      // u < p/q  <=>  u e_d S_z < e_z S_d  (p = e_z / S_z, q = e_d / S_d)
+      float lh, ll, rh, rl;
+      df_mul(edh, edl, Sz.x, Sz.y, lh, ll);
+      df_mul(lh, ll, u, 0.f, lh, ll);
+      df_mul(ezh, ezl, Sd.x, Sd.y, rh, rl);
+      acc = (edh == 0.f) ? (ezh > 0.f) : (lh < rh || (lh == rh && ll < rl));
+      pv = __fdiv_rn(__fadd_rn(ezh, ezl), __fadd_rn(Sz.x, Sz.y));
+      qv = __fdiv_rn(__fadd_rn(edh, edl), __fadd_rn(Sd.x, Sd.y));
     }
   }
   unsigned ball = __ballot_sync(kFull, acc);
@@ -865,7 +881,10 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
     BState bs;
     bs.n = n;
     bs.mode = (n < 0 || greedy) ? kModeNone : (n < k ? kModeResidual : kModeTarget);
-    bs.pad0 = bs.pad1 = 0;
+    bs.c_hi = c_hi;
+    bs.c_lo = c_lo;
+    bs.rho = (bs.mode == kModeResidual) ? __fdiv_rn(rsum[n].x, rsum[p.Pz + n].x) : 1.f;
+    bs.pad0 = bs.pad1 = bs.pad2 = 0;
     p.bstate[b] = bs;
     if (p.amb_cnt) p.amb_cnt[b] = 0;
     int e = 0;
@@ -898,7 +917,9 @@ __global__ void __launch_bounds__(kThreads) softmax_finalize_kernel(SoftmaxParam
     c_lo = __shfl_sync(kFull, c_lo, 0);
   }
   RowStat st;
-  merge_row(p.part + static_cast<int64_t>(r) * p.C, p.C, c_hi, c_lo, !greedy && !t_bad, tab, st);
+  float sh, sl;
+  merge_row(p.part + static_cast<int64_t>(r) * p.C, p.C, c_hi, c_lo, !greedy && !t_bad, tab, st,
+            sh, sl);
   bool bad = t_bad || (st.flags & 2) || (st.flags & 1);
   if (lane == 0) {
     if (bad) {
