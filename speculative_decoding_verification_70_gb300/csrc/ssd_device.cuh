@@ -209,6 +209,21 @@ __device__ __forceinline__ long long df_to_fix(float h, float l, float scale) {
   return __float2ll_rn(__fmul_rn(h, scale)) + __float2ll_rn(__fmul_rn(l, scale));
 }
 
+// An int64 as a float pair (48 significant bits: relative error <= 2^-48).
+__device__ __forceinline__ void i64_to_df(long long v, float& h, float& l) {
+  h = __ll2float_rn(v);
+  l = __ll2float_rn(v - __float2ll_rn(h));
+}
+
+// 1 / (h + l) as a normalised float pair: the correctly rounded reciprocal
+// of h and one correction from the exact residual 1 - (h + l) r (FMA).
+__device__ __forceinline__ void df_recip(float h, float l, float& rh, float& rl) {
+  const float r = __frcp_rn(h);
+  float e = __fmaf_rn(-h, r, 1.0f);
+  e = __fmaf_rn(-l, r, e);
+  two_sum(r, __fmul_rn(r, e), rh, rl);
+}
+
 // Split a positive double into a float pair.
 __device__ __forceinline__ void split_double(double v, float& h, float& l) {
   h = __double2float_rn(v);

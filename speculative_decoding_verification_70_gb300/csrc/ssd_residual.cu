@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
   __shared__ int s_chunk;
   __shared__ long long s_target;
   __shared__ RowCtx s_cx;
-  __shared__ double s_acc[2];            // rho = S_z / S_d and 2^12 / S_z
+  __shared__ float2 s_acc[2];            // rho = S_z / S_d and 2^12 / S_z, float pairs
   const int b = blockIdx.x, tid = threadIdx.x;
   const BState bs = p.bstate[b];
   if (bs.mode == kModeNone) return;
@@ -395,13 +395,21 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     c.rho = 1.f;
     c.c_hi = bs.c_hi;
     c.c_lo = bs.c_lo;
-    const double Sz = static_cast<double>(sz) * kInvFixMass;
-    const double Sd = static_cast<double>(sd) * kInvFixMass;
-    split_double(1.0 / Sz, c.iz_hi, c.iz_lo);
-    split_double(1.0 / Sd, c.id_hi, c.id_lo);
+    // normalisers and their inverses in double-float (no FP64 on this
+    // thread's chain); the 2^-42 unit scaling is exact
+    constexpr float kMass = 2.2737367544323206e-13f;  // 2^-42
+    float szh, szl, sdh, sdl;
+    i64_to_df(sz, szh, szl);
+    i64_to_df(sd, sdh, sdl);
+    szh *= kMass; szl *= kMass;
+    sdh *= kMass; sdl *= kMass;
+    df_recip(szh, szl, c.iz_hi, c.iz_lo);
+    df_recip(sdh, sdl, c.id_hi, c.id_lo);
     s_cx = c;
-    s_acc[0] = static_cast<double>(sz) / static_cast<double>(sd);
-    s_acc[1] = 4096.0 / Sz;
+    float rh, rl;
+    df_mul(szh, szl, c.id_hi, c.id_lo, rh, rl);
+    s_acc[0] = make_float2(rh, rl);
+    s_acc[1] = make_float2(c.iz_hi * 4096.f, c.iz_lo * 4096.f);
   }
   __syncthreads();
   const RowCtx cx = s_cx;
@@ -426,9 +434,16 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
   long long wq = 0;
   if (tid < p.C) {
     if (split) {
-      const double v = (static_cast<double>(ca) - s_acc[0] * static_cast<double>(cb)) * s_acc[1] +
-                       static_cast<double>(s_amb[tid]);
-      wq = v > 0.0 ? static_cast<long long>(v) : 0;
+      float ah, al, bh, bl, th, tl, vh, vl, mh, ml;
+      i64_to_df(ca, ah, al);
+      i64_to_df(cb, bh, bl);
+      df_mul(s_acc[0].x, s_acc[0].y, bh, bl, th, tl);       // rho B_c
+      df_sub(ah, al, th, tl, vh, vl);                       // A_c - rho B_c
+      df_mul(vh, vl, s_acc[1].x, s_acc[1].y, vh, vl);       // / S_z, in 2^60 units
+      i64_to_df(s_amb[tid], mh, ml);
+      df_acc(vh, vl, mh, ml);
+      wq = vh > 0.f ? __float2ll_rn(vh) + __float2ll_rn(vl) : 0;
+      if (wq < 0) wq = 0;
     } else if (resid_row) {
       wq = p.rmass[rb + tid];
     } else {
