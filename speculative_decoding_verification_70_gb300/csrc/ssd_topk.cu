@@ -35,6 +35,8 @@ constexpr int kPer = 4;  // candidates kept by each thread
 constexpr int kSecond = 256;  // entries of the second-chance buffer
 
 struct PassSmem {
+  float sv[kWarps][kThreads / kWarps * 4];  // each warp's 128 candidates (bitonic path)
+  int si[kWarps][kThreads / kWarps * 4];
   float lv[kMaxTopK];          // the candidates' top K (sorted)
   int li[kMaxTopK];
   float xv[kSecond];           // second chance: elements of overflowing threads
@@ -89,6 +91,56 @@ __device__ __forceinline__ void top4_push(Top4& s, float z, int idx) {
     s.t[3] = z;
     s.i[3] = idx;
   }
+}
+
+// One compare-exchange of a descending bitonic network on (value, index)
+// pairs in shared memory: after it, position i holds the pair that ranks
+// first when `desc`, else the one that ranks second.
+__device__ __forceinline__ void bitonic_cx(float* v, int* ix, int i, int l, bool desc) {
+  const float a = v[i], b = v[l];
+  const int ai = ix[i], bi = ix[l];
+  const bool swap = desc ? ranks_before(b, bi, a, ai) : ranks_before(a, ai, b, bi);
+  if (swap) {
+    v[i] = b;
+    ix[i] = bi;
+    v[l] = a;
+    ix[l] = ai;
+  }
+}
+
+// Warp-synchronous descending bitonic sort of n (a power of two, n / 2 a
+// multiple of 32) pairs in shared memory.
+__device__ __forceinline__ void warp_bitonic_sort(float* v, int* ix, int n) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 2; k <= n; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int pr = lane; pr < n / 2; pr += 32) {
+        const int i = (pr / j) * 2 * j + (pr % j);
+        bitonic_cx(v, ix, i, i + j, (i & k) == 0);
+      }
+      __syncwarp();
+    }
+}
+
+// Warp-synchronous: a[0..32) and b[0..32), each sorted descending, become
+// their top 32 (descending) in a: a ++ reverse(b) is bitonic, one merge
+// sorts it.
+__device__ __forceinline__ void warp_merge_top32(float* av, int* ai, const float* bv,
+                                                 const int* bi, float* tv, int* ti) {
+  const int lane = threadIdx.x & 31;
+  tv[lane] = av[lane];
+  ti[lane] = ai[lane];
+  tv[32 + lane] = bv[31 - lane];
+  ti[32 + lane] = bi[31 - lane];
+  __syncwarp();
+  for (int j = 32; j > 0; j >>= 1) {
+    const int i = (lane / j) * 2 * j + (lane % j);
+    bitonic_cx(tv, ti, i, i + j, true);
+    __syncwarp();
+  }
+  av[lane] = tv[lane];
+  ai[lane] = ti[lane];
+  __syncwarp();
 }
 
 // Best (value, index) of the elements of [lo, hi) (thread-strided vectors)
@@ -219,9 +271,35 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
   // certified: every element outside the candidates is <= M5, and at least K
   // candidates exceed it (or nothing finite lies outside the candidates)
   const bool certified = sm.cnt >= p.K || M5 == -INFINITY;
-  // the K best candidates: each warp ranks its 128 (four per lane, in
-  // registers), then warp 0 merges the eight sorted lists
-  {
+  // the K best candidates.  K <= 16: each warp ranks its 128 (four per
+  // lane, in registers) by K arg-max rounds and warp 0 merges the eight
+  // lists by K rounds.  K > 16: each warp bitonic-sorts its 128 in shared
+  // memory, then the eight sorted top-32 lists merge pairwise (three levels
+  // of bitonic merges); its cost does not grow with K and is below that of
+  // 2K rounds from K ~ 20 on (measured at V = 151936).
+  if (p.K > 16) {
+    float* v = sm.sv[warp];
+    int* ix = sm.si[warp];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      v[lane * kPer + q] = st.t[q];
+      ix[lane * kPer + q] = st.i[q];
+    }
+    __syncwarp();
+    warp_bitonic_sort(v, ix, 32 * kPer);
+    if (tid == 0) sm.nx = 0;
+    __syncthreads();
+    for (int step = 1; step < kWarps; step <<= 1) {  // lists in sv[w][0..32)
+      if ((warp & (2 * step - 1)) == 0)
+        warp_merge_top32(sm.sv[warp], sm.si[warp], sm.sv[warp + step], sm.si[warp + step],
+                         sm.sv[warp] + 32, sm.si[warp] + 32);
+      __syncthreads();
+    }
+    if (tid < p.K) {
+      sm.lv[tid] = sm.si[0][tid] == kIdxNone ? -INFINITY : sm.sv[0][tid];
+      sm.li[tid] = sm.si[0][tid];
+    }
+  } else {
     float t[kPer];
     int ix[kPer];
 #pragma unroll
@@ -255,25 +333,25 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
           }
       }
     }
-  }
-  if (tid == 0) sm.nx = 0;
-  __syncthreads();
-  if (warp == 0) {
-    int head = 0;
-    for (int rr = 0; rr < p.K; ++rr) {
-      float hv = -INFINITY;
-      int hi2 = kIdxNone;
-      if (lane < kWarps && head < p.K) {
-        hv = sm.wl[lane][head];
-        hi2 = sm.wi[lane][head];
-      }
-      float wv = hv;
-      int wi = hi2;
-      warp_argmax(wv, wi);
-      if (wi != kIdxNone && wi == hi2) ++head;
-      if (lane == 0) {
-        sm.lv[rr] = wv;
-        sm.li[rr] = wi;
+    if (tid == 0) sm.nx = 0;
+    __syncthreads();
+    if (warp == 0) {
+      int head = 0;
+      for (int rr = 0; rr < p.K; ++rr) {
+        float hv = -INFINITY;
+        int hi2 = kIdxNone;
+        if (lane < kWarps && head < p.K) {
+          hv = sm.wl[lane][head];
+          hi2 = sm.wi[lane][head];
+        }
+        float wv = hv;
+        int wi = hi2;
+        warp_argmax(wv, wi);
+        if (wi != kIdxNone && wi == hi2) ++head;
+        if (lane == 0) {
+          sm.lv[rr] = wv;
+          sm.li[rr] = wi;
+        }
       }
     }
   }

@@ -66,7 +66,8 @@ def test_verify_topk_matches_oracle(gpu_lib, name, over, temp, K, tp):
 
 def test_verify_topk_edges(gpu_lib):
     """Sentinels, rows with fewer than K finite logits, ties, an unaligned
-    row length (scalar path) and K = V."""
+    row length (scalar path) and K = V; K up to 16 and K above 16 take the
+    two candidate-selection paths of the pass kernel."""
     B, k, V = 8, 3, 37
     g = torch.Generator().manual_seed(11)
     Z = torch.randint(-3, 4, (B, k + 1, V), generator=g).float()    # many ties
@@ -80,7 +81,7 @@ def test_verify_topk_edges(gpu_lib):
     ua = torch.rand((B, k), generator=g)
     us = torch.rand(B, generator=g)
     inp = {"Z": Z, "D": D, "T": T, "u_acc": ua, "u_smp": us}
-    for K, tp in ((6, None), (V, None), (3, 0.6)):
+    for K, tp in ((6, None), (V, None), (3, 0.6), (32, None), (20, 0.6), (17, None)):
         if K > 32:
             continue
         top_p = None if tp is None else torch.full((B,), tp)
