@@ -20,6 +20,9 @@ Sources followed (cited by page title and section):
     Works": accept, then regenerate from the point of divergence.
   * Leviathan et al. 2023 / Chen et al. 2023: the min(1, p/q) acceptance,
     the norm(max(0, p - q)) residual and the bonus draw from p.
+  * "tanishqkumar/ssd" summary page, module notes on tree decoding, with
+    SpecInfer's multi-step speculative sampling (Miao et al. 2024) as the
+    rule for verifying a token tree.
 """
 from __future__ import annotations
 
@@ -75,6 +78,11 @@ def _load():
     lib.oracle_verify_recover_filtered.argtypes = [P, i64, P, i64, i32, i32, i32, i64, P, P,
                                                    i32, P, P, P, i32, P, P, P, P]
     lib.oracle_verify_recover_filtered.restype = i32
+    lib.oracle_verify_tree.argtypes = [P, i64, P, i64, i32, i32, i32, i64, P, P, P, P, P,
+                                       P, P, P]
+    lib.oracle_verify_tree.restype = i32
+    lib.oracle_verify_tree_f64.argtypes = lib.oracle_verify_tree.argtypes
+    lib.oracle_verify_tree_f64.restype = i32
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox4x32_10.restype = None
     u32 = ctypes.c_uint32
@@ -201,6 +209,42 @@ def verify_recover_filtered(Z, D, x, T, K: int, top_p, u_acc, u_smp,
         _ptr(u_acc), _ptr(u_smp), int(f64_uniforms), _ptr(acc), _ptr(pax), _ptr(qax),
         _ptr(out)), "verify_recover_filtered")
     return {"accept_len": acc, "p_at_x": pax, "q_at_x": qax, "out_tok": out}
+
+
+def verify_tree(Z, D, parent, tok, T, u_acc, u_smp, f64_uniforms: bool = False
+                ) -> Dict[str, np.ndarray]:
+    """Token-tree verification (multi-step speculative sampling over a tree
+    whose children at a node were drawn from the draft's q there).
+
+    Z, D: [B, N, V] target and draft logits at the N nodes.  parent, tok:
+    [B, N] int32 (parent[:, 0] == -1, parent[:, j] < j; tok[:, 0] unused).
+    T: [B].  u_acc: [B, N] (entry j tests node j), u_smp: [B]: binary32 as
+    the GPU library takes them, or double when f64_uniforms.
+
+    Returns accept_len [B], out_tok [B, N] (accepted tokens, the final
+    token, then -1) and out_node [B, N] (accepted node ids, then -1).
+    """
+    z, dt = _logits(Z)
+    d, dt2 = _logits(D)
+    if dt != dt2:
+        raise TypeError("Z and D must share a dtype")
+    B, N, V = z.shape
+    if d.shape != z.shape:
+        raise ValueError("D must be [B, N, V] like Z")
+    parent = np.ascontiguousarray(parent, dtype=np.int32).reshape(B, N)
+    tok = np.ascontiguousarray(tok, dtype=np.int32).reshape(B, N)
+    T = np.ascontiguousarray(T, dtype=np.float32).reshape(B)
+    udt = np.float64 if f64_uniforms else np.float32
+    u_acc = np.ascontiguousarray(u_acc, dtype=udt).reshape(B, N)
+    u_smp = np.ascontiguousarray(u_smp, dtype=udt).reshape(B)
+    acc = np.empty(B, dtype=np.int32)
+    out = np.empty((B, N), dtype=np.int32)
+    node = np.empty((B, N), dtype=np.int32)
+    fn = _load().oracle_verify_tree_f64 if f64_uniforms else _load().oracle_verify_tree
+    _check(fn(
+        _ptr(z), N * V, _ptr(d), N * V, dt, B, N, V, _ptr(parent), _ptr(tok), _ptr(T),
+        _ptr(u_acc), _ptr(u_smp), _ptr(acc), _ptr(out), _ptr(node)), "verify_tree")
+    return {"accept_len": acc, "out_tok": out, "out_node": node}
 
 
 def forked_topf(L, f: int, mask=None, fanout=None) -> Dict[str, np.ndarray]:

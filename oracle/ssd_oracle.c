@@ -48,6 +48,21 @@
  *      prefix of those whose probability mass is >= top_p times their mass;
  *      renormalise over what is kept.  Acceptance, the residual and the bonus
  *      draw then use the filtered p and q; greedy rows are unchanged.
+ *   R10 token-tree verification (the summary page's "tree decoding"; the
+ *      rule is the multi-step speculative sampling of SpecInfer, Miao et
+ *      al. 2024, for children drawn independently from the draft's q at
+ *      their parent): per batch row a tree of N nodes, node 0 the root,
+ *      parent[j] < j, children tried in increasing node index.  At the
+ *      current node with target law r (initially p of that node) each
+ *      child token x is accepted when u < r(x)/q(x) (R2 for q(x) == 0); an
+ *      accepted child becomes the current node (r = its p); a rejection
+ *      replaces r by norm(max(0, r - q)) (kept unchanged if that is all
+ *      zero, as R5).  When the children are exhausted the final token is
+ *      drawn from r by R4.  Greedy rows accept the first child whose token
+ *      is the argmax of the current node's target row and end with that
+ *      argmax.  All N target rows and all N draft rows are read (R7);
+ *      parent[0] != -1, parent[j] outside [0, j) or a token outside [0, V)
+ *      gives accept_len -2.
  *   R8 draft-side sampling: the drafter's token at T > 0 is the Gumbel-max
  *      draw argmax_v (z_v / T + G_v), G_v = -ln(-ln u_v), which is exactly a
  *      draw from softmax(z / T); u_v comes from the counter-based generator
@@ -542,6 +557,167 @@ int oracle_forked_topf(const void *L, int64_t l_bstride, int dtype, int B,
     return ORACLE_OK;
 }
 
+
+/*
+ * oracle_verify_tree_f64: token-tree verification (reading R10) for B batch rows
+ * of N nodes each.
+ *
+ * Z, D: target and draft logits, row (b, j) of node j at b*bstride + j*V.
+ * parent[b*N + j], tok[b*N + j]: the tree (entry 0 of tok unused).
+ * u_acc[b*N + j]: the uniform of node j's acceptance test (entry 0 unused);
+ * u_smp[b]: the final draw (double here; oracle_verify_tree below takes
+ * binary32 uniforms).  Outputs: accept_len[b] (accepted nodes, or a
+ * sentinel), out_tok[b*N + i]: the accepted tokens in path order, then the
+ * final token, then -1; out_node[b*N + i] (may be NULL): the accepted node
+ * ids, then -1.
+ */
+int oracle_verify_tree_f64(const void *Z, int64_t z_bstride, const void *D,
+                           int64_t d_bstride, int dtype, int B, int N, int64_t V,
+                           const int32_t *parent, const int32_t *tok, const float *T,
+                           const double *u_acc, const double *u_smp, int32_t *accept_len,
+                           int32_t *out_tok, int32_t *out_node)
+{
+    if (!Z || !D || !parent || !tok || !T || !u_acc || !u_smp || !accept_len || !out_tok ||
+        B < 0 || N < 1 || V < 1)
+        return ORACLE_BAD_ARG;
+    double *zrow = (double *)malloc((size_t)V * sizeof(double));
+    double *r = (double *)malloc((size_t)V * sizeof(double));
+    double *q = (double *)malloc((size_t)V * sizeof(double));
+    double *w = (double *)malloc((size_t)V * sizeof(double));
+    if (!zrow || !r || !q || !w) {
+        free(zrow); free(r); free(q); free(w);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parent + (int64_t)b * N;
+        const int32_t *tk = tok + (int64_t)b * N;
+        int32_t *out = out_tok + (int64_t)b * N;
+        int32_t *node = out_node ? out_node + (int64_t)b * N : NULL;
+        for (int j = 0; j < N; ++j) {
+            out[j] = -1;
+            if (node)
+                node[j] = -1;
+        }
+        double t = (double)T[b];
+        if (isnan(t) || t < 0.0) {
+            accept_len[b] = -1;
+            continue;
+        }
+        int bad_tree = par[0] != -1;
+        for (int j = 1; j < N; ++j)
+            if (par[j] < 0 || par[j] >= j || tk[j] < 0 || tk[j] >= V)
+                bad_tree = 1;
+        if (bad_tree) {
+            accept_len[b] = -2;
+            continue;
+        }
+        int greedy = (t == 0.0);
+        int rows_ok = 1;
+        for (int j = 0; j < N && rows_ok; ++j) {
+            load_row(Z, dtype, (int64_t)b * z_bstride + (int64_t)j * V, V, zrow);
+            rows_ok = row_is_valid(zrow, V, greedy);
+            load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)j * V, V, zrow);
+            rows_ok = rows_ok && row_is_valid(zrow, V, greedy);
+        }
+        if (!rows_ok) {
+            accept_len[b] = -1;
+            continue;
+        }
+
+        int cur = 0, depth = 0;
+        double m, S;
+        load_row(Z, dtype, (int64_t)b * z_bstride, V, zrow);
+        if (!greedy)
+            softmax_temp(zrow, V, t, r, &m, &S); /* r = p of the root */
+        for (;;) {
+            /* zrow holds the current node's target row */
+            int moved = 0;
+            if (greedy) {
+                int64_t a = argmax_lowest(zrow, V);
+                for (int c = cur + 1; c < N; ++c)
+                    if (par[c] == cur && tk[c] == a) {
+                        moved = c;
+                        break;
+                    }
+                if (!moved) {
+                    out[depth] = (int32_t)a;
+                    break;
+                }
+            } else {
+                int have_q = 0;
+                for (int c = cur + 1; c < N && !moved; ++c) {
+                    if (par[c] != cur)
+                        continue;
+                    if (!have_q) {
+                        load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)cur * V, V, w);
+                        softmax_temp(w, V, t, q, &m, &S);
+                        have_q = 1;
+                    }
+                    const int32_t x = tk[c];
+                    int acc;
+                    if (q[x] == 0.0)
+                        acc = r[x] > 0.0;
+                    else
+                        acc = u_acc[(int64_t)b * N + c] < r[x] / q[x];
+                    if (acc) {
+                        moved = c;
+                    } else {
+                        /* the residual: norm(max(0, r - q)), r kept if all zero */
+                        double tot = 0.0;
+                        for (int64_t v = 0; v < V; ++v) {
+                            double d = r[v] - q[v];
+                            w[v] = d > 0.0 ? d : 0.0;
+                            tot += w[v];
+                        }
+                        if (tot > 0.0)
+                            for (int64_t v = 0; v < V; ++v)
+                                r[v] = w[v] / tot;
+                    }
+                }
+                if (!moved) {
+                    out[depth] = (int32_t)inverse_cdf(r, V, u_smp[b]);
+                    break;
+                }
+            }
+            out[depth] = tk[moved];
+            if (node)
+                node[depth] = moved;
+            ++depth;
+            cur = moved;
+            load_row(Z, dtype, (int64_t)b * z_bstride + (int64_t)cur * V, V, zrow);
+            if (!greedy)
+                softmax_temp(zrow, V, t, r, &m, &S);
+        }
+        accept_len[b] = depth;
+    }
+    free(zrow); free(r); free(q); free(w);
+    return ORACLE_OK;
+}
+
+/* The same with binary32 uniforms, as the GPU library takes them. */
+int oracle_verify_tree(const void *Z, int64_t z_bstride, const void *D, int64_t d_bstride,
+                       int dtype, int B, int N, int64_t V, const int32_t *parent,
+                       const int32_t *tok, const float *T, const float *u_acc,
+                       const float *u_smp, int32_t *accept_len, int32_t *out_tok,
+                       int32_t *out_node)
+{
+    if (!u_acc || !u_smp || B < 0 || N < 1)
+        return ORACLE_BAD_ARG;
+    double *ua = (double *)malloc(((size_t)B * N + 1) * sizeof(double));
+    double *us = (double *)malloc(((size_t)B + 1) * sizeof(double));
+    if (!ua || !us) {
+        free(ua); free(us);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t i = 0; i < (int64_t)B * N; ++i)
+        ua[i] = (double)u_acc[i];
+    for (int b = 0; b < B; ++b)
+        us[b] = (double)u_smp[b];
+    int rc = oracle_verify_tree_f64(Z, z_bstride, D, d_bstride, dtype, B, N, V, parent, tok,
+                                    T, ua, us, accept_len, out_tok, out_node);
+    free(ua); free(us);
+    return rc;
+}
 
 /* ------------------------------------------------------------------------
  * Draft-side sampling (reading R8).

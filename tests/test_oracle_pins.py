@@ -591,3 +591,210 @@ def test_draft_sample_special_cases():
     bad = z.copy()
     bad[0, 0, 2] = np.nan
     assert oracle.draft_sample(bad, np.ones(1, np.float32), seed=1, offset=1)[0, 0] == -1
+
+
+# ---------------------------------------------------------------------------
+# token-tree verification (multi-step speculative sampling over a tree)
+# ---------------------------------------------------------------------------
+def _tree_call(Z, D, par, tok, T, ua, us):
+    r = oracle.verify_tree(Z[None], D[None], np.asarray(par, np.int32)[None],
+                           np.asarray(tok, np.int32)[None], [T],
+                           np.asarray(ua, np.float64)[None], [us], f64_uniforms=True)
+    return int(r["accept_len"][0]), [int(t) for t in r["out_tok"][0]], \
+        [int(n) for n in r["out_node"][0]]
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tree_exactness_by_enumeration(seed):
+    """Exactness of the tree rule (SpecInfer's multi-step speculative
+    sampling; "SSD: drafting and verification on separate GPUs": the method
+    does not change the output law).  Tree: root with children 1 and 2
+    (tokens drawn independently from the root's q), node 1 with child 3
+    (token drawn from node 1's q).  The law of the first two output tokens
+    (completed from the target when only one is produced) must be
+    p_root(t1) * p_t1(t2), where p_v is the target law after token v.  All
+    measures come from bisection on the oracle; V = 3."""
+    rng = np.random.default_rng(300 + seed)
+    V, T = 3, float(np.float32(0.8))
+    Zr = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    Dr = (Zr + rng.standard_normal(V) * 1.5).astype(np.float32)
+    Zc = (rng.standard_normal((V, V)) * 1.5).astype(np.float32)      # target after token v
+    Dc = (Zc + rng.standard_normal((V, V)) * 1.5).astype(np.float32)
+    Zg = rng.standard_normal(V).astype(np.float32)
+    pr, qr = softmax_ref(Zr, T), softmax_ref(Dr, T)
+    pc, qc = softmax_ref(Zc, T), softmax_ref(Dc, T)
+    par = [-1, 0, 0, 1]
+    law = np.zeros((V, V))
+    for x1, x2, y in itertools.product(range(V), repeat=3):
+        w = qr[x1] * qr[x2] * qc[x1, y]
+        Z = np.stack([Zr, Zc[x1], Zc[x2], Zg])
+        D = np.stack([Dr, Dc[x1], Dc[x2], Dr])
+        tok = [0, x1, x2, y]
+        call = lambda u1, u2, u3, us: _tree_call(Z, D, par, tok, T, [0.5, u1, u2, u3], us)
+        a1, acc1, rej1 = _split(lambda u: call(u, 0.5, 0.5, 0.5)[2][0] == 1)
+        if acc1 is not None:
+            a3, acc3, rej3 = _split(lambda u: call(acc1, 0.5, u, 0.5)[2][1] == 3)
+            if acc3 is not None:
+                law[x1, y] += w * a1 * a3
+            if rej3 is not None:
+                dist = _token_distribution(lambda u: call(acc1, 0.5, rej3, u)[1][1], V)
+                law[x1] += w * a1 * (1 - a3) * dist
+        if rej1 is not None:
+            a2, acc2, rej2 = _split(lambda u: call(rej1, u, 0.5, 0.5)[2][0] == 2)
+            if acc2 is not None:
+                dist = _token_distribution(lambda u: call(rej1, acc2, 0.5, u)[1][1], V)
+                law[x2] += w * (1 - a1) * a2 * dist
+            if rej2 is not None:
+                dist = _token_distribution(lambda u: call(rej1, rej2, 0.5, u)[1][0], V)
+                law += w * (1 - a1) * (1 - a2) * dist[:, None] * pc
+    target = pr[:, None] * pc
+    assert abs(law.sum() - 1.0) < 1e-12
+    assert np.max(np.abs(law - target)) < 1e-12
+
+
+def test_tree_exactness_detects_a_missing_residual_update():
+    """The enumeration is sensitive: trying the second child against the
+    unchanged p (no residual update after the first rejection) changes the
+    law of the first token.  Computed here in numpy for two leaf children."""
+    rng = np.random.default_rng(9)
+    p = softmax_ref(rng.standard_normal(4) * 1.5, 1.0)
+    q = softmax_ref(rng.standard_normal(4) * 1.5, 1.0)
+    a = np.minimum(1.0, p / q)
+    rej1 = 1 - (q * a).sum()
+    wrong = q * a + rej1 * (q * a) + rej1 * (1 - (q * a).sum()) * p
+    assert np.max(np.abs(wrong - p)) > 1e-3
+
+
+def test_tree_chain_is_the_chain_rule():
+    """A tree that is a chain (parent[j] = j - 1, tok[j] = x[j-1]) gives the
+    chain verify-and-recover step's tokens."""
+    rng = np.random.default_rng(41)
+    B, k, V = 96, 4, 20
+    Z = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    D = (Z + rng.standard_normal((B, k + 1, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, k)).astype(np.int32)
+    x[::3] = np.argmax(Z[::3, :k], axis=2)          # some greedy agreement
+    T = rng.choice(np.array([0.0, 0.6, 1.0, 1.4], np.float32), B)
+    ua = rng.random((B, k)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    chain = oracle.verify_recover(Z, D[:, :k], x, T, ua, us)
+    par = np.tile(np.arange(-1, k, dtype=np.int32), (B, 1))
+    tok = np.concatenate([np.zeros((B, 1), np.int32), x], axis=1)
+    uat = np.concatenate([np.zeros((B, 1), np.float32), ua], axis=1)
+    tree = oracle.verify_tree(Z, D, par, tok, T, uat, us)
+    assert np.array_equal(tree["accept_len"], chain["accept_len"])
+    assert np.array_equal(tree["out_tok"], chain["out_tok"])
+    n = tree["accept_len"]
+    for b in range(B):
+        assert list(tree["out_node"][b, :n[b]]) == list(range(1, n[b] + 1))
+    assert 0 < (n > 0).sum() < B
+
+
+def test_tree_single_node_is_an_inverse_cdf_draw():
+    """A tree of one node draws the token from softmax(z / T) by inverse CDF
+    (scipy softmax, numpy cumulative sum and searchsorted)."""
+    rng = np.random.default_rng(3)
+    B, V = 400, 50
+    Z = (rng.standard_normal((B, 1, V)) * 2).astype(np.float32)
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    r = oracle.verify_tree(Z, Z, np.full((B, 1), -1, np.int32), np.zeros((B, 1), np.int32), T,
+                           np.zeros((B, 1), np.float32), us)
+    assert (r["accept_len"] == 0).all()
+    for b in range(B):
+        c = np.cumsum(softmax_ref(Z[b, 0], float(T[b])))
+        assert r["out_tok"][b, 0] == np.searchsorted(c, float(us[b]) * c[-1], side="right")
+
+
+def _random_trees(rng, B, N):
+    par = np.full((B, N), -1, np.int32)
+    for j in range(1, N):
+        par[:, j] = rng.integers(0, j, B)
+    return par
+
+
+def test_tree_greedy_invariants():
+    """T = 0: every accepted node's token is the argmax of its parent's
+    target row and no earlier sibling carries it; the last node has no child
+    with its argmax, and the final token is that argmax."""
+    rng = np.random.default_rng(17)
+    B, N, V = 300, 12, 6
+    Z = rng.integers(-2, 3, (B, N, V)).astype(np.float32)             # ties
+    D = rng.standard_normal((B, N, V)).astype(np.float32)
+    par = _random_trees(rng, B, N)
+    am = np.argmax(Z, axis=2)                                          # lowest index on ties
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    hit = rng.random((B, N)) < 0.6
+    for b in range(B):
+        for j in range(1, N):
+            if hit[b, j]:
+                tok[b, j] = am[b, par[b, j]]
+    r = oracle.verify_tree(Z, D, par, tok, np.zeros(B, np.float32), rng.random((B, N)),
+                           rng.random(B))
+    n = r["accept_len"]
+    assert (n >= 0).all() and (n >= 2).any()
+    for b in range(B):
+        cur = 0
+        for i in range(n[b]):
+            c = r["out_node"][b, i]
+            assert par[b, c] == cur and tok[b, c] == am[b, cur] == r["out_tok"][b, i]
+            assert not any(par[b, s] == cur and tok[b, s] == tok[b, c] for s in range(1, c))
+            cur = c
+        assert r["out_tok"][b, n[b]] == am[b, cur]
+        assert not any(par[b, s] == cur and tok[b, s] == am[b, cur] for s in range(1, N))
+        assert (r["out_tok"][b, n[b] + 1:] == -1).all() and (r["out_node"][b, n[b]:] == -1).all()
+
+
+def test_tree_sentinels():
+    rng = np.random.default_rng(5)
+    B, N, V = 6, 4, 9
+    Z = rng.standard_normal((B, N, V)).astype(np.float32)
+    D = rng.standard_normal((B, N, V)).astype(np.float32)
+    par = np.tile(np.array([-1, 0, 0, 1], np.int32), (B, 1))
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    T = np.ones(B, np.float32)
+    T[0] = -1.0                      # invalid temperature
+    par[1, 2] = 2                    # parent not before the node
+    tok[2, 3] = V                    # token out of range
+    par[3, 0] = 0                    # root with a parent
+    D[4, 3, 2] = np.nan              # NaN in a leaf's draft row (read too)
+    r = oracle.verify_tree(Z, D, par, tok, T, rng.random((B, N)), rng.random(B))
+    assert list(r["accept_len"]) [:5] == [-1, -2, -2, -2, -1]
+    assert r["accept_len"][5] >= 0
+    assert (r["out_tok"][:5] == -1).all() and (r["out_node"][:5] == -1).all()
+
+
+def test_tree_law_by_sampling():
+    """Bushier tree (root with three children drawn from q, each with two
+    children drawn from that child's q), 2 * 10^5 rows: the first two tokens
+    follow p_root(t1) * p_t1(t2) (chi-square)."""
+    rng = np.random.default_rng(23)
+    B, V, T = 200_000, 5, 1.0
+    Zr = rng.standard_normal(V).astype(np.float32) * 1.5
+    Dr = (Zr + rng.standard_normal(V) * 1.5).astype(np.float32)
+    Zc = (rng.standard_normal((V, V)) * 1.5).astype(np.float32)
+    Dc = (Zc + rng.standard_normal((V, V)) * 1.5).astype(np.float32)
+    pr, qr = softmax_ref(Zr, T), softmax_ref(Dr, T)
+    pc, qc = softmax_ref(Zc, T), softmax_ref(Dc, T)
+    par = np.tile(np.array([-1, 0, 0, 0, 1, 1, 2, 2, 3, 3], np.int32), (B, 1))
+    N = par.shape[1]
+    tok = np.zeros((B, N), np.int32)
+    tok[:, 1:4] = _draw_from(qr, rng.random((B, 3)))
+    for j in range(4, N):
+        parent_tok = tok[:, par[0, j]]
+        tok[:, j] = (np.cumsum(qc[parent_tok], axis=1) <= rng.random(B)[:, None]).sum(1).clip(0, V - 1)
+    Z = np.empty((B, N, V), np.float32)
+    D = np.empty((B, N, V), np.float32)
+    Z[:, 0], D[:, 0] = Zr, Dr
+    Z[:, 1:], D[:, 1:] = Zc[tok[:, 1:]], Dc[tok[:, 1:]]
+    r = oracle.verify_tree(Z, D, par, tok, np.full(B, T, np.float32),
+                           rng.random((B, N)).astype(np.float32),
+                           rng.random(B).astype(np.float32))
+    n, out = r["accept_len"], r["out_tok"]
+    t1 = out[:, 0].astype(np.int64)
+    t2 = np.where(n >= 1, out[:, 1],
+                  (np.cumsum(pc[t1], axis=1) <= rng.random(B)[:, None]).sum(1).clip(0, V - 1))
+    obs = np.bincount(t1 * V + t2, minlength=V * V)
+    exp = (pr[:, None] * pc).reshape(-1) * B
+    assert scipy.stats.chisquare(obs, exp).pvalue > 1e-4
+    assert (n >= 1).mean() > 0.3 and (n == 0).any() and (n == 2).any()
