@@ -304,6 +304,54 @@ def topk_verify(ssd, w, inp, dev, K=32, top_p=0.9, reps=50):
             "stream_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
 
 
+def tree_verify(ssd, W, dev, reps=20):
+    """Token-tree verification on the tree workload (64 batch rows, trees of
+    widths (4, 2, 1) = 21 nodes, V = 151936, bf16, T = 0.7): milliseconds per
+    call, the statistics pass's GB/s over the 2N rows and the walk's time."""
+    import torch
+    cfg = W.TREE_B64
+    par = W.tree_parents(cfg["widths"])
+    inp = W.make_tree_inputs(cfg["B"], par, cfg["V"], dtype=cfg["dtype"], temp=cfg["temp"],
+                             z_std=cfg["z_std"], d_std=cfg["d_std"], peaks=cfg["peaks"],
+                             peak_boost=cfg["peak_boost"], seed=4242, device=dev)
+    B, N, V = inp["Z"].shape
+    out = {}
+
+    def call():
+        return ssd.ssd_verify_tree(inp["Z"], inp["D"], inp["parent"], inp["tok"], inp["T"],
+                                   inp["u_acc"], inp["u_smp"], ws=out.get("ws"), out=out)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    ssd.profile_begin(8 * reps)
+    for _ in range(reps):
+        call()
+    torch.cuda.synchronize()
+    prof = ssd.profile_end()
+    per = {k: v["total_ms"] / max(1, v["timed"]) for k, v in prof.items()}
+    nbytes = B * 2 * N * V * inp["Z"].element_size()
+    acc = out["accept_len"].float().mean().item()
+    res = {"workload": "B=%d N=%d (widths %s) V=%d bf16 T=0.7" % (B, N, cfg["widths"], V),
+           "ms": round(ms, 4), "rows_per_s": round(B / (ms / 1e3), 1),
+           "mean_accepted": round(acc, 3)}
+    if "stats" in per:
+        res["stats_ms"] = round(per["stats"], 4)
+        res["stats_gbs"] = round(nbytes / (per["stats"] / 1e3) / 1e9, 1)
+    if "tree_walk" in per:
+        res["walk_ms"] = round(per["tree_walk"], 4)
+    del inp
+    return res
+
+
 def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
     """Time the oracle (as it stands, one host thread) on a bounded sample of
     the batch rows: verify_recover + forked_topf + the dict cache."""
@@ -429,6 +477,7 @@ def gpu_arm(args):
         line["latency_b1"] = b1_latency(ssd, W, dev)
         line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)
         line["topk_verify"] = topk_verify(ssd, w, inp, dev)
+        line["tree_verify"] = tree_verify(ssd, W, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
     if rank == 0:

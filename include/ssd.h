@@ -87,6 +87,7 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 #define SSD_MAX_K 31   /* draft length: one warp ballot holds k flags */
 #define SSD_MAX_F 16   /* forked recovery fan-out                    */
 #define SSD_MAX_M 64   /* masked tokens per (b, position)            */
+#define SSD_MAX_TREE_NODES 64  /* nodes of one draft tree              */
 
 SSD_API const char *ssd_status_string(ssd_status s);
 
@@ -343,6 +344,56 @@ SSD_API ssd_status ssd_verify_topk(const void *Z, int64_t z_bstride, const void 
                            const float *u_acc, int32_t *accept_len, float *p_at_x,
                            float *q_at_x, const float *u_smp, int32_t *out_tok, void *ws,
                            size_t ws_bytes, ssd_stream_t stream);
+
+/*
+ * ssd_verify_tree -- verification of a draft token tree per batch row (the
+ * "tanishqkumar/ssd" summary's tree decoding), by the multi-step speculative
+ * sampling of SpecInfer (Miao et al. 2024), which keeps the target's output
+ * law when the children of a node were drawn independently from the
+ * draft's q at that node:
+ *   start at the root with r = p(root); try the children of the current
+ *   node in increasing node index; child x is accepted when
+ *   u_acc[b, child] < r(x) / q(x) (q(x) == 0: accepted iff r(x) > 0); an
+ *   accepted child becomes the current node with r = its p; a rejection
+ *   replaces r by norm(max(0, r - q)) (unchanged if that is all zero); when
+ *   the children are exhausted the final token is drawn from r by inverse
+ *   CDF with u_smp[b] (smallest v whose prefix sum exceeds u times the
+ *   total).  T == 0 rows accept the first child whose token is the argmax
+ *   (lowest index) of the current node's target row and end with that
+ *   argmax.
+ * One streaming pass over all 2N rows gives each row's maximum, argmax and
+ * sum; then one CTA per batch row walks the tree, with one pass over the
+ * current node's two rows per rejection (the next residual mass) and one for
+ * the final draw when it is not already known.
+ *   Z        : target logits at the nodes, row (b, j) at Z + b*z_bstride +
+ *              j*V (the target's logits after node j's path; node 0 is the
+ *              last committed position).  z_bstride >= N*V.
+ *   D        : draft logits at the nodes, same layout (q of node j's
+ *              children).  All N rows are read and checked, leaves included.
+ *   N        : nodes per tree, 1 <= N <= SSD_MAX_TREE_NODES.
+ *   parent   : [B, N] int32 device: parent[b, 0] == -1, 0 <= parent[b, j] < j.
+ *   tok      : [B, N] int32 device: node j's token (entry 0 unused).
+ *   T        : [B] temperatures; u_acc: [B, N] uniforms in [0, 1), entry
+ *              (b, j) tests node j (entry 0 unused); u_smp: [B].
+ *   accept_len : [B] accepted nodes (path depth), or a sentinel: -1 for
+ *              T < 0 or NaN or an invalid row (as ssd_verify), -2 for an
+ *              invalid tree (parent or token out of range).
+ *   out_tok  : [B, N]: the accepted tokens in path order, the final token,
+ *              then -1 (all -1 on a sentinel).
+ *   out_node : [B, N] or NULL: the accepted node ids, then -1.
+ *   ws       : ssd_tree_workspace_bytes(B, N, V) bytes (its first word is
+ *              the device error word, as for ssd_verify).
+ * Errors: SSD_ERR_INVALID_ARG for null required pointers, sizes out of
+ * range, strides below N*V or misaligned pointers; SSD_ERR_WORKSPACE when
+ * ws_bytes is too small; SSD_ERR_CUDA when a launch fails.
+ */
+SSD_API size_t ssd_tree_workspace_bytes(int B, int N, int V);
+SSD_API ssd_status ssd_verify_tree(const void *Z, int64_t z_bstride, const void *D,
+                           int64_t d_bstride, ssd_dtype dtype, int B, int N, int V,
+                           const int32_t *parent, const int32_t *tok, const float *T,
+                           const float *u_acc, const float *u_smp, int32_t *accept_len,
+                           int32_t *out_tok, int32_t *out_node, void *ws, size_t ws_bytes,
+                           ssd_stream_t stream);
 
 /*
  * Speculation cache ([SSD] roadmap: the speculation cache; [SUM] cache

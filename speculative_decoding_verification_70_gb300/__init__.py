@@ -28,6 +28,7 @@ from ._binding import (  # noqa: F401
     ssd_verify_fork,
     ssd_verify_fork_cache,
     ssd_verify_topk,
+    ssd_verify_tree,
     workspace_bytes,
 )
 

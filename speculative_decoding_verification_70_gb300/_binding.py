@@ -57,6 +57,9 @@ SIGNATURES = [
     ("ssd_topk_workspace_bytes", _Z, [_I, _I, _I, _I]),
     ("ssd_verify_topk", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P,
                              _P, _P, _P, _Z, _P]),
+    ("ssd_tree_workspace_bytes", _Z, [_I, _I, _I]),
+    ("ssd_verify_tree", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                             _P, _Z, _P]),
     ("ssd_verify_fork_cache", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _I, _P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _Z, _P]),
     ("ssd_spec_cache_create", _I, [_I, _I, _P]),
@@ -452,6 +455,52 @@ def ssd_verify_topk(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.
         _dev(o["accept_len"], "accept_len"), _dev(o["p_at_x"], "p_at_x"),
         _dev(o["q_at_x"], "q_at_x"), _opt(u_smp, "u_smp"), _dev(o["out_tok"], "out_tok"),
         wp, wn, _stream(stream)))
+    o["ws"] = ws
+    return o
+
+
+def ssd_verify_tree(Z: torch.Tensor, D: torch.Tensor, parent: torch.Tensor,
+                    tok: torch.Tensor, T: torch.Tensor, u_acc: torch.Tensor,
+                    u_smp: torch.Tensor, *, ws: Optional[torch.Tensor] = None,
+                    out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Verify a draft token tree per batch row (multi-step speculative
+    sampling; greedy at T == 0).  Z, D: [B, N, V] target and draft logits at
+    the N nodes; parent, tok: [B, N] int32 (parent[:, 0] == -1, parent[:, j]
+    < j); u_acc: [B, N] float32 (entry j tests node j), u_smp: [B].
+
+    Returns accept_len [B], out_tok [B, N] (accepted tokens, the final
+    token, then -1) and out_node [B, N] (accepted node ids, then -1)."""
+    lib = load_library()
+    if Z.dim() != 3 or D.shape != Z.shape:
+        raise ValueError("Z and D must both be [B, N, V]")
+    if Z.dtype != D.dtype:
+        raise TypeError("Z and D must share a dtype")
+    B, N, V = Z.shape
+    for t, name in ((parent, "parent"), (tok, "tok")):
+        _want(t, torch.int32, name)
+        if t.shape != (B, N):
+            raise ValueError("%s must be [B, N]" % name)
+    _want(T, torch.float32, "T")
+    _want(u_acc, torch.float32, "u_acc")
+    _want(u_smp, torch.float32, "u_smp")
+    dev = Z.device
+    if ws is None:
+        n = lib.ssd_tree_workspace_bytes(B, N, V)
+        if n == 0:
+            raise SSDError("ssd_tree_workspace_bytes", 1)
+        ws = new_workspace(n, dev)
+    wp, wn = _ws_ptr(ws)
+    o = {} if out is None else out
+    if "accept_len" not in o:
+        o["accept_len"] = torch.empty(B, dtype=torch.int32, device=dev)
+        o["out_tok"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+        o["out_node"] = torch.empty((B, N), dtype=torch.int32, device=dev)
+    _check("ssd_verify_tree", lib.ssd_verify_tree(
+        _dev(Z, "Z"), N * V, _dev(D, "D"), N * V, _dtype_code(Z), B, N, V,
+        _dev(parent, "parent"), _dev(tok, "tok"), _dev(T, "T"), _dev(u_acc, "u_acc"),
+        _dev(u_smp, "u_smp"), _dev(o["accept_len"], "accept_len"),
+        _dev(o["out_tok"], "out_tok"), _dev(o["out_node"], "out_node"), wp, wn,
+        _stream(stream)))
     o["ws"] = ws
     return o
 

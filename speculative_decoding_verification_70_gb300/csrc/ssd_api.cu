@@ -25,6 +25,7 @@ cudaError_t launch_topk_verify(const TopkParams& p, int dtype, bool vec, cudaStr
 #define SSD_TOPK_MAX_GROUP 32
 #endif
 cudaError_t launch_topk_finalize(const TopkParams& p, cudaStream_t s);
+cudaError_t launch_tree_walk(const TreeParams& p, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
@@ -620,6 +621,48 @@ ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, i
   dp.err = sp.err;
   ProfScope ps("draft_finalize", S(stream));
   return cuda_status(launch_draft_finalize(dp, S(stream)));
+}
+
+size_t ssd_tree_workspace_bytes(int B, int N, int V) {
+  if (B < 1 || N < 1 || N > kMaxTreeNodes || V < 2) return 0;
+  return make_tree_layout(B, N, V).total;
+}
+
+ssd_status ssd_verify_tree(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
+                           ssd_dtype dtype, int B, int N, int V, const int32_t* parent,
+                           const int32_t* tok, const float* T, const float* u_acc,
+                           const float* u_smp, int32_t* accept_len, int32_t* out_tok,
+                           int32_t* out_node, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (!Z || !D || !parent || !tok || !T || !u_acc || !u_smp || !accept_len || !out_tok || !ws)
+    return SSD_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || N > kMaxTreeNodes || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
+  if (z_bstride < static_cast<int64_t>(N) * V || d_bstride < static_cast<int64_t>(N) * V)
+    return SSD_ERR_INVALID_ARG;
+  if (!aligned(Z, esize(dtype)) || !aligned(D, esize(dtype)) || !aligned(ws, 256))
+    return SSD_ERR_INVALID_ARG;
+  const TreeLayout L = make_tree_layout(B, N, V, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(Z, z_bstride, V, dtype) && vec_ok(D, d_bstride, V, dtype);
+  const int dt = dtype == SSD_BF16 ? 1 : 0;
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = Z; sp.zb = z_bstride; sp.Pz = N;
+  sp.D = D; sp.db = d_bstride; sp.Pds = N; sp.Pdf = 0;
+  sp.T = T; sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = L.R; sp.Rp = L.R;
+  sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  cudaError_t e = run_stats(sp, B, dt, vec, S(stream));  // all 2N rows, one launch
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  TreeParams tp;
+  memset(&tp, 0, sizeof tp);
+  tp.Z = Z; tp.zb = z_bstride; tp.D = D; tp.db = d_bstride;
+  tp.B = B; tp.N = N; tp.V = V; tp.C = L.ch.C; tp.Rp = L.R;
+  tp.parent = parent; tp.tok = tok; tp.T = T; tp.u_acc = u_acc; tp.u_smp = u_smp;
+  tp.part = sp.part; tp.accept_len = accept_len; tp.out_tok = out_tok; tp.out_node = out_node;
+  tp.err = sp.err;
+  ProfScope ps("tree_walk", S(stream));
+  return cuda_status(launch_tree_walk(tp, dt, vec, S(stream)));
 }
 
 size_t ssd_topk_workspace_bytes(int B, int k, int V, int K) {

@@ -133,6 +133,31 @@ struct ResidualParams {
   int32_t* out_tok;    // [B][k+1]
 };
 
+// Token-tree verification (ssd_verify_tree).
+constexpr int kMaxTreeNodes = 64;
+
+struct TreeLayout {
+  size_t err, part, total;
+  int R;          // rows per batch row: N target, N draft
+  Chunking ch;
+};
+
+struct TreeParams {
+  const void* Z; int64_t zb;
+  const void* D; int64_t db;
+  int B, N, V, C, Rp;
+  const int32_t* parent;   // [B][N]
+  const int32_t* tok;      // [B][N]
+  const float* T;
+  const float* u_acc;      // [B][N]
+  const float* u_smp;      // [B]
+  const PartStat* part;    // [B][Rp][C]: target rows 0..N-1, draft rows N..2N-1
+  int32_t* accept_len;
+  int32_t* out_tok;        // [B][N]
+  int32_t* out_node;       // [B][N] or null
+  int* err;
+};
+
 // Top-k / top-p filtered verify (ssd_verify_topk).
 constexpr int kMaxTopK = 32;
 
@@ -292,6 +317,17 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
   L.gpart = off;                    off = align256(off + sizeof(GumbelPart) * B * L.Pf * C);
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
+  L.total = off;
+  return L;
+}
+
+inline TreeLayout make_tree_layout(int B, int N, int V, int esize = 4) {
+  TreeLayout L;
+  L.R = 2 * N;
+  L.ch = make_chunking(B, L.R, V, esize);
+  size_t off = 0;
+  L.err = off;                      off = align256(off + 16);
+  L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * L.ch.C);
   L.total = off;
   return L;
 }

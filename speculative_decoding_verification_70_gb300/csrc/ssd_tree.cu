@@ -1,0 +1,388 @@
+// ssd_tree.cu -- token-tree verification: the walk over a draft tree of N
+// nodes per batch row after the statistics pass over its 2N logit rows.
+//
+// Sources: "tanishqkumar/ssd" summary, module notes (tree decoding in
+// asynchronous speculative decoding; the temperature sampler: greedy at
+// T = 0); "SSD: drafting and verification on separate GPUs", "What changes
+// in SSD" (verification keeps the target's output law); the verification
+// rule for a tree whose children were drawn from the draft's q at their
+// parent is the multi-step speculative sampling of SpecInfer (Miao et al.
+// 2024): at the current node with target law r (initially its p) the
+// children are tried in index order, a child x is accepted when
+// u < r(x)/q(x), a rejection replaces r by norm(max(0, r - q)), and when the
+// children run out the token is drawn from r.
+//
+// Closed form used here (instead of materialising r): after j rejections at
+// a node, r_j = max(0, p - c_j q) / W(c_j) with W(c) = sum_v max(0, p - c q),
+// c_0 = 0 and c_{j+1} = c_j + W(c_j).  In the row's own units (e_z = 2^((z -
+// m_z) c2), e_d likewise, S_z, S_d their sums) that is the weight
+// w(v) = max(0, e_z(v) - rho_j e_d(v)) with rho_j = c_j S_z / S_d and the
+// scaled mass Wsc_j = sum_v w(v) = W(c_j) S_z; rho_{j+1} = rho_j + Wsc_j / S_d.
+// The acceptance test u < r_j(x)/q(x) becomes u Wsc_j e_d(x) < S_d w(x), and
+// each rejection costs one pass over the node's two rows for the next Wsc.
+//
+// Layout of the work: one CTA of kTreeThreads per batch row.  Every thread
+// owns a contiguous range of E elements of a row (so that the draw's
+// inverse CDF is a block scan of per-thread sums followed by a walk of one
+// range); the decisions are taken by thread 0 and broadcast through shared
+// memory; passes use all threads, with double-float element weights and
+// compensated sums, and the draw converts the per-thread sums to exact
+// 2^-48 fixed point for an order-independent scan.
+#include <math.h>
+
+#include "ssd_device.cuh"
+#include "ssd_layout.h"
+#include "ssd_merge.cuh"
+#include "ssd_scan.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kTreeThreads = 512;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr float kFix = 281474976710656.0f;  // 2^48
+
+struct TreeSmem {
+  float2 tab[64];
+  float2 c2;
+  int par[kMaxTreeNodes], tok[kMaxTreeNodes];
+  float m[2 * kMaxTreeNodes];                // row maxima: target rows, then draft rows
+  float sh[2 * kMaxTreeNodes], sl[2 * kMaxTreeNodes];  // row sums (float pairs)
+  int am[2 * kMaxTreeNodes];                 // lowest index of the maximum
+  int flags, bad;
+  float rh[kTreeWarps], rl[kTreeWarps];      // block sums
+  long long scan[kTreeWarps];
+  int accept;                                // thread 0's decision
+  int sel, last;                             // the draw
+};
+
+// Block-wide inclusive scan of int64 (exact).  *total gets the block total.
+__device__ __forceinline__ long long tree_scan_i64(long long v, long long* sm, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) sm[warp] = v;
+  __syncthreads();
+  long long off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kTreeWarps; ++w) {
+    const long long s = sm[w];
+    if (w < warp) off += s;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return v + off;
+}
+
+// Block sum of float pairs (every thread gets the total).
+__device__ __forceinline__ void tree_sum_df(float h, float l, TreeSmem& sm, float& th,
+                                            float& tl) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(kFull, h, o);
+    const float ol = __shfl_xor_sync(kFull, l, o);
+    df_acc(h, l, oh, ol);
+  }
+  if (lane == 0) {
+    sm.rh[warp] = h;
+    sm.rl[warp] = l;
+  }
+  __syncthreads();
+  th = 0.f;
+  tl = 0.f;
+  for (int w = 0; w < kTreeWarps; ++w) df_acc(th, tl, sm.rh[w], sm.rl[w]);
+  __syncthreads();
+}
+
+// The draw weight of one element: max(0, e_z - rho e_d) as a float pair
+// (e_z alone when rho == 0).  Returns false when the weight is zero.
+__device__ __forceinline__ bool tree_weight(float z, float d, float mz, float md, float2 c2,
+                                            float rho_h, float rho_l, const float2* tab,
+                                            float& wh, float& wl) {
+  float xh, xl, ah, al;
+  arg_df(z, mz, c2.x, c2.y, xh, xl);
+  exp2_df(xh, xl, tab, ah, al);
+  if (rho_h == 0.f) {
+    wh = ah;
+    wl = al;
+    return ah > 0.f;
+  }
+  float bh, bl, rbh, rbl;
+  arg_df(d, md, c2.x, c2.y, xh, xl);
+  exp2_df(xh, xl, tab, bh, bl);
+  df_mul(rho_h, rho_l, bh, bl, rbh, rbl);
+  df_sub(ah, al, rbh, rbl, wh, wl);
+  return wh > 0.f;
+}
+
+// One pass over the node's rows: this thread's compensated sum of the
+// weights of its range and the last index with a positive weight (-1).
+template <typename Tag, bool VEC>
+__device__ __forceinline__ void tree_pass(const typename Tag::Elem* zr,
+                                          const typename Tag::Elem* dr, int lo, int hi, float mz,
+                                          float md, float2 c2, float rho_h, float rho_l,
+                                          const float2* tab, float& acc, float& comp,
+                                          int& last) {
+  acc = 0.f;
+  comp = 0.f;
+  last = -1;
+  const bool use_d = rho_h != 0.f;
+  if (VEC) {
+    constexpr int kV = Tag::kVec;
+    for (int v = lo; v < hi; v += kV) {
+      float z[8], d[8];
+      Tag::loadv_cached(zr + v, z);
+      if (use_d) Tag::loadv_cached(dr + v, d);
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        float wh, wl;
+        if (tree_weight(z[e], use_d ? d[e] : 0.f, mz, md, c2, rho_h, rho_l, tab, wh, wl)) {
+          comp_acc(acc, comp, wh, wl);
+          last = v + e;
+        }
+      }
+    }
+  } else {
+    for (int v = lo; v < hi; ++v) {
+      float wh, wl;
+      const float d = use_d ? Tag::load1(dr + v) : 0.f;
+      if (tree_weight(Tag::load1(zr + v), d, mz, md, c2, rho_h, rho_l, tab, wh, wl)) {
+        comp_acc(acc, comp, wh, wl);
+        last = v;
+      }
+    }
+  }
+}
+
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
+  using Elem = typename Tag::Elem;
+  __shared__ TreeSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, N = p.N;
+  load_exp2_table(sm.tab);
+  if (tid < N) {
+    sm.par[tid] = p.parent[static_cast<int64_t>(b) * N + tid];
+    sm.tok[tid] = p.tok[static_cast<int64_t>(b) * N + tid];
+  }
+  if (tid == 0) {
+    sm.flags = 0;
+    sm.bad = 0;
+  }
+  const float T = p.T[b];
+  const bool t_bad = !(T >= 0.f);  // NaN or negative
+  const bool greedy = T == 0.f;
+  const float2 c2 = cta_temp_coeff(greedy || t_bad ? 1.f : T, &sm.c2);  // holds a barrier
+  if (tid < N) {
+    const int pj = sm.par[tid], tj = sm.tok[tid];
+    const bool ok = tid == 0 ? pj == -1 : (pj >= 0 && pj < tid && tj >= 0 && tj < p.V);
+    if (!ok) atomicOr(&sm.bad, 1);
+  }
+  // merged statistics of the 2N rows (one warp per row)
+  const bool do_exp = !greedy && !t_bad;
+  for (int r = warp; r < 2 * N; r += kTreeWarps) {
+    RowStat rs;
+    float h, l;
+    merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c2.x, c2.y, do_exp,
+              sm.tab, rs, h, l);
+    if (lane == 0) {
+      sm.m[r] = rs.m;
+      sm.am[r] = rs.argmax;
+      sm.sh[r] = h;
+      sm.sl[r] = l;
+      if (rs.flags) atomicOr(&sm.flags, rs.flags);
+    }
+  }
+  int32_t* out_tok = p.out_tok + static_cast<int64_t>(b) * N;
+  int32_t* out_node = p.out_node ? p.out_node + static_cast<int64_t>(b) * N : nullptr;
+  for (int i = tid; i < N; i += kTreeThreads) {
+    out_tok[i] = -1;
+    if (out_node) out_node[i] = -1;
+  }
+  __syncthreads();
+  if (t_bad || sm.bad || sm.flags) {  // sentinels, in the order of the oracle's checks
+    if (tid == 0) {
+      p.accept_len[b] = (!t_bad && sm.bad) ? -2 : -1;
+      atomicOr(p.err, t_bad ? 0x1 : (sm.bad ? 0x4 : 0x2));
+    }
+    return;
+  }
+  if (greedy) {  // first child carrying the argmax, then the argmax
+    if (tid == 0) {
+      int cur = 0, depth = 0;
+      for (;;) {
+        const int a = sm.am[cur];
+        int nxt = 0;
+        for (int c = cur + 1; c < N; ++c)
+          if (sm.par[c] == cur && sm.tok[c] == a) {
+            nxt = c;
+            break;
+          }
+        out_tok[depth] = a;
+        if (!nxt) break;
+        if (out_node) out_node[depth] = nxt;
+        ++depth;
+        cur = nxt;
+      }
+      p.accept_len[b] = depth;
+    }
+    return;
+  }
+
+  const int V = p.V;
+  int E = (V + kTreeThreads - 1) / kTreeThreads;
+  E = (E + 7) / 8 * 8;
+  const int lo = min(V, tid * E), hi = min(V, lo + E);
+  const Elem* Zb = static_cast<const Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb;
+  const Elem* Db = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db;
+  int cur = 0, depth = 0, c = 1;
+  float rho_h = 0.f, rho_l = 0.f;           // rho of the current residual
+  float W_h = sm.sh[0], W_l = sm.sl[0];     // its scaled mass (S_z at a fresh node)
+  bool ready = false;                       // acc/comp/last hold a pass for (rho, W)
+  float acc = 0.f, comp = 0.f;
+  int last = -1;
+  for (;;) {
+    while (c < N && sm.par[c] != cur) ++c;
+    if (c >= N) break;  // the children of cur are exhausted
+    const Elem* zr = Zb + static_cast<int64_t>(cur) * V;
+    const Elem* dr = Db + static_cast<int64_t>(cur) * V;
+    const float mz = sm.m[cur], md = sm.m[N + cur];
+    if (tid == 0) {
+      const int x = sm.tok[c];
+      float xh, xl, ezh, ezl, edh, edl;
+      arg_df(Tag::load1(zr + x), mz, c2.x, c2.y, xh, xl);
+      exp2_df(xh, xl, sm.tab, ezh, ezl);
+      arg_df(Tag::load1(dr + x), md, c2.x, c2.y, xh, xl);
+      exp2_df(xh, xl, sm.tab, edh, edl);
+      float wh, wl, th, tl, lh, ll, rh, rl, dh, dl;
+      df_mul(rho_h, rho_l, edh, edl, th, tl);
+      df_sub(ezh, ezl, th, tl, wh, wl);          // w(x) = e_z - rho e_d
+      int ok = 0;
+      if (wh > 0.f) {
+        df_mul(W_h, W_l, edh, edl, th, tl);
+        df_mul(p.u_acc[static_cast<int64_t>(b) * N + c], 0.f, th, tl, lh, ll);  // u Wsc e_d
+        df_mul(sm.sh[N + cur], sm.sl[N + cur], wh, wl, rh, rl);                 // S_d w(x)
+        df_sub(rh, rl, lh, ll, dh, dl);
+        ok = dh > 0.f;
+      }
+      sm.accept = ok;
+    }
+    __syncthreads();
+    const bool accepted = sm.accept != 0;
+    __syncthreads();
+    if (accepted) {
+      if (tid == 0) {
+        out_tok[depth] = sm.tok[c];
+        if (out_node) out_node[depth] = c;
+      }
+      ++depth;
+      cur = c;
+      c = cur + 1;
+      rho_h = rho_l = 0.f;
+      W_h = sm.sh[cur];
+      W_l = sm.sl[cur];
+      ready = false;
+      continue;
+    }
+    // rejected: rho' = rho + Wsc / S_d, Wsc' = sum_v max(0, e_z - rho' e_d)
+    float ih, il, qh, ql, nh, nl;
+    df_recip(sm.sh[N + cur], sm.sl[N + cur], ih, il);
+    df_mul(W_h, W_l, ih, il, qh, ql);
+    nh = rho_h;
+    nl = rho_l;
+    df_acc(nh, nl, qh, ql);
+    float a2, c2p;
+    int l2;
+    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, nh, nl, sm.tab, a2, c2p, l2);
+    float sh2, sl2, Th, Tl;
+    two_sum(a2, c2p, sh2, sl2);
+    tree_sum_df(sh2, sl2, sm, Th, Tl);
+    if (Th > 0.f) {
+      rho_h = nh;
+      rho_l = nl;
+      W_h = Th;
+      W_l = Tl;
+      acc = a2;
+      comp = c2p;
+      last = l2;
+      ready = true;
+    }  // else: an all-zero residual leaves r unchanged
+    ++c;
+  }
+  // the final token: inverse CDF of the weights max(0, e_z - rho e_d)
+  const Elem* zr = Zb + static_cast<int64_t>(cur) * V;
+  const Elem* dr = Db + static_cast<int64_t>(cur) * V;
+  const float mz = sm.m[cur], md = sm.m[N + cur];
+  if (!ready) {
+    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, rho_h, rho_l, sm.tab, acc, comp, last);
+    float sh2, sl2;
+    two_sum(acc, comp, sh2, sl2);
+    tree_sum_df(sh2, sl2, sm, W_h, W_l);
+  }
+  // per-thread sums in units of 2^-48 of the total
+  float rwh, rwl, fh, fl;
+  df_recip(W_h, W_l, rwh, rwl);
+  {
+    float h, l;
+    two_sum(acc, comp, h, l);
+    df_mul(h, l, rwh, rwl, fh, fl);
+  }
+  const long long mine = df_to_fix(fh, fl, kFix);
+  long long total;
+  const long long incl = tree_scan_i64(mine, sm.scan, &total);
+  const float u = p.u_smp[b];
+  const long long target = __float2ll_rd(__fmul_rn(u, kFix));
+  if (tid == 0) {
+    sm.sel = kTreeThreads;
+    sm.last = -1;
+  }
+  __syncthreads();
+  if (incl > target && incl - mine <= target) atomicMin(&sm.sel, tid);
+  if (last >= 0) atomicMax(&sm.last, last);
+  __syncthreads();
+  const int owner = sm.sel;
+  if (tid == owner) {  // walk this thread's range in the same order as the pass
+    long long cum = incl - mine;
+    int tok = last;
+    for (int v = lo; v < hi; ++v) {
+      float wh, wl;
+      const float d = rho_h != 0.f ? Tag::load1(dr + v) : 0.f;
+      if (tree_weight(Tag::load1(zr + v), d, mz, md, c2, rho_h, rho_l, sm.tab, wh, wl)) {
+        float ph, pl;
+        df_mul(wh, wl, rwh, rwl, ph, pl);
+        cum += df_to_fix(ph, pl, kFix);
+        if (cum > target) {
+          tok = v;
+          break;
+        }
+      }
+    }
+    out_tok[depth] = tok;
+    p.accept_len[b] = depth;
+  }
+  if (owner == kTreeThreads && tid == 0) {  // rounding left no crossing: the last positive weight
+    out_tok[depth] = sm.last;
+    p.accept_len[b] = depth;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tree_walk(const TreeParams& p, int dtype, bool vec, cudaStream_t s) {
+  if (p.B <= 0) return cudaSuccess;
+  if (dtype == 1) {
+    if (vec) tree_walk_kernel<BF16Tag, true><<<p.B, kTreeThreads, 0, s>>>(p);
+    else tree_walk_kernel<BF16Tag, false><<<p.B, kTreeThreads, 0, s>>>(p);
+  } else {
+    if (vec) tree_walk_kernel<F32Tag, true><<<p.B, kTreeThreads, 0, s>>>(p);
+    else tree_walk_kernel<F32Tag, false><<<p.B, kTreeThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

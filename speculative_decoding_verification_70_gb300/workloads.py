@@ -175,6 +175,112 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
             "u_smp": u_smp.contiguous()}
 
 
+# ---------------------------------------------------------------------------
+# token trees (tree decoding: "tanishqkumar/ssd" summary, module notes)
+# ---------------------------------------------------------------------------
+def tree_parents(widths) -> np.ndarray:
+    """Parents of a level-ordered tree in which every node of level l has
+    widths[l] children (node 0 the root): e.g. (4, 2, 1) gives 1 + 4 + 8 + 8
+    = 21 nodes."""
+    par = [-1]
+    level = [0]
+    for w in widths:
+        nxt = []
+        for u in level:
+            for _ in range(w):
+                par.append(u)
+                nxt.append(len(par) - 1)
+        level = nxt
+    return np.asarray(par, dtype=np.int32)
+
+
+def random_tree_parents(B: int, N: int, seed: int) -> np.ndarray:
+    """[B, N] parents of random recursive trees (node j hangs below a
+    uniformly drawn earlier node)."""
+    rng = np.random.default_rng(seed)
+    par = np.full((B, N), -1, dtype=np.int32)
+    for j in range(1, N):
+        par[:, j] = rng.integers(0, j, size=B)
+    return par
+
+
+# The tree benchmark workload: Qwen3-sized vocabulary, bf16, 64 batch rows,
+# trees of widths (4, 2, 1) = 21 nodes, per-row draft noise as qwen_b64.
+TREE_B64 = dict(B=64, widths=(4, 2, 1), V=151936, dtype="bf16", z_std=3.0, d_std=-1.0,
+                peaks=5, peak_boost=8.0, temp="0.7")
+
+
+def make_tree_inputs(B: int, parent, V: int, dtype: str = "f32", temp="1.0",
+                     z_std: float = 3.0, d_std: float = 1.0, peaks: int = 5,
+                     peak_boost: float = 8.0, seed: int = 4242, device="cpu",
+                     b_block: int = 16) -> Dict[str, torch.Tensor]:
+    """Draw one batch of token trees.
+
+    parent: [N] (the same tree in every batch row) or [B, N] int32.
+    Z [B,N,V] ~ N(0, z_std) plus `peaks` logits raised by `peak_boost` at
+    uniform indices; D = Z + N(0, d_std) (d_std < 0: per-row std drawn from
+    {0.3, 1, 3}).  temp: a number, "mixed" or "stochastic" (as the chain
+    workloads).  Node j's token is drawn from softmax(D[parent[j]] / T) by
+    Gumbel-max (so that siblings are independent draws from the parent's
+    q); on T == 0 rows from softmax(D[parent[j]]) with the first child of
+    every node forced to the draft argmax.  u_acc [B,N], u_smp [B] uniform.
+    """
+    device = torch.device(device)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    par = np.asarray(parent, dtype=np.int32)
+    if par.ndim == 1:
+        par = np.broadcast_to(par, (B, par.shape[0]))
+    par = np.array(par, dtype=np.int32, copy=True)
+    N = par.shape[1]
+    rng = np.random.default_rng(seed)
+    pk_idx = torch.from_numpy(rng.integers(0, V, size=(B * N, max(peaks, 1)))).to(device)
+    sig = (rng.choice(np.array([0.3, 1.0, 3.0]), size=B) if d_std < 0
+           else np.full(B, d_std)).astype(np.float32)
+    w = Workload("tree", B, 1, 0, V, dtype, z_std, d_std, peaks, peak_boost, "uniform",
+                 str(temp), False)
+    T = temperatures(w, seed, str(temp)).to(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    Z = torch.empty((B, N, V), dtype=dt, device=device)
+    D = torch.empty((B, N, V), dtype=dt, device=device)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=device)
+    par_t = torch.from_numpy(par.astype(np.int64)).to(device)
+    sig_t = torch.from_numpy(sig).to(device)
+    first = np.zeros((B, N), dtype=bool)
+    for j in range(1, N):
+        first[:, j] = ~(par[:, 1:j] == par[:, j:j + 1]).any(axis=1)
+    first_t = torch.from_numpy(first).to(device)
+    for b0 in range(0, B, b_block):
+        b1 = min(B, b0 + b_block)
+        nb = b1 - b0
+        z = torch.randn((nb, N, V), generator=gen, device=device) * z_std
+        if peaks:
+            pk = pk_idx[b0 * N:b1 * N].view(nb, N, -1)
+            z.scatter_add_(2, pk, torch.full(pk.shape, peak_boost, device=device))
+        zq = z.to(dt)
+        Z[b0:b1] = zq
+        d = zq.float() + torch.randn((nb, N, V), generator=gen, device=device) * \
+            sig_t[b0:b1].view(nb, 1, 1)
+        dq = d.to(dt)
+        D[b0:b1] = dq
+        # each node's token from its parent's draft row
+        pd = torch.gather(dq.float(), 1, par_t[b0:b1].clamp_min(0)[:, :, None].expand(nb, N, V))
+        tb = T[b0:b1].view(nb, 1, 1)
+        u = torch.rand((nb, N, V), generator=gen, device=device)
+        g = -torch.log(-torch.log(u.clamp_min(1e-38)))
+        score = pd / torch.where(tb > 0, tb, torch.ones_like(tb)) + g
+        t = torch.argmax(score, dim=2)
+        am = torch.argmax(pd, dim=2)
+        t = torch.where((tb.view(nb, 1) == 0) & first_t[b0:b1], am, t)
+        tok[b0:b1] = t.to(torch.int32)
+        del z, zq, d, dq, pd, u, g, score
+    tok[:, 0] = 0
+    u_acc = torch.rand((B, N), generator=gen, device=device)
+    u_smp = torch.rand((B,), generator=gen, device=device)
+    return {"Z": Z, "D": D, "parent": torch.from_numpy(par).to(device), "tok": tok,
+            "T": T.contiguous(), "u_acc": u_acc.contiguous(), "u_smp": u_smp.contiguous()}
+
+
 def cache_workload(fork_tok: torch.Tensor, depth: int, V: int, n_queries: int,
                    seed: int) -> Dict[str, torch.Tensor]:
     """Speculation-cache traffic for the SSD workload: one entry per forked

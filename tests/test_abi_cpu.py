@@ -206,3 +206,37 @@ def test_next_rows_reject_bad_arguments_on_host(lib):
     # fan-out: F as f
     assert lib.ssd_forked_recovery_fanout(P, 8 * 40, 0, 1, 2, 40, 17, P, None, 0, P, P, P, big,
                                           None) == INVALID
+
+
+def test_tree_rejects_bad_arguments_on_host(lib):
+    """ssd_verify_tree refuses bad arguments before touching CUDA."""
+    INVALID, DTYPE, WS = 1, 2, 6
+    P = 1 << 20
+    big = 1 << 30
+    # ssd_verify_tree(Z, zb, D, db, dt, B, N, V, parent, tok, T, u_acc, u_smp, acc, out_tok,
+    #                 out_node, ws, ws_bytes, stream)
+    ok = dict(Z=P, zb=5 * 1000, D=P, db=5 * 1000, dt=0, B=2, N=5, V=1000, par=P, tok=P, T=P,
+              ua=P, us=P, acc=P, out=P, node=None, ws=P, wsb=big)
+
+    def tree(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.ssd_verify_tree(a["Z"], a["zb"], a["D"], a["db"], a["dt"], a["B"], a["N"],
+                                   a["V"], a["par"], a["tok"], a["T"], a["ua"], a["us"],
+                                   a["acc"], a["out"], a["node"], a["ws"], a["wsb"], None)
+    assert tree(dt=7) == DTYPE
+    for key in ("Z", "D", "par", "tok", "T", "ua", "us", "acc", "out", "ws"):
+        assert tree(**{key: None}) == INVALID, key
+    assert tree(N=0) == INVALID
+    assert tree(N=65, zb=65 * 1000, db=65 * 1000) == INVALID   # at most 64 nodes
+    assert tree(V=1) == INVALID
+    assert tree(zb=4 * 1000) == INVALID                        # stride below N * V
+    assert tree(db=4 * 1000) == INVALID
+    assert tree(Z=P + 2) == INVALID                            # misaligned
+    assert tree(ws=P + 16) == INVALID
+    assert tree(wsb=16) == WS
+    assert lib.ssd_tree_workspace_bytes(2, 65, 1000) == 0
+    assert lib.ssd_tree_workspace_bytes(2, 0, 1000) == 0
+    n = lib.ssd_tree_workspace_bytes(2, 5, 1000)
+    assert n > 0 and n % 256 == 0
+    assert lib.ssd_tree_workspace_bytes(4, 5, 1000) > n
