@@ -21,13 +21,19 @@
 // The acceptance test u < r_j(x)/q(x) becomes u Wsc_j e_d(x) < S_d w(x), and
 // each rejection costs one pass over the node's two rows for the next Wsc.
 //
-// Layout of the work: one CTA of kTreeThreads per batch row.  Every thread
-// owns a contiguous range of E elements of a row (so that the draw's
-// inverse CDF is a block scan of per-thread sums followed by a walk of one
-// range); the decisions are taken by thread 0 and broadcast through shared
-// memory; passes use all threads, with double-float element weights and
-// compensated sums, and the draw converts the per-thread sums to exact
-// 2^-48 fixed point for an order-independent scan.
+// Layout of the work: one thread-block cluster of cs CTAs (1..8, chosen so
+// that the grid fills the GPU) per batch row.  Every CTA merges the row
+// statistics and takes the walk's decisions itself (thread 0, the same
+// deterministic arithmetic on the same data in every CTA, so the cluster's
+// control flow stays uniform); a pass splits the row's elements over the
+// cluster's threads, each owning a contiguous range of E elements (so that
+// the draw's inverse CDF is a scan of per-thread sums followed by a walk of
+// one range).  Pass totals are exchanged through distributed shared memory
+// (each CTA publishes its sum, a cluster barrier, every CTA adds the cs
+// sums in rank order).  Element weights are double-float with compensated
+// sums; the draw converts the per-thread sums to exact 2^-48 fixed point
+// for an order-independent scan.  Rank 0 writes the outputs.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "ssd_device.cuh"
@@ -42,9 +48,15 @@ constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr float kFix = 281474976710656.0f;  // 2^48
 
+namespace cg = cooperative_groups;
+
 struct TreeSmem {
   float2 tab[64];
   float2 c2;
+  float2 slot[2];                            // this CTA's pass sum (by pass parity)
+  long long ctot;                            // this CTA's fixed-point total (the draw)
+  int clast;                                 // this CTA's last positive index
+  int res;                                   // rank 0: the drawn token (-1: none)
   int par[kMaxTreeNodes], tok[kMaxTreeNodes];
   float m[2 * kMaxTreeNodes];                // row maxima: target rows, then draft rows
   float sh[2 * kMaxTreeNodes], sl[2 * kMaxTreeNodes];  // row sums (float pairs)
@@ -53,7 +65,6 @@ struct TreeSmem {
   float rh[kTreeWarps], rl[kTreeWarps];      // block sums
   long long scan[kTreeWarps];
   int accept;                                // thread 0's decision
-  int sel, last;                             // the draw
 };
 
 // Block-wide inclusive scan of int64 (exact).  *total gets the block total.
@@ -159,12 +170,32 @@ __device__ __forceinline__ void tree_pass(const typename Tag::Elem* zr,
   }
 }
 
+// Cluster total of the CTAs' sums (h, l): publish, cluster barrier, add the
+// cs sums in rank order (every CTA gets the same total).  Slots alternate by
+// pass parity, so a slot is rewritten only after the next barrier.
+__device__ __forceinline__ void cluster_total(cg::cluster_group& cl, TreeSmem& sm, int& parity,
+                                              float h, float l, float& th, float& tl) {
+  if (threadIdx.x == 0) sm.slot[parity] = make_float2(h, l);
+  cl.sync();
+  th = 0.f;
+  tl = 0.f;
+  const int cs = static_cast<int>(cl.num_blocks());
+  for (int r = 0; r < cs; ++r) {
+    const float2 v = *cl.map_shared_rank(&sm.slot[parity], r);
+    df_acc(th, tl, v.x, v.y);
+  }
+  parity ^= 1;
+}
+
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   using Elem = typename Tag::Elem;
   __shared__ TreeSmem sm;
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = static_cast<int>(cl.num_blocks()), rank = static_cast<int>(cl.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x, N = p.N;
+  const int b = blockIdx.x / cs, N = p.N;
+  const bool lead = rank == 0 && tid == 0;   // writes the outputs
   load_exp2_table(sm.tab);
   if (tid < N) {
     sm.par[tid] = p.parent[static_cast<int64_t>(b) * N + tid];
@@ -173,6 +204,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   if (tid == 0) {
     sm.flags = 0;
     sm.bad = 0;
+    sm.res = -1;
   }
   const float T = p.T[b];
   const bool t_bad = !(T >= 0.f);  // NaN or negative
@@ -183,7 +215,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     const bool ok = tid == 0 ? pj == -1 : (pj >= 0 && pj < tid && tj >= 0 && tj < p.V);
     if (!ok) atomicOr(&sm.bad, 1);
   }
-  // merged statistics of the 2N rows (one warp per row)
+  // merged statistics of the 2N rows (one warp per row, in every CTA)
   const bool do_exp = !greedy && !t_bad;
   for (int r = warp; r < 2 * N; r += kTreeWarps) {
     RowStat rs;
@@ -200,20 +232,21 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   }
   int32_t* out_tok = p.out_tok + static_cast<int64_t>(b) * N;
   int32_t* out_node = p.out_node ? p.out_node + static_cast<int64_t>(b) * N : nullptr;
-  for (int i = tid; i < N; i += kTreeThreads) {
-    out_tok[i] = -1;
-    if (out_node) out_node[i] = -1;
-  }
+  if (rank == 0)
+    for (int i = tid; i < N; i += kTreeThreads) {
+      out_tok[i] = -1;
+      if (out_node) out_node[i] = -1;
+    }
   __syncthreads();
   if (t_bad || sm.bad || sm.flags) {  // sentinels, in the order of the oracle's checks
-    if (tid == 0) {
+    if (lead) {
       p.accept_len[b] = (!t_bad && sm.bad) ? -2 : -1;
       atomicOr(p.err, t_bad ? 0x1 : (sm.bad ? 0x4 : 0x2));
     }
-    return;
+    return;  // every CTA of the cluster leaves here (same data, same test)
   }
   if (greedy) {  // first child carrying the argmax, then the argmax
-    if (tid == 0) {
+    if (lead) {
       int cur = 0, depth = 0;
       for (;;) {
         const int a = sm.am[cur];
@@ -235,12 +268,14 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   }
 
   const int V = p.V;
-  int E = (V + kTreeThreads - 1) / kTreeThreads;
+  int E = (V + cs * kTreeThreads - 1) / (cs * kTreeThreads);
   E = (E + 7) / 8 * 8;
-  const int lo = min(V, tid * E), hi = min(V, lo + E);
+  const int g = rank * kTreeThreads + tid;
+  const int lo = static_cast<int>(min(static_cast<long long>(V), static_cast<long long>(g) * E));
+  const int hi = min(V, lo + E);
   const Elem* Zb = static_cast<const Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb;
   const Elem* Db = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db;
-  int cur = 0, depth = 0, c = 1;
+  int cur = 0, depth = 0, c = 1, parity = 0;
   float rho_h = 0.f, rho_l = 0.f;           // rho of the current residual
   float W_h = sm.sh[0], W_l = sm.sl[0];     // its scaled mass (S_z at a fresh node)
   bool ready = false;                       // acc/comp/last hold a pass for (rho, W)
@@ -276,7 +311,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     const bool accepted = sm.accept != 0;
     __syncthreads();
     if (accepted) {
-      if (tid == 0) {
+      if (lead) {
         out_tok[depth] = sm.tok[c];
         if (out_node) out_node[depth] = c;
       }
@@ -299,9 +334,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     float a2, c2p;
     int l2;
     tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, nh, nl, sm.tab, a2, c2p, l2);
-    float sh2, sl2, Th, Tl;
+    float sh2, sl2, Bh, Bl, Th, Tl;
     two_sum(a2, c2p, sh2, sl2);
-    tree_sum_df(sh2, sl2, sm, Th, Tl);
+    tree_sum_df(sh2, sl2, sm, Bh, Bl);
+    cluster_total(cl, sm, parity, Bh, Bl, Th, Tl);
     if (Th > 0.f) {
       rho_h = nh;
       rho_l = nl;
@@ -320,9 +356,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   const float mz = sm.m[cur], md = sm.m[N + cur];
   if (!ready) {
     tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, rho_h, rho_l, sm.tab, acc, comp, last);
-    float sh2, sl2;
+    float sh2, sl2, Bh, Bl;
     two_sum(acc, comp, sh2, sl2);
-    tree_sum_df(sh2, sl2, sm, W_h, W_l);
+    tree_sum_df(sh2, sl2, sm, Bh, Bl);
+    cluster_total(cl, sm, parity, Bh, Bl, W_h, W_l);
   }
   // per-thread sums in units of 2^-48 of the total
   float rwh, rwl, fh, fl;
@@ -333,23 +370,26 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     df_mul(h, l, rwh, rwl, fh, fl);
   }
   const long long mine = df_to_fix(fh, fl, kFix);
-  long long total;
-  const long long incl = tree_scan_i64(mine, sm.scan, &total);
+  long long cta_total;
+  const long long incl_cta = tree_scan_i64(mine, sm.scan, &cta_total);
+  if (tid == 0) sm.clast = -1;
+  __syncthreads();
+  if (last >= 0) atomicMax(&sm.clast, last);
+  if (tid == 0) sm.ctot = cta_total;
+  cl.sync();
+  long long before = 0;                     // the fixed-point totals of lower ranks
+  int clast = -1;
+  for (int r = 0; r < cs; ++r) {
+    if (r < rank) before += *cl.map_shared_rank(&sm.ctot, r);
+    clast = max(clast, *cl.map_shared_rank(&sm.clast, r));
+  }
+  const long long incl = before + incl_cta;
   const float u = p.u_smp[b];
   const long long target = __float2ll_rd(__fmul_rn(u, kFix));
-  if (tid == 0) {
-    sm.sel = kTreeThreads;
-    sm.last = -1;
-  }
-  __syncthreads();
-  if (incl > target && incl - mine <= target) atomicMin(&sm.sel, tid);
-  if (last >= 0) atomicMax(&sm.last, last);
-  __syncthreads();
-  const int owner = sm.sel;
-  if (tid == owner) {  // walk this thread's range in the same order as the pass
+  if (incl > target && incl - mine <= target) {  // one thread of the cluster
     long long cum = incl - mine;
     int tok = last;
-    for (int v = lo; v < hi; ++v) {
+    for (int v = lo; v < hi; ++v) {  // walk the range in the order of the pass
       float wh, wl;
       const float d = rho_h != 0.f ? Tag::load1(dr + v) : 0.f;
       if (tree_weight(Tag::load1(zr + v), d, mz, md, c2, rho_h, rho_l, sm.tab, wh, wl)) {
@@ -362,27 +402,58 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
         }
       }
     }
-    out_tok[depth] = tok;
-    p.accept_len[b] = depth;
+    *cl.map_shared_rank(&sm.res, 0) = tok;
   }
-  if (owner == kTreeThreads && tid == 0) {  // rounding left no crossing: the last positive weight
-    out_tok[depth] = sm.last;
+  cl.sync();  // the token is in rank 0's shared memory; no remote access follows
+  if (lead) {
+    out_tok[depth] = sm.res >= 0 ? sm.res : clast;  // rounding left no crossing: last positive
     p.accept_len[b] = depth;
   }
 }
 
 }  // namespace
 
+// Cluster size per batch row: enough CTAs to fill the GPU (about two
+// 512-thread CTAs per SM), at most SSD_TREE_MAX_CLUSTER.
+#ifndef SSD_TREE_MAX_CLUSTER
+#define SSD_TREE_MAX_CLUSTER 8
+#endif
+
+template <typename Tag, bool VEC>
+static cudaError_t launch_tree_t(const TreeParams& p, int cs, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B) * cs, 1, 1);
+  cfg.blockDim = dim3(kTreeThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tree_walk_kernel<Tag, VEC>, p);
+}
+
 cudaError_t launch_tree_walk(const TreeParams& p, int dtype, bool vec, cudaStream_t s) {
   if (p.B <= 0) return cudaSuccess;
-  if (dtype == 1) {
-    if (vec) tree_walk_kernel<BF16Tag, true><<<p.B, kTreeThreads, 0, s>>>(p);
-    else tree_walk_kernel<BF16Tag, false><<<p.B, kTreeThreads, 0, s>>>(p);
-  } else {
-    if (vec) tree_walk_kernel<F32Tag, true><<<p.B, kTreeThreads, 0, s>>>(p);
-    else tree_walk_kernel<F32Tag, false><<<p.B, kTreeThreads, 0, s>>>(p);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  int cs = 1;
+  while (cs < SSD_TREE_MAX_CLUSTER && static_cast<long long>(p.B) * cs * 2 <= 2LL * sms) cs *= 2;
+  for (;;) {
+    cudaError_t e;
+    if (dtype == 1)
+      e = vec ? launch_tree_t<BF16Tag, true>(p, cs, s) : launch_tree_t<BF16Tag, false>(p, cs, s);
+    else
+      e = vec ? launch_tree_t<F32Tag, true>(p, cs, s) : launch_tree_t<F32Tag, false>(p, cs, s);
+    if (e == cudaSuccess || cs == 1) return e;
+    (void)cudaGetLastError();  // a cluster this size cannot be placed: halve it
+    cs /= 2;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace ssd

@@ -228,9 +228,8 @@ def make_tree_inputs(B: int, parent, V: int, dtype: str = "f32", temp="1.0",
     device = torch.device(device)
     dt = torch.float32 if dtype == "f32" else torch.bfloat16
     par = np.asarray(parent, dtype=np.int32)
-    if par.ndim == 1:
-        par = np.broadcast_to(par, (B, par.shape[0]))
-    par = np.array(par, dtype=np.int32, copy=True)
+    par = np.repeat(par[None], B, axis=0) if par.ndim == 1 else par.copy()
+    par = np.ascontiguousarray(par, dtype=np.int32)
     N = par.shape[1]
     rng = np.random.default_rng(seed)
     pk_idx = torch.from_numpy(rng.integers(0, V, size=(B * N, max(peaks, 1)))).to(device)
