@@ -600,11 +600,27 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiling captures only; not the metric's workload)")
+    ap.add_argument("--tree-only", action="store_true",
+                    help="only the token-tree measurement (profiling captures; B from --batch)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
+    elif args.tree_only:
+        tree_only(args)
     else:
         gpu_arm(args)
+
+
+def tree_only(args):
+    """The tree measurement alone, for profiler captures (--batch overrides
+    the tree workload's B; --steps sets the timed calls)."""
+    import torch
+    import speculative_decoding_verification_70_gb300 as ssd
+    from speculative_decoding_verification_70_gb300 import workloads as W
+    if args.batch:
+        W.TREE_B64 = dict(W.TREE_B64, B=args.batch)
+    torch.cuda.set_device(0)
+    print(json.dumps(tree_verify(ssd, W, "cuda", reps=max(1, args.steps))), flush=True)
 
 
 if __name__ == "__main__":
