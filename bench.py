@@ -36,6 +36,7 @@ UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
 CACHE_DEPTH = 7
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stats_pass_mixed512.md")
+NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["speculative_decoding_verification_70_gb300/csrc/ssd_stats.cu",
                   "speculative_decoding_verification_70_gb300/csrc/ssd_scan.cuh",
                   "speculative_decoding_verification_70_gb300/csrc/ssd_device.cuh",
@@ -460,6 +461,9 @@ def gpu_arm(args):
                 "per_kernel_gbs": {k: round(row_bytes / (per_kernel[k] / 1e3) / 1e9, 1)
                                    for k in ("stats", "stats_topf") if k in per_kernel},
                 "step_algorithmic_gbs": round(nbytes / (ms_step / 1e3) / 1e9, 1),
+                # against the part's nominal HBM3e bandwidth as well (8 TB/s)
+                "nominal_gbs": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "ms_per_step_by_scope": {k: round(v, 5) for k, v in per_kernel.items()}}
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -472,7 +476,11 @@ def gpu_arm(args):
                        "global_batch": w.B * world, "per_gpu_batch": w.B,
                        "l2": "inputs (%.2f GB per step) larger than L2" % (nbytes / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "gpu_launches": launches, "roofline": roof, "clocks": clock, "e2e": e2e}
+            "gpu_launches": launches, "roofline": roof, "clocks": clock, "e2e": e2e,
+            # logit rows verified per second: the 2k+1 rows of acceptance and
+            # recovery per batch row
+            "logit_rows_per_s": round(value * (2 * w.k + 1), 1),
+            "us_per_step": round(ms_step * 1e3, 2)}
     if rank == 0 and world == 1:
         line["latency_b1"] = b1_latency(ssd, W, dev)
         line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)

@@ -122,3 +122,54 @@ def test_gpu_draft_sampler_law_on_a_million_rows(gpu_lib):
     assert scipy_stats.chisquare(np.bincount(x, minlength=V), p * N).pvalue > 1e-3
     ref = oracle.draft_sample(D, Tv, 0xABCDEF, 2)[:, 0]
     assert (ref != x).sum() <= 1e-4 * N
+
+
+def test_gpu_tree_law_on_a_million_rows(gpu_lib):
+    """Token-tree verification keeps the target law (multi-step speculative
+    sampling; tree decoding, "tanishqkumar/ssd" summary, module notes):
+    10^6 trees (root with three children drawn from the root's q, each with
+    two children drawn from that child's q), V = 5, one call.  The first two
+    tokens (completed from the target when one is produced) follow
+    p_root(t1) * p_t1(t2); every row equals the oracle's."""
+    rng = np.random.default_rng(91)
+    B, V, T = 1_000_000, 5, 1.0
+    Zr = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    Dr = (Zr + rng.standard_normal(V) * 1.5).astype(np.float32)
+    Zc = (rng.standard_normal((V, V)) * 1.5).astype(np.float32)
+    Dc = (Zc + rng.standard_normal((V, V)) * 1.5).astype(np.float32)
+    pr, qr = _softmax64(Zr[None], T)[0], _softmax64(Dr[None], T)[0]
+    pc, qc = _softmax64(Zc, T), _softmax64(Dc, T)
+    par = np.array([-1, 0, 0, 0, 1, 1, 2, 2, 3, 3], np.int32)
+    N = len(par)
+    tok = np.zeros((B, N), np.int32)
+    for j in range(1, 4):
+        tok[:, j] = _draw_from(qr, rng.random(B))
+    for j in range(4, N):
+        pt = tok[:, par[j]]
+        tok[:, j] = np.minimum((np.cumsum(qc[pt], axis=1) <= rng.random(B)[:, None]).sum(1), V - 1)
+    Z = np.empty((B, N, V), np.float32)
+    D = np.empty((B, N, V), np.float32)
+    Z[:, 0], D[:, 0] = Zr, Dr
+    Z[:, 1:], D[:, 1:] = Zc[tok[:, 1:]], Dc[tok[:, 1:]]
+    ua = rng.random((B, N)).astype(np.float32)
+    us = rng.random(B).astype(np.float32)
+    host = {"Z": torch.from_numpy(Z), "D": torch.from_numpy(D),
+            "parent": torch.from_numpy(np.repeat(par[None], B, axis=0)),
+            "tok": torch.from_numpy(tok), "T": torch.full((B,), T),
+            "u_acc": torch.from_numpy(ua), "u_smp": torch.from_numpy(us)}
+    dev = {k: v.cuda() for k, v in host.items()}
+    out = gpu_lib.ssd_verify_tree(dev["Z"], dev["D"], dev["parent"], dev["tok"], dev["T"],
+                                  dev["u_acc"], dev["u_smp"])
+    torch.cuda.synchronize()
+    assert gpu_lib.get_device_error(out["ws"]) == 0
+    n = out["accept_len"].cpu().numpy()
+    o = out["out_tok"].cpu().numpy()
+    assert (n >= 0).all() and (n >= 1).mean() > 0.3 and (n == 2).any()
+    t1 = o[:, 0].astype(np.int64)
+    t2 = np.where(n >= 1, o[:, 1],
+                  np.minimum((np.cumsum(pc[t1], axis=1) <= rng.random(B)[:, None]).sum(1), V - 1))
+    obs = np.bincount(t1 * V + t2, minlength=V * V)
+    assert scipy_stats.chisquare(obs, (pr[:, None] * pc).reshape(-1) * B).pvalue > 1e-3
+    ref = oracle.verify_tree(Z, D, host["parent"].numpy(), tok, host["T"].numpy(), ua, us)
+    diff = (ref["accept_len"] != n) | (ref["out_tok"] != o).any(axis=1)
+    assert diff.sum() <= 1e-4 * B, int(diff.sum())
