@@ -216,7 +216,8 @@ def verify_tree(Z, D, parent, tok, T, u_acc, u_smp, f64_uniforms: bool = False
     """Token-tree verification (multi-step speculative sampling over a tree
     whose children at a node were drawn from the draft's q there).
 
-    Z, D: [B, N, V] target and draft logits at the N nodes.  parent, tok:
+    Z, D: [B, N, V] target and draft logits at the N nodes (a leaf's draft
+    row is not read).  parent, tok:
     [B, N] int32 (parent[:, 0] == -1, parent[:, j] < j; tok[:, 0] unused).
     T: [B].  u_acc: [B, N] (entry j tests node j), u_smp: [B]: binary32 as
     the GPU library takes them, or double when f64_uniforms.

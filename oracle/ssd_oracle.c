@@ -60,9 +60,10 @@
  *      zero, as R5).  When the children are exhausted the final token is
  *      drawn from r by R4.  Greedy rows accept the first child whose token
  *      is the argmax of the current node's target row and end with that
- *      argmax.  All N target rows and all N draft rows are read (R7);
- *      parent[0] != -1, parent[j] outside [0, j) or a token outside [0, V)
- *      gives accept_len -2.
+ *      argmax.  All N target rows are read, and the draft rows of the
+ *      nodes that have children (a leaf's q is never used), with R7's
+ *      checks; parent[0] != -1, parent[j] outside [0, j) or a token outside
+ *      [0, V) gives accept_len -2.
  *   R8 draft-side sampling: the drafter's token at T > 0 is the Gumbel-max
  *      draw argmax_v (z_v / T + G_v), G_v = -ln(-ln u_v), which is exactly a
  *      draw from softmax(z / T); u_v comes from the counter-based generator
@@ -616,8 +617,14 @@ int oracle_verify_tree_f64(const void *Z, int64_t z_bstride, const void *D,
         for (int j = 0; j < N && rows_ok; ++j) {
             load_row(Z, dtype, (int64_t)b * z_bstride + (int64_t)j * V, V, zrow);
             rows_ok = row_is_valid(zrow, V, greedy);
-            load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)j * V, V, zrow);
-            rows_ok = rows_ok && row_is_valid(zrow, V, greedy);
+            int has_child = 0;
+            for (int c = j + 1; c < N; ++c)
+                if (par[c] == j)
+                    has_child = 1;
+            if (has_child && rows_ok) {
+                load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)j * V, V, zrow);
+                rows_ok = row_is_valid(zrow, V, greedy);
+            }
         }
         if (!rows_ok) {
             accept_len[b] = -1;

@@ -757,7 +757,8 @@ def test_tree_sentinels():
     par[1, 2] = 2                    # parent not before the node
     tok[2, 3] = V                    # token out of range
     par[3, 0] = 0                    # root with a parent
-    D[4, 3, 2] = np.nan              # NaN in a leaf's draft row (read too)
+    D[4, 1, 2] = np.nan              # NaN in the draft row of node 1 (it has a child)
+    D[5, 3, 2] = np.nan              # NaN in a leaf's draft row: never used, not read
     r = oracle.verify_tree(Z, D, par, tok, T, rng.random((B, N)), rng.random(B))
     assert list(r["accept_len"]) [:5] == [-1, -2, -2, -2, -1]
     assert r["accept_len"][5] >= 0
