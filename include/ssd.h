@@ -361,15 +361,17 @@ SSD_API ssd_status ssd_verify_topk(const void *Z, int64_t z_bstride, const void 
  *   total).  T == 0 rows accept the first child whose token is the argmax
  *   (lowest index) of the current node's target row and end with that
  *   argmax.
- * One streaming pass over all 2N rows gives each row's maximum, argmax and
- * sum; then one CTA per batch row walks the tree, with one pass over the
- * current node's two rows per rejection (the next residual mass) and one for
- * the final draw when it is not already known.
+ * One streaming pass over the N target rows and the inner nodes' draft rows
+ * gives each row's maximum, argmax and sum; then a thread-block cluster per
+ * batch row walks the tree, with one pass over the current node's two rows
+ * per rejection (the next residual mass) and one for the final draw when it
+ * is not already known.
  *   Z        : target logits at the nodes, row (b, j) at Z + b*z_bstride +
  *              j*V (the target's logits after node j's path; node 0 is the
  *              last committed position).  z_bstride >= N*V.
  *   D        : draft logits at the nodes, same layout (q of node j's
- *              children).  All N rows are read and checked, leaves included.
+ *              children).  Only the rows of nodes that have children are
+ *              read and checked: a leaf's q is never used.
  *   N        : nodes per tree, 1 <= N <= SSD_MAX_TREE_NODES.
  *   parent   : [B, N] int32 device: parent[b, 0] == -1, 0 <= parent[b, j] < j.
  *   tok      : [B, N] int32 device: node j's token (entry 0 unused).

@@ -465,8 +465,9 @@ def ssd_verify_tree(Z: torch.Tensor, D: torch.Tensor, parent: torch.Tensor,
                     out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
     """Verify a draft token tree per batch row (multi-step speculative
     sampling; greedy at T == 0).  Z, D: [B, N, V] target and draft logits at
-    the N nodes; parent, tok: [B, N] int32 (parent[:, 0] == -1, parent[:, j]
-    < j); u_acc: [B, N] float32 (entry j tests node j), u_smp: [B].
+    the N nodes (a leaf's draft row is not read); parent, tok: [B, N] int32
+    (parent[:, 0] == -1, parent[:, j] < j); u_acc: [B, N] float32 (entry j
+    tests node j), u_smp: [B].
 
     Returns accept_len [B], out_tok [B, N] (accepted tokens, the final
     token, then -1) and out_node [B, N] (accepted node ids, then -1)."""

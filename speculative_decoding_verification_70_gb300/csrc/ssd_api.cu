@@ -652,7 +652,9 @@ ssd_status ssd_verify_tree(const void* Z, int64_t z_bstride, const void* D, int6
   sp.T = T; sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = L.R; sp.Rp = L.R;
   sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
   sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
-  cudaError_t e = run_stats(sp, B, dt, vec, S(stream));  // all 2N rows, one launch
+  sp.tree_parent = parent;  // leaves' draft rows are skipped
+  sp.tree_N = N;
+  cudaError_t e = run_stats(sp, B, dt, vec, S(stream));  // the 2N rows, one launch
   if (e != cudaSuccess) return SSD_ERR_CUDA;
   TreeParams tp;
   memset(&tp, 0, sizeof tp);

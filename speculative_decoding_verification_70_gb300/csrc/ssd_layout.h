@@ -88,6 +88,9 @@ struct StatsParams {
   GumbelPart* gpart;   // [B][Pf][C]
   uint32_t seed_lo, seed_hi, offset;
   int Pf;              // row pitch of gpart[] and topk[] (k + 1)
+  // token trees: draft row j is read only if node j has a child (null: all)
+  const int32_t* tree_parent;  // [B][tree_N]
+  int tree_N;
 };
 
 struct FinalizeParams {

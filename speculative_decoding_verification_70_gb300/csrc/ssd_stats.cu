@@ -438,6 +438,12 @@ __global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : 6)
     need_stats = j < p.Pds;
     need_top = HAS_TOPF && j < p.Pdf;
     if (!need_stats && !need_top) return;
+    if (p.tree_parent) {  // a tree leaf's draft row is never used: not read
+      const int t = threadIdx.x;
+      const bool kid = t > j && t < p.tree_N &&
+                       p.tree_parent[static_cast<int64_t>(b) * p.tree_N + t] == j;
+      if (!__syncthreads_or(kid)) return;
+    }
   }
   float T = p.T ? p.T[b] : 0.f;
   bool do_exp = need_stats && (T > 0.f);  // uniform over the CTA

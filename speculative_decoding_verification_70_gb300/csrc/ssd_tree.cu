@@ -215,9 +215,24 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     const bool ok = tid == 0 ? pj == -1 : (pj >= 0 && pj < tid && tj >= 0 && tj < p.V);
     if (!ok) atomicOr(&sm.bad, 1);
   }
-  // merged statistics of the 2N rows (one warp per row, in every CTA)
+  // merged statistics of the N target rows and of the draft rows of nodes
+  // with children (one warp per row, in every CTA); a leaf's draft row was
+  // not read
   const bool do_exp = !greedy && !t_bad;
   for (int r = warp; r < 2 * N; r += kTreeWarps) {
+    if (r >= N) {
+      bool kid = false;
+      for (int c = r - N + 1 + lane; c < N; c += 32) kid |= sm.par[c] == r - N;
+      if (!__any_sync(kFull, kid)) {
+        if (lane == 0) {
+          sm.m[r] = -INFINITY;
+          sm.am[r] = kIdxNone;
+          sm.sh[r] = 0.f;
+          sm.sl[r] = 0.f;
+        }
+        continue;
+      }
+    }
     RowStat rs;
     float h, l;
     merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c2.x, c2.y, do_exp,

@@ -151,15 +151,16 @@ def test_tree_deep_chain_and_many_siblings(gpu_lib):
 
 
 def test_tree_edges(gpu_lib):
-    """Sentinels (invalid T, NaN in a leaf's draft row, bad parent, token out
-    of range), children with q(x) = 0, duplicate sibling tokens and greedy
-    rows with ties."""
+    """Sentinels (invalid T, NaN in a draft row with children, bad parent,
+    token out of range), a NaN in a leaf's draft row (not read), children
+    with q(x) = 0, duplicate sibling tokens and greedy rows with ties."""
     B, V = 12, 40
     par = W.tree_parents((3, 2))
     inp = W.make_tree_inputs(B, par, V, temp="mixed", seed=31, peaks=0)
     Z, D = inp["Z"], inp["D"]
     inp["T"][0] = -1.0
-    D[1, 7, 3] = float("nan")                        # node 7 is a leaf
+    D[1, 1, 3] = float("nan")                        # node 1 has children
+    D[7, 7, 3] = float("nan")                        # node 7 is a leaf: not read
     inp["parent"][2, 5] = 5                          # parent not before the node
     inp["tok"][3, 4] = V                             # token out of range
     inp["T"][4] = 0.9
@@ -172,6 +173,7 @@ def test_tree_edges(gpu_lib):
     out = _run(gpu_lib, inp)
     ref, _ = _compare(inp, out)
     assert list(ref["accept_len"][:4]) == [-1, -1, -2, -2]
+    assert ref["accept_len"][7] >= 0
     assert ref["accept_len"][6] >= 1 and to_np(out["out_node"])[6, 0] == 1
     gpu_lib.get_device_error(out["ws"], clear=True)
 
