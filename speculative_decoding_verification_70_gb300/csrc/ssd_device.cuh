@@ -105,6 +105,18 @@ __device__ __forceinline__ float ex2_fast(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor in the stream has
+// finished; pdl_wait() blocks until the predecessor has completed and its
+// memory is visible (a no-op for an ordinary launch).  pdl_trigger() lets
+// the successor's launch begin once every CTA of this grid has called it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Error-free transformations (Knuth's TwoSum, FMA-based TwoProduct).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {

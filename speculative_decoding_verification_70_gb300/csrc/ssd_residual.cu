@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
+  pdl_trigger();  // the mass kernel may be scheduled (it waits for this grid)
   const int c = blockIdx.x, b = blockIdx.y + p.b0;
   BState bs;
   RowCtx cx;
@@ -252,6 +253,8 @@ __global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams 
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ RowCtx s_cx;
+  pdl_wait();     // the norm kernel has completed
+  pdl_trigger();  // the select kernel may be scheduled
   const int c = blockIdx.x;
   load_exp2_table(tab);
   for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
@@ -362,6 +365,7 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
 // floor(u * W).  Only the two normaliser inverses are taken by one thread.
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParams p) {
+  pdl_wait();  // the mass kernel has completed
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
   __shared__ long long s_amb[kThreads];  // per-chunk exact mass of the ambiguous elements (2^60)
@@ -538,19 +542,44 @@ cudaError_t launch_residual_norm(const ResidualParams& p0, int B, int dtype, boo
   }
   return cudaSuccess;
 }
+#undef SSD_DISPATCH
+
+
+// The mass and select kernels follow the norm and mass kernels on the same
+// stream with programmatic stream serialization: their launch overlaps the
+// predecessor's tail and each waits (griddepcontrol.wait) before touching
+// memory.
+template <typename Kernel>
+static cudaError_t launch_after(Kernel kernel, dim3 grid, cudaStream_t s, const ResidualParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+#define SSD_DISPATCH_AFTER(KERNEL, GRID)                                              \
+  (dtype == 1 ? (vec ? launch_after(KERNEL<BF16Tag, true>, GRID, s, p)                \
+                     : launch_after(KERNEL<BF16Tag, false>, GRID, s, p))              \
+              : (vec ? launch_after(KERNEL<F32Tag, true>, GRID, s, p)                 \
+                     : launch_after(KERNEL<F32Tag, false>, GRID, s, p)))
 
 cudaError_t launch_residual_mass(const ResidualParams& p0, int B, int dtype, bool vec, cudaStream_t s) {
   ResidualParams p = p0;
   p.B = B;
-  SSD_DISPATCH(residual_mass_kernel, dim3(p.C, B < kMassRowSlots ? B : kMassRowSlots));
-  return cudaGetLastError();
+  return SSD_DISPATCH_AFTER(residual_mass_kernel, dim3(p.C, B < kMassRowSlots ? B : kMassRowSlots));
 }
 
 cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
-  SSD_DISPATCH(residual_select_kernel, dim3(B));
-  return cudaGetLastError();
+  return SSD_DISPATCH_AFTER(residual_select_kernel, dim3(B));
 }
-#undef SSD_DISPATCH
+#undef SSD_DISPATCH_AFTER
 
 cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s) {
   residual_prep_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);
