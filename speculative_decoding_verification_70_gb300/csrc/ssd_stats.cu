@@ -709,13 +709,16 @@ __device__ __forceinline__ float logit_at(const void* base, int dtype, int64_t i
 }
 
 // grid: B.  Verification (and, when fork_tok != null, the forked top-f).
-__global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
+// NW warps per CTA: 8 for large batches; 16 at small B, where the CTA's
+// row merges are the critical path (one round for 2(k+1) <= 16 rows).
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) finalize_kernel(FinalizeParams p) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float2 tab[64];
   __shared__ RowStat rs[2 * (32 + 1)];
   __shared__ float2 rsum[2 * (32 + 1)];  // each row's S as a float pair
-  __shared__ int heads[kWarps][256];
+  __shared__ int heads[NW][256];
   load_exp2_table(tab);
   __syncthreads();
 
@@ -732,7 +735,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(FinalizeParams p) {
 
   // 1. merge the row statistics
   const int nstat = p.Pz + p.Pds;
-  for (int r = warp; r < p.R; r += kWarps) {
+  for (int r = warp; r < p.R; r += NW) {
     bool is_target = r < p.Pz;
     int j = r - p.Pz;
     bool need_stats = is_target || j < p.Pds;
@@ -978,7 +981,8 @@ cudaError_t launch_draft_finalize(const DraftParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_finalize(const FinalizeParams& p, cudaStream_t s) {
-  finalize_kernel<<<p.B, kThreads, 0, s>>>(p);
+  if (p.B <= 152) finalize_kernel<16><<<p.B, 16 * 32, 0, s>>>(p);
+  else finalize_kernel<kWarps><<<p.B, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
