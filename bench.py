@@ -308,7 +308,8 @@ def topk_verify(ssd, w, inp, dev, K=32, top_p=0.9, reps=50):
 def tree_verify(ssd, W, dev, reps=20):
     """Token-tree verification on the tree workload (64 batch rows, trees of
     widths (4, 2, 1) = 21 nodes, V = 151936, bf16, T = 0.7): milliseconds per
-    call, the statistics pass's GB/s over the 2N rows and the walk's time."""
+    call, the statistics pass's GB/s over the rows it reads (the N target rows
+    and the draft rows of nodes with children) and the walk's time."""
     import torch
     cfg = W.TREE_B64
     par = W.tree_parents(cfg["widths"])
@@ -339,9 +340,12 @@ def tree_verify(ssd, W, dev, reps=20):
     torch.cuda.synchronize()
     prof = ssd.profile_end()
     per = {k: v["total_ms"] / max(1, v["timed"]) for k, v in prof.items()}
-    nbytes = B * 2 * N * V * inp["Z"].element_size()
+    # rows read: the N target rows and the draft rows of nodes with children
+    inner = len(set(int(j) for j in par[1:]))
+    nbytes = B * (N + inner) * V * inp["Z"].element_size()
     acc = out["accept_len"].float().mean().item()
     res = {"workload": "B=%d N=%d (widths %s) V=%d bf16 T=0.7" % (B, N, cfg["widths"], V),
+           "rows_read_per_tree": N + inner,
            "ms": round(ms, 4), "rows_per_s": round(B / (ms / 1e3), 1),
            "mean_accepted": round(acc, 3)}
     if "stats" in per:
@@ -608,27 +612,40 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiling captures only; not the metric's workload)")
-    ap.add_argument("--tree-only", action="store_true",
-                    help="only the token-tree measurement (profiling captures; B from --batch)")
+    ap.add_argument("--only", choices=["tree", "topk", "draft"], default=None,
+                    help="one of the next rows' measurements alone (profiling captures; "
+                         "B from --batch, timed calls from --steps)")
+    ap.add_argument("--topk-k", type=int, default=32, help="K of --only topk")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
-    elif args.tree_only:
-        tree_only(args)
+    elif args.only:
+        only_arm(args)
     else:
         gpu_arm(args)
 
 
-def tree_only(args):
-    """The tree measurement alone, for profiler captures (--batch overrides
-    the tree workload's B; --steps sets the timed calls)."""
+def only_arm(args):
+    """One of the next rows' measurements alone, for profiler captures:
+    tree (the tree workload), topk or draft (the benchmark workload); --batch
+    overrides B, --steps sets the timed calls."""
     import torch
     import speculative_decoding_verification_70_gb300 as ssd
     from speculative_decoding_verification_70_gb300 import workloads as W
-    if args.batch:
-        W.TREE_B64 = dict(W.TREE_B64, B=args.batch)
     torch.cuda.set_device(0)
-    print(json.dumps(tree_verify(ssd, W, "cuda", reps=max(1, args.steps))), flush=True)
+    reps = max(1, args.steps)
+    if args.only == "tree":
+        if args.batch:
+            W.TREE_B64 = dict(W.TREE_B64, B=args.batch)
+        res = tree_verify(ssd, W, "cuda", reps=reps)
+    else:
+        w = W.workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
+        inp = W.make_inputs(w, device="cuda", seed=W.default_seed(WORKLOAD))
+        if args.only == "topk":
+            res = topk_verify(ssd, w, inp, "cuda", K=args.topk_k, reps=reps)
+        else:
+            res = draft_pipeline(ssd, w, inp, "cuda", reps=reps)
+    print(json.dumps(res), flush=True)
 
 
 if __name__ == "__main__":
