@@ -65,6 +65,8 @@ struct TreeSmem {
   float rh[kTreeWarps], rl[kTreeWarps];      // block sums
   long long scan[kTreeWarps];
   int accept;                                // thread 0's decision
+  float2 ez[kMaxTreeNodes], ed[kMaxTreeNodes];  // node j's e_z, e_d at its parent's rows
+  float u[kMaxTreeNodes];                    // node j's acceptance uniform
 };
 
 // Block-wide inclusive scan of int64 (exact).  *total gets the block total.
@@ -282,6 +284,26 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     return;
   }
 
+  // every child's e_z(x) and e_d(x) at its parent's rows, gathered in
+  // parallel (one thread per node) so that each decision is a few
+  // double-float operations of thread 0
+  if (tid > 0 && tid < N) {
+    const int pj = sm.par[tid], x = sm.tok[tid];
+    const Elem* zr = static_cast<const Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb +
+                     static_cast<int64_t>(pj) * p.V;
+    const Elem* dr = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db +
+                     static_cast<int64_t>(pj) * p.V;
+    float xh, xl, h, l;
+    arg_df(Tag::load1(zr + x), sm.m[pj], c2.x, c2.y, xh, xl);
+    exp2_df(xh, xl, sm.tab, h, l);
+    sm.ez[tid] = make_float2(h, l);
+    arg_df(Tag::load1(dr + x), sm.m[N + pj], c2.x, c2.y, xh, xl);
+    exp2_df(xh, xl, sm.tab, h, l);
+    sm.ed[tid] = make_float2(h, l);
+    sm.u[tid] = p.u_acc[static_cast<int64_t>(b) * N + tid];
+  }
+  __syncthreads();
+
   const int V = p.V;
   int E = (V + cs * kTreeThreads - 1) / (cs * kTreeThreads);
   E = (E + 7) / 8 * 8;
@@ -303,19 +325,14 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     const Elem* dr = Db + static_cast<int64_t>(cur) * V;
     const float mz = sm.m[cur], md = sm.m[N + cur];
     if (tid == 0) {
-      const int x = sm.tok[c];
-      float xh, xl, ezh, ezl, edh, edl;
-      arg_df(Tag::load1(zr + x), mz, c2.x, c2.y, xh, xl);
-      exp2_df(xh, xl, sm.tab, ezh, ezl);
-      arg_df(Tag::load1(dr + x), md, c2.x, c2.y, xh, xl);
-      exp2_df(xh, xl, sm.tab, edh, edl);
+      const float ezh = sm.ez[c].x, ezl = sm.ez[c].y, edh = sm.ed[c].x, edl = sm.ed[c].y;
       float wh, wl, th, tl, lh, ll, rh, rl, dh, dl;
       df_mul(rho_h, rho_l, edh, edl, th, tl);
       df_sub(ezh, ezl, th, tl, wh, wl);          // w(x) = e_z - rho e_d
       int ok = 0;
       if (wh > 0.f) {
         df_mul(W_h, W_l, edh, edl, th, tl);
-        df_mul(p.u_acc[static_cast<int64_t>(b) * N + c], 0.f, th, tl, lh, ll);  // u Wsc e_d
+        df_mul(sm.u[c], 0.f, th, tl, lh, ll);                                   // u Wsc e_d
         df_mul(sm.sh[N + cur], sm.sl[N + cur], wh, wl, rh, rl);                 // S_d w(x)
         df_sub(rh, rl, lh, ll, dh, dl);
         ok = dh > 0.f;

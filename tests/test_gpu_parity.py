@@ -479,3 +479,39 @@ def test_sampled_token_agreement_rate(gpu_lib):
     assert rep.sampled_rows >= 10000
     assert rep.sampled_mismatch <= 1e-4 * rep.rows, rep.summary()
     print(rep.summary())
+
+
+@pytest.mark.parametrize("u", [0.0, float(np.nextafter(np.float32(1.0), np.float32(0.0)))])
+def test_uniforms_at_the_ends(gpu_lib, u):
+    """u = 0 and the largest binary32 below 1, for every acceptance and draw:
+    u = 0 accepts every draft token with p(x) > 0 and draws the first token
+    of positive weight (exact on both sides); u just below 1 rejects unless
+    p(x)/q(x) >= 1 and draws near the end of the CDF (compared with the
+    boundary rule)."""
+    w = W.workload("llama_sd", B=12)
+    inp = W.make_inputs(w, device=DEV, seed=515, temp="stochastic")
+    inp["u_acc"].fill_(u)
+    inp["u_smp"].fill_(u)
+    out = run_verify(gpu_lib, inp)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inp, np.arange(w.B))
+    if u == 0.0:
+        assert np.array_equal(to_np(out["accept_len"]), ref["accept_len"])
+        assert np.array_equal(to_np(out["out_tok"]), ref["out_tok"])
+        assert (ref["accept_len"] == w.k).all()
+    rep = compare_verify(inp, out, np.arange(w.B), ref, Report())
+    assert not rep.failures, rep.failures
+    tr = W.make_tree_inputs(12, W.tree_parents((3, 2)), 4096, temp="stochastic", seed=516,
+                            device=DEV)
+    tr["u_acc"].fill_(u)
+    tr["u_smp"].fill_(u)
+    to = gpu_lib.ssd_verify_tree(tr["Z"], tr["D"], tr["parent"], tr["tok"], tr["T"],
+                                 tr["u_acc"], tr["u_smp"])
+    torch.cuda.synchronize()
+    tc = {k: v.cpu() for k, v in tr.items()}
+    rt = oracle.verify_tree(tc["Z"], tc["D"], tc["parent"], tc["tok"], tc["T"], tc["u_acc"],
+                            tc["u_smp"])
+    if u == 0.0:
+        for key in ("accept_len", "out_tok", "out_node"):
+            assert np.array_equal(to_np(to[key]), rt[key]), key
+        assert (rt["accept_len"] == 2).all()      # the first child at every level
