@@ -50,6 +50,8 @@ struct PassSmem {
   int i[kWarps], n[kWarps];
   float bv[kWarps];
   int bi[kWarps];
+  float tw[2 * kWarps];        // each warp's two largest fourth values
+  float tau;
 };
 
 // A thread's four best (value, index) pairs, sorted, and b5, the largest
@@ -143,6 +145,40 @@ __device__ __forceinline__ void warp_merge_top32(float* av, int* ai, const float
   __syncwarp();
 }
 
+// A lower bound of the value of the K-th largest element seen so far by
+// the CTA: the m-th largest (m = ceil(K/4) <= 2 kWarps) of the warps' two
+// largest fourth values, since m threads then hold four elements each at or
+// above it.  An element below the bound cannot be among the K largest.
+// -inf while fewer than m lists are full.  Every thread must call it (two
+// barriers).
+__device__ __forceinline__ float topk_lower_bound(float t3, int i3, int m, PassSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float v = i3 == kIdxNone ? -INFINITY : t3;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {  // this warp's two largest (one instance removed)
+    float w = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(kFull, w, o));
+    if (lane == 0) sm.tw[2 * warp + r] = w;
+    const unsigned own = __ballot_sync(kFull, v == w);
+    if (lane == __ffs(own) - 1) v = -INFINITY;
+  }
+  __syncthreads();
+  if (warp == 0) {  // lane a ranks value a among the 2 kWarps values (ties by position)
+    const float x = lane < 2 * kWarps ? sm.tw[lane] : -INFINITY;
+    int above = 0;
+#pragma unroll
+    for (int c = 0; c < 2 * kWarps; ++c) {
+      const float y = sm.tw[c];
+      above += (y > x || (y == x && c < lane)) ? 1 : 0;
+    }
+    const unsigned hit = __ballot_sync(kFull, lane < 2 * kWarps && above == m - 1);
+    if (lane == __ffs(hit) - 1) sm.tau = x;
+  }
+  __syncthreads();
+  return sm.tau;
+}
+
 // Best (value, index) of the elements of [lo, hi) (thread-strided vectors)
 // that rank after (pv, pi), -inf and NaN skipped.
 template <typename Tag, bool VEC>
@@ -210,7 +246,14 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
   st.b5 = -INFINITY;
   st.nan = 0;
   const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
-  for (int vb = v0 + tid; vb < v1; vb += kThreads * U) {
+  // Vectors whose maximum is below tau, a lower bound of the K-th largest
+  // value (refreshed after 1, 2, 4, 8, ... rounds), are skipped: at a whole
+  // row per CTA this spares most of the divergent list insertions.
+  const int m4 = (p.K + kPer - 1) / kPer;
+  float tau = -INFINITY;
+  int it = 0;
+  for (int base = v0; base < v1; base += kThreads * U, ++it) {  // block-uniform trips
+    const int vb = base + tid;
     typename Tag::Raw raw[U];
     float sc[U];
 #pragma unroll
@@ -233,6 +276,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
         for (int e = 1; e < kV; ++e) vm = max_nan(vm, z[e]);
         if (vm != vm) {
           st.nan = 1;
+        } else if (vm < tau) {
+          // below the bound: none of these is among the K largest
         } else if (!(vm > st.t[3])) {
           st.b5 = fmaxf(st.b5, vm);  // the whole vector stays below the list
         } else {
@@ -241,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 4) topk_pass_kernel(TopkParams p) {
         }
       }
     }
+    if (((it + 1) & it) == 0 && base + kThreads * U < v1)
+      tau = topk_lower_bound(st.t[kPer - 1], st.i[kPer - 1], m4, sm);
   }
   // the warps' largest "fifth" values
   float w5 = st.nan ? NAN : st.b5;
