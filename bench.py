@@ -612,7 +612,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiling captures only; not the metric's workload)")
-    ap.add_argument("--only", choices=["tree", "topk", "draft"], default=None,
+    ap.add_argument("--only", choices=["tree", "topk", "draft", "b1"], default=None,
                     help="one of the next rows' measurements alone (profiling captures; "
                          "B from --batch, timed calls from --steps)")
     ap.add_argument("--topk-k", type=int, default=32, help="K of --only topk")
@@ -627,8 +627,9 @@ def main():
 
 def only_arm(args):
     """One of the next rows' measurements alone, for profiler captures:
-    tree (the tree workload), topk or draft (the benchmark workload); --batch
-    overrides B, --steps sets the timed calls."""
+    tree (the tree workload), topk or draft (the benchmark workload), b1 (the
+    B = 1 SSD step, eager then as a graph); --batch overrides B, --steps sets
+    the timed calls."""
     import torch
     import speculative_decoding_verification_70_gb300 as ssd
     from speculative_decoding_verification_70_gb300 import workloads as W
@@ -638,6 +639,8 @@ def only_arm(args):
         if args.batch:
             W.TREE_B64 = dict(W.TREE_B64, B=args.batch)
         res = tree_verify(ssd, W, "cuda", reps=reps)
+    elif args.only == "b1":
+        res = b1_latency(ssd, W, "cuda", reps=reps)
     else:
         w = W.workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
         inp = W.make_inputs(w, device="cuda", seed=W.default_seed(WORKLOAD))
