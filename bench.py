@@ -388,6 +388,36 @@ def cpu_baseline_sample(inp, w, target_s=15.0, max_rows=None):
                       % (rows, w.B, WORKLOAD, dt)}
 
 
+def _oracle_worker(job):
+    """One process of the all-cores CPU baseline: draw `rows` batch rows of
+    the benchmark workload with its own seed and time the oracle's step on
+    them (verify_recover + forked_topf + the dict cache)."""
+    rows, seed = job
+    import torch
+    from speculative_decoding_verification_70_gb300 import workloads as W
+    torch.set_num_threads(1)
+    w = W.workload(WORKLOAD, B=rows)
+    inp = W.make_inputs(w, device="cpu", seed=seed)
+    t0 = time.perf_counter()
+    run_oracle_step(inp, w, rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(rows_per_core=48):
+    """The oracle on every host core: one spawned process per core, each on
+    its own bounded sample of the workload; throughput = all rows / the
+    slowest process's oracle time."""
+    import multiprocessing as mp
+    import oracle
+    oracle.build()
+    n = len(os.sched_getaffinity(0))
+    with mp.get_context("spawn").Pool(n) as pool:
+        times = pool.map(_oracle_worker, [(rows_per_core, 9000 + i) for i in range(n)])
+    return {"value": n * rows_per_core / max(times), "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": "%d processes x %d batch rows of %s each (own seeds); the slowest "
+                      "took %.1f s" % (n, rows_per_core, WORKLOAD, max(times))}
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -492,6 +522,7 @@ def gpu_arm(args):
         line["tree_verify"] = tree_verify(ssd, W, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
     if rank == 0:
         print(json.dumps(line), flush=True)
     step.cache.close()
