@@ -218,3 +218,25 @@ def test_tree_graph_replay(gpu_lib):
     torch.cuda.synchronize()
     for k in ref:
         assert torch.equal(out[k], ref[k]), k
+
+
+def test_tree_golden_cases(gpu_lib):
+    """The hand-derived cases of tests/golden/tree_cases.json on the GPU."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "tree_cases.json")) as fh:
+        cases = json.load(fh)["cases"]
+    for case in cases:
+        Z = np.log(np.array(case["target_weights"], dtype=np.float64)).astype(np.float32)[None]
+        D = np.log(np.array(case["draft_weights"], dtype=np.float64)).astype(np.float32)[None]
+        t = lambda a, dt: torch.tensor(a, dtype=dt, device=DEV)
+        out = gpu_lib.ssd_verify_tree(t(Z, torch.float32), t(D, torch.float32),
+                                      t([case["parent"]], torch.int32),
+                                      t([case["tok"]], torch.int32),
+                                      t([case["T"]], torch.float32),
+                                      t([case["u_acc"]], torch.float32),
+                                      t([case["u_smp"]], torch.float32))
+        torch.cuda.synchronize()
+        assert int(out["accept_len"][0]) == case["accept_len"], case["name"]
+        assert to_np(out["out_tok"])[0].tolist() == case["out_tok"], case["name"]
+        assert to_np(out["out_node"])[0].tolist() == case["out_node"], case["name"]

@@ -799,3 +799,22 @@ def test_tree_law_by_sampling():
     exp = (pr[:, None] * pc).reshape(-1) * B
     assert scipy.stats.chisquare(obs, exp).pvalue > 1e-4
     assert (n >= 1).mean() > 0.3 and (n == 0).any() and (n == 2).any()
+
+
+def tree_golden_inputs(case):
+    """Arrays of one hand-derived tree case (tests/golden/tree_cases.json)."""
+    Z = np.log(np.array(case["target_weights"], dtype=np.float64)).astype(np.float32)[None]
+    D = np.log(np.array(case["draft_weights"], dtype=np.float64)).astype(np.float32)[None]
+    return (Z, D, np.array([case["parent"]], np.int32), np.array([case["tok"]], np.int32),
+            np.array([case["T"]], np.float32), np.array([case["u_acc"]]),
+            np.array([case["u_smp"]]))
+
+
+def test_golden_tree_cases():
+    g = _golden("tree_cases.json")
+    for case in g["cases"]:
+        Z, D, par, tok, T, ua, us = tree_golden_inputs(case)
+        r = oracle.verify_tree(Z, D, par, tok, T, ua, us, f64_uniforms=True)
+        assert r["accept_len"][0] == case["accept_len"], case["name"]
+        assert list(r["out_tok"][0]) == case["out_tok"], case["name"]
+        assert list(r["out_node"][0]) == case["out_node"], case["name"]
