@@ -97,13 +97,14 @@ SSD_API int ssd_version(void);
 /*
  * Streams, graphs, batch size.  Every call enqueues work on the caller's
  * stream and returns: no device allocation, no host synchronisation (except
- * the error-word reads, which say so).  A batched verify (B >= 32) runs its
- * target-row and draft-row statistics on two internal streams forked from
- * and joined back to the caller's stream by events; the streams and events
- * are created on the first such call on a device.  Calls can therefore be
- * captured into a CUDA graph (make one batched call on the device before
- * capturing).  B may exceed 65535: kernels launch in grids of 65535 batch
- * rows.
+ * the error-word reads, which say so).  The verify calls (all but
+ * ssd_verify_noalloc) run the target-row and draft-row statistics on two
+ * internal streams forked from and joined back to the caller's stream by
+ * events, and the SSD round step inserts the forks into the cache on the
+ * second one beside the draw; the streams and events are created on the
+ * first such call on a device.  Calls can therefore be captured into a CUDA
+ * graph (make one verify call on the device before capturing).  B may exceed
+ * 65535: kernels launch in grids of 65535 batch rows.
  */
 
 /*
