@@ -419,11 +419,13 @@ cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool
   return e;
 }
 
-// Schedule: for B >= 32 the batch is cut into S slices.  The target-row and
-// draft-row statistics of each slice run on two internal streams; the
-// slice's finalisation and draw run on the caller's stream after both
-// (events), overlapping the next slice's statistics.  The caller's stream
-// waits for everything before its next work, so stream order is kept.
+// Schedule: for B >= SSD_MIN_STREAMED_B (every batch by default) the batch
+// is cut into S = max(1, B / SSD_SLICE_ROWS) slices (one slice up to 2047
+// rows).  The target-row and draft-row statistics of each slice run on two
+// internal streams; the slice's finalisation and draw run on the caller's
+// stream after both (events), overlapping the next slice's statistics.  The
+// caller's stream waits for everything before its next work, so stream order
+// is kept.
 ssd_status run_verify(const VerifyCall& c, bool fork) {
   ssd_status st = check_common(c, fork);
   if (st != SSD_OK) return st;
