@@ -672,6 +672,8 @@ ssd_status ssd_verify_tree(const void* Z, int64_t z_bstride, const void* D, int6
   tp.parent = parent; tp.tok = tok; tp.T = T; tp.u_acc = u_acc; tp.u_smp = u_smp;
   tp.part = sp.part; tp.accept_len = accept_len; tp.out_tok = out_tok; tp.out_node = out_node;
   tp.err = sp.err;
+  tp.cache = reinterpret_cast<float4*>(wsp(ws, L.cache));
+  tp.cache_stride = static_cast<int64_t>(L.cache_stride);
   ProfScope ps("tree_walk", S(stream));
   return cuda_status(launch_tree_walk(tp, dt, vec, S(stream)));
 }

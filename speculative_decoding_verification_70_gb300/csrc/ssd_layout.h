@@ -139,8 +139,10 @@ struct ResidualParams {
 // Token-tree verification (ssd_verify_tree).
 constexpr int kMaxTreeNodes = 64;
 
+constexpr int kTreeCacheMinV = 32768;
+
 struct TreeLayout {
-  size_t err, part, total;
+  size_t err, part, cache, cache_stride, total;
   int R;          // rows per batch row: N target, N draft
   Chunking ch;
 };
@@ -159,6 +161,8 @@ struct TreeParams {
   int32_t* out_tok;        // [B][N]
   int32_t* out_node;       // [B][N] or null
   int* err;
+  float4* cache;           // [B][cache_stride]: e_z, e_d (float pairs) at the node being walked
+  int64_t cache_stride;    // 0: no cache (short rows)
 };
 
 // Top-k / top-p filtered verify (ssd_verify_topk).
@@ -331,6 +335,10 @@ inline TreeLayout make_tree_layout(int B, int N, int V, int esize = 4) {
   size_t off = 0;
   L.err = off;                      off = align256(off + 16);
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * L.ch.C);
+  // per tree V + 32768 slots (the walk's thread ranges, padded) when rows
+  // are long enough for the cache to pay; none otherwise
+  L.cache_stride = V >= kTreeCacheMinV ? static_cast<size_t>(V) + 32768 : 0;
+  L.cache = off;                    off = align256(off + sizeof(float) * 4 * B * L.cache_stride);
   L.total = off;
   return L;
 }

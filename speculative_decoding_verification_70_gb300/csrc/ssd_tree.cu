@@ -112,26 +112,50 @@ __device__ __forceinline__ void tree_sum_df(float h, float l, TreeSmem& sm, floa
   __syncthreads();
 }
 
+// max(0, e_z - rho e_d) from the two exponentials (float pairs); false when
+// the weight is zero.
+__device__ __forceinline__ bool tree_w(float ah, float al, float bh, float bl, float rho_h,
+                                       float rho_l, float& wh, float& wl) {
+  float rbh, rbl;
+  df_mul(rho_h, rho_l, bh, bl, rbh, rbl);
+  df_sub(ah, al, rbh, rbl, wh, wl);
+  return wh > 0.f;
+}
+
+// The two exponentials of one element: e_z = 2^((z - m_z) c2), e_d likewise.
+__device__ __forceinline__ void tree_exps(float z, float d, float mz, float md, float2 c2,
+                                          const float2* tab, float4& e) {
+  float xh, xl;
+  arg_df(z, mz, c2.x, c2.y, xh, xl);
+  exp2_df(xh, xl, tab, e.x, e.y);
+  arg_df(d, md, c2.x, c2.y, xh, xl);
+  exp2_df(xh, xl, tab, e.z, e.w);
+}
+
 // The draw weight of one element: max(0, e_z - rho e_d) as a float pair
 // (e_z alone when rho == 0).  Returns false when the weight is zero.
 __device__ __forceinline__ bool tree_weight(float z, float d, float mz, float md, float2 c2,
                                             float rho_h, float rho_l, const float2* tab,
                                             float& wh, float& wl) {
-  float xh, xl, ah, al;
-  arg_df(z, mz, c2.x, c2.y, xh, xl);
-  exp2_df(xh, xl, tab, ah, al);
   if (rho_h == 0.f) {
-    wh = ah;
-    wl = al;
-    return ah > 0.f;
+    float xh, xl;
+    arg_df(z, mz, c2.x, c2.y, xh, xl);
+    exp2_df(xh, xl, tab, wh, wl);
+    return wh > 0.f;
   }
-  float bh, bl, rbh, rbl;
-  arg_df(d, md, c2.x, c2.y, xh, xl);
-  exp2_df(xh, xl, tab, bh, bl);
-  df_mul(rho_h, rho_l, bh, bl, rbh, rbl);
-  df_sub(ah, al, rbh, rbl, wh, wl);
-  return wh > 0.f;
+  float4 e;
+  tree_exps(z, d, mz, md, c2, tab, e);
+  return tree_w(e.x, e.y, e.z, e.w, rho_h, rho_l, wh, wl);
 }
+
+// Passes over a node's rows.  kCompute: weights from the logits (rho == 0:
+// e_z alone); kStore: the same with rho != 0, keeping each element's two
+// exponentials in the tree's cache row; kCached: later passes at the same
+// node read them back (a load and a few double-float operations instead of
+// two exponentials).  Every thread reads back only what it wrote; element
+// lo + i of thread g sits at cache[i * nt + g] (nt threads per tree), so a
+// warp's accesses are 512 contiguous bytes.
+constexpr int kCompute = 0, kStore = 1, kCached = 2;
 
 // One pass over the node's rows: this thread's compensated sum of the
 // weights of its range and the last index with a positive weight (-1).
@@ -139,11 +163,55 @@ template <typename Tag, bool VEC>
 __device__ __forceinline__ void tree_pass(const typename Tag::Elem* zr,
                                           const typename Tag::Elem* dr, int lo, int hi, float mz,
                                           float md, float2 c2, float rho_h, float rho_l,
-                                          const float2* tab, float& acc, float& comp,
-                                          int& last) {
+                                          const float2* tab, float4* cache, int nt, int mode,
+                                          float& acc, float& comp, int& last) {
   acc = 0.f;
   comp = 0.f;
   last = -1;
+  if (mode == kCached) {
+    for (int v = lo; v < hi; ++v) {
+      const float4 e = cache[static_cast<int64_t>(v - lo) * nt];
+      float wh, wl;
+      if (tree_w(e.x, e.y, e.z, e.w, rho_h, rho_l, wh, wl)) {
+        comp_acc(acc, comp, wh, wl);
+        last = v;
+      }
+    }
+    return;
+  }
+  if (mode == kStore) {
+    if (VEC) {
+      constexpr int kV = Tag::kVec;
+      for (int v = lo; v < hi; v += kV) {
+        float z[8], d[8];
+        Tag::loadv_cached(zr + v, z);
+        Tag::loadv_cached(dr + v, d);
+#pragma unroll
+        for (int e = 0; e < kV; ++e) {
+          float4 x;
+          tree_exps(z[e], d[e], mz, md, c2, tab, x);
+          cache[static_cast<int64_t>(v + e - lo) * nt] = x;
+          float wh, wl;
+          if (tree_w(x.x, x.y, x.z, x.w, rho_h, rho_l, wh, wl)) {
+            comp_acc(acc, comp, wh, wl);
+            last = v + e;
+          }
+        }
+      }
+    } else {
+      for (int v = lo; v < hi; ++v) {
+        float4 x;
+        tree_exps(Tag::load1(zr + v), Tag::load1(dr + v), mz, md, c2, tab, x);
+        cache[static_cast<int64_t>(v - lo) * nt] = x;
+        float wh, wl;
+        if (tree_w(x.x, x.y, x.z, x.w, rho_h, rho_l, wh, wl)) {
+          comp_acc(acc, comp, wh, wl);
+          last = v;
+        }
+      }
+    }
+    return;
+  }
   const bool use_d = rho_h != 0.f;
   if (VEC) {
     constexpr int kV = Tag::kVec;
@@ -318,6 +386,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   bool ready = false;                       // acc/comp/last hold a pass for (rho, W)
   float acc = 0.f, comp = 0.f;
   int last = -1;
+  const int nt = cs * kTreeThreads;         // E * nt <= V + 8 nt <= V + 32768
+  const bool use_cache = p.cache_stride > 0;
+  float4* cache = use_cache ? p.cache + static_cast<int64_t>(b) * p.cache_stride + g : nullptr;
+  int cached = -1;                          // the node whose exponentials the cache holds
   for (;;) {
     while (c < N && sm.par[c] != cur) ++c;
     if (c >= N) break;  // the children of cur are exhausted
@@ -365,7 +437,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     df_acc(nh, nl, qh, ql);
     float a2, c2p;
     int l2;
-    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, nh, nl, sm.tab, a2, c2p, l2);
+    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, nh, nl, sm.tab, cache, nt,
+                        !use_cache ? kCompute : (cached == cur ? kCached : kStore), a2, c2p,
+                        l2);
+    cached = cur;
     float sh2, sl2, Bh, Bl, Th, Tl;
     two_sum(a2, c2p, sh2, sl2);
     tree_sum_df(sh2, sl2, sm, Bh, Bl);
@@ -386,8 +461,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   const Elem* zr = Zb + static_cast<int64_t>(cur) * V;
   const Elem* dr = Db + static_cast<int64_t>(cur) * V;
   const float mz = sm.m[cur], md = sm.m[N + cur];
+  const bool from_cache = use_cache && rho_h != 0.f && cached == cur;
   if (!ready) {
-    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, rho_h, rho_l, sm.tab, acc, comp, last);
+    tree_pass<Tag, VEC>(zr, dr, lo, hi, mz, md, c2, rho_h, rho_l, sm.tab, cache, nt,
+                        from_cache ? kCached : kCompute, acc, comp, last);
     float sh2, sl2, Bh, Bl;
     two_sum(acc, comp, sh2, sl2);
     tree_sum_df(sh2, sl2, sm, Bh, Bl);
@@ -423,8 +500,15 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
     int tok = last;
     for (int v = lo; v < hi; ++v) {  // walk the range in the order of the pass
       float wh, wl;
-      const float d = rho_h != 0.f ? Tag::load1(dr + v) : 0.f;
-      if (tree_weight(Tag::load1(zr + v), d, mz, md, c2, rho_h, rho_l, sm.tab, wh, wl)) {
+      bool pos;
+      if (from_cache) {
+        const float4 e = cache[static_cast<int64_t>(v - lo) * nt];
+        pos = tree_w(e.x, e.y, e.z, e.w, rho_h, rho_l, wh, wl);
+      } else {
+        const float d = rho_h != 0.f ? Tag::load1(dr + v) : 0.f;
+        pos = tree_weight(Tag::load1(zr + v), d, mz, md, c2, rho_h, rho_l, sm.tab, wh, wl);
+      }
+      if (pos) {
         float ph, pl;
         df_mul(wh, wl, rwh, rwl, ph, pl);
         cum += df_to_fix(ph, pl, kFix);
