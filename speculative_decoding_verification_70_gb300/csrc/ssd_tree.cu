@@ -31,8 +31,11 @@
 // one range).  Pass totals are exchanged through distributed shared memory
 // (each CTA publishes its sum, a cluster barrier, every CTA adds the cs
 // sums in rank order).  Element weights are double-float with compensated
-// sums; the draw converts the per-thread sums to exact 2^-48 fixed point
-// for an order-independent scan.  Rank 0 writes the outputs.
+// sums; a node's first residual pass keeps each element's two exponentials
+// in the workspace (rows of at least 32768 elements) for the later passes
+// at that node and the draw.  The draw converts the per-thread sums to
+// exact 2^-48 fixed point for an order-independent scan.  Rank 0 writes the
+// outputs.
 #include <cooperative_groups.h>
 #include <math.h>
 
