@@ -385,7 +385,10 @@ SSD_API ssd_status ssd_verify_topk(const void *Z, int64_t z_bstride, const void 
  *              then -1 (all -1 on a sentinel).
  *   out_node : [B, N] or NULL: the accepted node ids, then -1.
  *   ws       : ssd_tree_workspace_bytes(B, N, V) bytes (its first word is
- *              the device error word, as for ssd_verify).
+ *              the device error word, as for ssd_verify).  For V >= 32768
+ *              it includes a cache of 16 (V + 32768) bytes per tree, where a
+ *              node's first residual pass keeps each element's two
+ *              exponentials for the later passes at that node.
  * Errors: SSD_ERR_INVALID_ARG for null required pointers, sizes out of
  * range, strides below N*V or misaligned pointers; SSD_ERR_WORKSPACE when
  * ws_bytes is too small; SSD_ERR_CUDA when a launch fails.
