@@ -233,6 +233,103 @@ def b1_latency(ssd, W, dev, reps=300):
             "eager_us": round(eager, 2), "graph_us": round(graph, 2)}
 
 
+def config_throughput(ssd, W, dev, name, temp=None, sets=128, rounds=10, peak=None):
+    """One workload of the table in its own launch configuration, measured
+    like the headline step: ms per call with CUDA events over `rounds`
+    passes through `sets` input sets (the sets together are larger than L2,
+    so each call streams its logits from HBM), rows/s, and GB/s over the
+    algorithmic bytes (every logit row read once: the 2k+1 rows of the
+    verify plus, for the SSD round step, draft row k).  B = 1 workloads are
+    also captured as one CUDA graph of `sets` steps (per-step time of the
+    replay).  The SSD workloads run ssd_verify_fork_cache (verify + forks +
+    cache clear / insert / outcome lookup), the sync one ssd_verify."""
+    import torch
+    w = W.workload(name)
+    forks = w.ssd and w.f > 0
+    s = 4 if w.dtype == "f32" else 2
+    rows_read = (2 * w.k + 1) + (1 if forks else 0)
+    step_bytes = w.B * rows_read * w.V * s
+    # enough sets to hold 3x the 129 MB L2 (at most `sets`, at least 2)
+    nsets = max(2, min(sets, -(-3 * 129 * 2 ** 20 // step_bytes)))
+    inp = W.make_inputs(W.workload(name, B=w.B * nsets), device=dev,
+                        seed=W.default_seed(name) + 17, temp=temp)
+    stream = torch.cuda.current_stream()
+    ws = ssd.new_workspace(ssd.workspace_bytes(w.B, w.k, w.V, w.f if forks else 0), dev)
+    cache = ssd.SpecCache(1 << max(6, (2 * w.B * (w.k + 1) * w.f - 1).bit_length()),
+                          CACHE_DEPTH) if forks else None
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    payload = torch.randint(0, w.V, (w.B * (w.k + 1) * max(w.f, 1), CACHE_DEPTH), generator=g,
+                            device=dev, dtype=torch.int32)
+    views = []
+    for i in range(nsets):
+        sl = slice(i * w.B, (i + 1) * w.B)
+        views.append(({key: v[sl] for key, v in inp.items()}, {}))
+
+    def call(i):
+        v, o = views[i]
+        if forks:
+            ssd.ssd_verify_fork_cache(v["Z"], v["D"], v["x"], v["T"], v["u_acc"], v["u_smp"],
+                                      w.f, v["mask"], cache, payload, ws=ws, out=o)
+        else:
+            ssd.ssd_verify(v["Z"], v["D"], v["x"], v["T"], v["u_acc"], v["u_smp"], ws=ws, out=o)
+
+    def sweep():
+        for i in range(nsets):
+            call(i)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms = timed(sweep, rounds) / nsets
+    prof_stats = None
+    if w.B > 1:   # the statistics pass as a phase (fork to join), per-launch events
+        ssd.profile_begin(16 * nsets)
+        sweep()
+        torch.cuda.synchronize()
+        prof = ssd.profile_end()
+        if prof.get("stats_pass", {}).get("timed"):
+            prof_stats = prof["stats_pass"]["total_ms"] / prof["stats_pass"]["timed"]
+    peak = peak or measured_peaks()[0]
+    vb = w.B * (2 * w.k + 1) * w.V * s + (w.B * w.V * s if forks else 0)
+    res = {"workload": "%s: B=%d k=%d%s V=%d %s, T=%s" % (
+               name, w.B, w.k, (" f=%d" % w.f) if forks else "", w.V, w.dtype,
+               temp if temp is not None else w.temp),
+           "call": "ssd_verify_fork_cache" if forks else "ssd_verify",
+           "us_per_step": round(ms * 1e3, 2), "rows_per_s": round(w.B / (ms / 1e3), 1),
+           "algorithmic_bytes": vb, "gbs": round(vb / (ms / 1e3) / 1e9, 1),
+           "frac_of_measured_peak": round(vb / (ms / 1e3) / 1e9 / peak, 4),
+           "input_sets": nsets, "l2": "each call reads a set not touched since %d calls ago"
+                                     % (nsets - 1)}
+    if prof_stats:
+        res["stats_pass_ms"] = round(prof_stats, 5)
+        res["stats_pass_gbs"] = round(vb / (prof_stats / 1e3) / 1e9, 1)
+        res["stats_pass_frac_of_measured_peak"] = round(vb / (prof_stats / 1e3) / 1e9 / peak, 4)
+    if w.B == 1:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            sweep()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            sweep()
+        res["graph_us_per_step"] = round(timed(graph.replay, rounds) / nsets * 1e3, 2)
+    if cache is not None:
+        cache.close()
+    del inp, views
+    return res
+
+
 def draft_pipeline(ssd, w, inp, dev, reps=50):
     """The drafter's side fused with the verify (the next step of the hot
     path): ssd_draft_sample over the k+1 SSD draft rows (Gumbel-max tokens,
@@ -516,6 +613,14 @@ def gpu_arm(args):
             "logit_rows_per_s": round(value * (2 * w.k + 1), 1),
             "us_per_step": round(ms_step * 1e3, 2)}
     if rank == 0 and world == 1:
+        peak = measured_peaks()[0]
+        line["configs"] = {
+            "llama_sd_T0": config_throughput(ssd, W, dev, "llama_sd", "0", peak=peak),
+            "llama_sd_T1": config_throughput(ssd, W, dev, "llama_sd", "1.0", peak=peak),
+            "ssd_fork_T0": config_throughput(ssd, W, dev, "ssd_fork", "0", peak=peak),
+            "ssd_fork_T1": config_throughput(ssd, W, dev, "ssd_fork", "1.0", peak=peak),
+            "qwen_b64": config_throughput(ssd, W, dev, "qwen_b64", peak=peak),
+        }
         line["latency_b1"] = b1_latency(ssd, W, dev)
         line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)
         line["topk_verify"] = topk_verify(ssd, w, inp, dev)
@@ -643,7 +748,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override B (profiling captures only; not the metric's workload)")
-    ap.add_argument("--only", choices=["tree", "topk", "draft", "b1"], default=None,
+    ap.add_argument("--only", choices=["tree", "topk", "draft", "b1", "qwen_b64", "llama_sd",
+                                       "ssd_fork"], default=None,
                     help="one of the next rows' measurements alone (profiling captures; "
                          "B from --batch, timed calls from --steps)")
     ap.add_argument("--topk-k", type=int, default=32, help="K of --only topk")
@@ -672,6 +778,8 @@ def only_arm(args):
         res = tree_verify(ssd, W, "cuda", reps=reps)
     elif args.only == "b1":
         res = b1_latency(ssd, W, "cuda", reps=reps)
+    elif args.only in ("qwen_b64", "llama_sd", "ssd_fork"):
+        res = config_throughput(ssd, W, "cuda", args.only, rounds=reps)
     else:
         w = W.workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
         inp = W.make_inputs(w, device="cuda", seed=W.default_seed(WORKLOAD))

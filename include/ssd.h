@@ -196,6 +196,13 @@ SSD_API ssd_status ssd_verify(const void *Z, int64_t z_bstride, const void *D,
  *     that overlap on the GPU (other streams, other host threads) race.
  *   - The array's device error word is not exposed: data errors show as the
  *     accept_len sentinels.
+ *   - u_smp may be NULL (out_tok then too): acceptance only.  T > 0 rows then
+ *     get no recovery / bonus token (out_tok[b][n] = -1, if out_tok is
+ *     given), and no later call can draw it, because ssd_sample_residual
+ *     needs the statistics in a workspace this call does not expose.
+ *   - Argument checks run before the array is touched: invalid sizes return
+ *     SSD_ERR_INVALID_ARG, sizes beyond the array SSD_ERR_WORKSPACE, then
+ *     null or misaligned pointers SSD_ERR_INVALID_ARG.
  */
 #define SSD_NOALLOC_SCRATCH_BYTES (8u << 20)
 SSD_API ssd_status ssd_verify_noalloc(const void *Z, int64_t z_bstride, const void *D,
@@ -500,6 +507,22 @@ typedef struct {
 
 SSD_API ssd_status ssd_profile_begin(int max_launches);
 SSD_API ssd_status ssd_profile_end(ssd_profile_entry *out, int cap, int *n_out);
+
+/*
+ * Vocabulary split override (tuning and tests; not part of the method).
+ * Every logit row is split into chunks ("split-V") that CTAs stream and
+ * whose partial statistics are merged in chunk order.  chunk_elems > 0 fixes
+ * the chunk length (rounded up to a multiple of 8 and clamped to
+ * [ceil(V / 256), 32 KB of logits]); chunks_per_cta > 0 fixes how many
+ * consecutive chunks one statistics CTA streams (at most the chunk count).
+ * 0 restores the built-in policy.  The setting is process-wide and read when
+ * a call (or a workspace-size query) lays out its workspace, so query the
+ * workspace size after setting it.  Integer results (accept lengths, tokens,
+ * forks, cache lookups) do not depend on it; float outputs (p_at_x, q_at_x,
+ * softmax sums) can differ in the last bits, because the chunk sums round
+ * differently.  Returns SSD_ERR_INVALID_ARG for negative values.
+ */
+SSD_API ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta);
 
 /*
  * Self-test hook for the library's extended-precision exponential (used by

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     profile_begin,
     profile_end,
     selftest_exp2,
+    set_split,
     softmax_workspace_bytes,
     ssd_draft_sample,
     ssd_forked_recovery,

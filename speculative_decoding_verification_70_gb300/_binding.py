@@ -75,6 +75,7 @@ SIGNATURES = [
     ("ssd_selftest_exp2", _I, [_P, _P, _P, _I, _P]),
     ("ssd_verify_noalloc", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P]),
+    ("ssd_set_split", _I, [_I, _I]),
     ("ssd_profile_begin", _I, [_I]),
     ("ssd_profile_end", _I, [_P, _I, _P]),
 ]
@@ -576,6 +577,13 @@ def selftest_exp2(x_hi: torch.Tensor, x_lo: torch.Tensor, stream=None) -> torch.
     _check("ssd_selftest_exp2", load_library().ssd_selftest_exp2(
         _dev(x_hi, "x_hi"), _dev(x_lo, "x_lo"), _dev(out, "out"), x_hi.numel(), _stream(stream)))
     return out
+
+
+def set_split(chunk_elems: int = 0, chunks_per_cta: int = 0):
+    """Override the vocabulary split (elements per chunk, chunks per
+    statistics CTA; 0 = the library's policy) for later calls in this
+    process.  Integer results do not depend on it."""
+    _check("ssd_set_split", load_library().ssd_set_split(int(chunk_elems), int(chunks_per_cta)))
 
 
 def profile_begin(max_launches: int = 4096):

@@ -9,6 +9,10 @@
 #include <new>
 #include <vector>
 
+#ifndef SSD_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 #include "../../include/ssd.h"
 #include "ssd_layout.h"
 
@@ -108,6 +112,19 @@ struct ProfScope {
   ProfScope& operator=(const ProfScope&) = delete;
 };
 
+// One NVTX range per library call (header-only NVTX3: a no-op unless a
+// profiler such as Nsight Systems or Nsight Compute injects itself).
+struct CallRange {
+#ifndef SSD_NO_NVTX
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+#else
+  explicit CallRange(const char*) {}
+#endif
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+
 inline cudaStream_t S(ssd_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline ssd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
@@ -183,6 +200,7 @@ cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaS
   sp.G = 1;
   while (sp.G < 4 && static_cast<long long>(B) * rows_plain * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
     sp.G *= 2;
+  sp.G = split_group(sp.G, sp.C);
   cudaError_t e = cudaSuccess;
   if (rows_plain > 0) {
     ProfScope ps("stats", s_plain);
@@ -201,6 +219,7 @@ cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaS
   pt.G = 1;
   while (pt.G < 4 && static_cast<long long>(B) * sp.Pdf * ((sp.C + 2 * pt.G - 1) / (2 * pt.G)) >= 2432)
     pt.G *= 2;
+  pt.G = split_group(pt.G, sp.C);
   return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s_topf);
 }
 
@@ -515,6 +534,7 @@ ssd_status ssd_get_device_error(void* ws, ssd_stream_t stream, int32_t* out, int
 ssd_status ssd_softmax_temp(const void* logits, ssd_dtype dtype, int rows, int V, const float* T,
                             float* probs, float* row_max, float* row_sum, int32_t* row_argmax,
                             void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_softmax_temp");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!logits || !T || !row_max || !row_sum || !row_argmax || !ws) return SSD_ERR_INVALID_ARG;
   if (rows < 1 || V < 1 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -555,6 +575,7 @@ ssd_status ssd_verify(const void* Z, int64_t z_bstride, const void* D, int64_t d
                       const float* u_acc, int32_t* accept_len, float* p_at_x, float* q_at_x,
                       const float* u_smp, int32_t* out_tok, void* ws, size_t ws_bytes,
                       ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify");
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
@@ -569,6 +590,7 @@ ssd_status ssd_verify_drafted(const void* Z, int64_t z_bstride, const void* D, i
                               const float* T, const float* u_acc, int32_t* accept_len,
                               float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
                               void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_drafted");
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
@@ -584,6 +606,7 @@ ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, i
                             uint32_t offset, int32_t* x_out, int64_t x_bstride, int f,
                             int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
                             ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_draft_sample");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!D || !T || !x_out || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -614,6 +637,7 @@ ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, i
   sp.G = 1;
   while (sp.G < 4 && static_cast<long long>(B) * rows * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
     sp.G *= 2;
+  sp.G = split_group(sp.G, sp.C);
   const int dt = dtype == SSD_BF16 ? 1 : 0;
   cudaError_t e;
   {
@@ -642,6 +666,7 @@ ssd_status ssd_verify_tree(const void* Z, int64_t z_bstride, const void* D, int6
                            const int32_t* tok, const float* T, const float* u_acc,
                            const float* u_smp, int32_t* accept_len, int32_t* out_tok,
                            int32_t* out_node, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_tree");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!Z || !D || !parent || !tok || !T || !u_acc || !u_smp || !accept_len || !out_tok || !ws)
     return SSD_ERR_INVALID_ARG;
@@ -688,6 +713,7 @@ ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int6
                            int K, const float* top_p, const float* u_acc, int32_t* accept_len,
                            float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
                            void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_topk");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!Z || !D || !x || !T || !u_acc || !accept_len || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -712,6 +738,7 @@ ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int6
   while (tp.G < SSD_TOPK_MAX_GROUP && tp.G < tp.C &&
          static_cast<long long>(B) * L.R * ((tp.C + 2 * tp.G - 1) / (2 * tp.G)) >= 2432)
     tp.G *= 2;
+  tp.G = split_group(tp.G, tp.C);
   tp.T = T; tp.top_p = top_p; tp.x = x; tp.u_acc = u_acc; tp.u_smp = u_smp;
   tp.accept_len = accept_len; tp.p_at_x = p_at_x; tp.q_at_x = q_at_x; tp.out_tok = out_tok;
   tp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
@@ -735,6 +762,7 @@ ssd_status ssd_verify_fork_fanout(const void* Z, int64_t z_bstride, const void* 
                                   const int32_t* fanout, const int32_t* mask, int M,
                                   int32_t* fork_tok, float* fork_logit, void* ws, size_t ws_bytes,
                                   ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_fork_fanout");
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
@@ -756,6 +784,7 @@ ssd_status ssd_verify_fork_cache(const void* Z, int64_t z_bstride, const void* D
                                  ssd_spec_cache* cache, int clear, const int32_t* payload,
                                  int32_t* hit, int32_t* tok_out, void* ws, size_t ws_bytes,
                                  ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_fork_cache");
   if (!cache || !payload || !hit || !tok_out || !out_tok) return SSD_ERR_INVALID_ARG;
   if (k + 1 > 256 || static_cast<int64_t>(B) * (k + 1) * f > 0x7fffffff) return SSD_ERR_INVALID_ARG;
   VerifyCall c;
@@ -786,6 +815,7 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
                                ssd_dtype dtype, int B, int k, int V, const int32_t* x,
                                const float* T, const int32_t* accept_len, const float* u_smp,
                                int32_t* out_tok, void* ws, size_t ws_bytes, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_sample_residual");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!Z || !D || !x || !T || !accept_len || !u_smp || !out_tok || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -839,6 +869,7 @@ ssd_status ssd_forked_recovery_fanout(const void* L_, int64_t l_bstride, ssd_dty
                                       const int32_t* mask, int M, int32_t* fork_tok,
                                       float* fork_logit, void* ws, size_t ws_bytes,
                                       ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_forked_recovery_fanout");
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!L_ || !fork_tok || !fork_logit || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || P < 1 || P > SSD_MAX_K + 1 || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
@@ -927,6 +958,7 @@ void ssd_spec_cache_destroy(ssd_spec_cache* c) {
 }
 
 ssd_status ssd_spec_cache_clear(ssd_spec_cache* c, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_spec_cache_clear");
   if (!c) return SSD_ERR_INVALID_ARG;
   const size_t kb = sizeof(unsigned long long) * c->view.capacity;
   cudaError_t e = cudaMemsetAsync(c->view.keys, 0xff, kb, S(stream));
@@ -937,6 +969,7 @@ ssd_status ssd_spec_cache_clear(ssd_spec_cache* c, ssd_stream_t stream) {
 ssd_status ssd_spec_cache_insert(ssd_spec_cache* c, const int32_t* b, const int32_t* pos,
                                  const int32_t* tok, const int32_t* payload, int n,
                                  ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_spec_cache_insert");
   if (!c || n < 0) return SSD_ERR_INVALID_ARG;
   if (n == 0) return SSD_OK;
   if (!b || !pos || !tok || !payload) return SSD_ERR_INVALID_ARG;
@@ -948,6 +981,7 @@ ssd_status ssd_spec_cache_insert(ssd_spec_cache* c, const int32_t* b, const int3
 
 ssd_status ssd_spec_cache_insert_forks(ssd_spec_cache* c, const int32_t* fork_tok, int B, int P,
                                        int f, const int32_t* payload, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_spec_cache_insert_forks");
   if (!c || !fork_tok || !payload || B < 1 || P < 1 || P > 256 || f < 1) return SSD_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * P * f > 0x7fffffff) return SSD_ERR_INVALID_ARG;
   InsertArgs a;
@@ -959,6 +993,7 @@ ssd_status ssd_spec_cache_insert_forks(ssd_spec_cache* c, const int32_t* fork_to
 ssd_status ssd_spec_cache_lookup(const ssd_spec_cache* c, const int32_t* b, const int32_t* pos,
                                  const int32_t* tok, int n, int32_t* hit, int32_t* tok_out,
                                  ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_spec_cache_lookup");
   if (!c || n < 0) return SSD_ERR_INVALID_ARG;
   if (n == 0) return SSD_OK;
   if (!b || !pos || !tok || !hit || !tok_out) return SSD_ERR_INVALID_ARG;
@@ -972,6 +1007,7 @@ ssd_status ssd_spec_cache_lookup(const ssd_spec_cache* c, const int32_t* b, cons
 ssd_status ssd_spec_cache_lookup_outcome(const ssd_spec_cache* c, const int32_t* accept_len,
                                          const int32_t* out_tok, int B, int k, int32_t* hit,
                                          int32_t* tok_out, ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_spec_cache_lookup_outcome");
   if (!c || !accept_len || !out_tok || !hit || !tok_out || B < 1 || k < 1 || k > SSD_MAX_K)
     return SSD_ERR_INVALID_ARG;
   LookupArgs a;
@@ -1034,18 +1070,34 @@ ssd_status ssd_verify_noalloc(const void* Z, int64_t z_bstride, const void* D, i
                               const float* T, const float* u_acc, int32_t* accept_len,
                               float* p_at_x, float* q_at_x, const float* u_smp, int32_t* out_tok,
                               ssd_stream_t stream) {
+  CallRange nvtx_range("ssd_verify_noalloc");
   VerifyCall c;
   memset(&c, 0, sizeof c);
   c.Z = Z; c.zb = z_bstride; c.D = D; c.db = d_bstride; c.dt = dtype;
   c.B = B; c.k = k; c.V = V; c.x = x; c.T = T; c.u_acc = u_acc;
   c.accept_len = accept_len; c.p_at_x = p_at_x; c.q_at_x = q_at_x;
   c.u_smp = u_smp; c.out_tok = out_tok; c.stream = S(stream);
+  // sizes first (ssd_workspace_bytes is 0 for invalid ones), then the size
+  // limit, then every pointer: nothing reaches the scratch lookup or a
+  // launch unless all of them pass
+  if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
   if (ssd_workspace_bytes(B, k, V, 0) > SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_WORKSPACE;
-  ssd_status st = noalloc_scratch(&c.ws);
+  c.ws = &c;  // stands in for the scratch pointer in the argument check only
+  ssd_status st = check_common(c, false);
+  if (st != SSD_OK) return st;
+  st = noalloc_scratch(&c.ws);
   if (st != SSD_OK) return st;
   c.ws_bytes = SSD_NOALLOC_SCRATCH_BYTES;
   c.single_stream = true;
-  return run_verify(c, false);  // checks the other arguments first
+  return run_verify(c, false);
+}
+
+ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta) {
+  if (chunk_elems < 0 || chunks_per_cta < 0) return SSD_ERR_INVALID_ARG;
+  g_split.chunk.store(chunk_elems, std::memory_order_relaxed);
+  g_split.group.store(chunks_per_cta, std::memory_order_relaxed);
+  return SSD_OK;
 }
 
 ssd_status ssd_profile_begin(int max_launches) {

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ssd {
 
 constexpr int kMaxMask = 64;        // masked tokens per (b, position)
@@ -141,6 +143,17 @@ constexpr int kMaxTreeNodes = 64;
 
 constexpr int kTreeCacheMinV = 32768;
 
+// The tree walk runs kTreeThreads threads per CTA in clusters of at most
+// SSD_TREE_MAX_CLUSTER CTAs.  A pass gives each of the cluster's nt threads a
+// range of E = ceil(V / nt) elements rounded up to a multiple of 8, so the
+// ranges cover at most V + 8 nt slots of a tree's cache row: kTreeCachePad is
+// that padding for the largest cluster.
+constexpr int kTreeThreads = 512;
+#ifndef SSD_TREE_MAX_CLUSTER
+#define SSD_TREE_MAX_CLUSTER 8
+#endif
+constexpr int kTreeCachePad = 8 * SSD_TREE_MAX_CLUSTER * kTreeThreads;
+
 struct TreeLayout {
   size_t err, part, cache, cache_stride, total;
   int R;          // rows per batch row: N target, N draft
@@ -270,11 +283,31 @@ struct LookupArgs {
   int32_t* tok_out;
 };
 
+// Host-side override of the vocabulary split (ssd_set_split): elements per
+// chunk and chunks per statistics CTA, 0 for the policy.  Read when a call
+// lays out its workspace and sizes its grids.
+struct SplitOverride {
+  std::atomic<int> chunk{0};
+  std::atomic<int> group{0};
+};
+inline SplitOverride g_split;
+
+// Chunks per CTA of a streaming pass: the override if set (at most C), else
+// the policy's choice.
+inline int split_group(int policy, int C) {
+  const int g = g_split.group.load(std::memory_order_relaxed);
+  if (g <= 0) return policy;
+  return g < C ? g : C;
+}
+
 // Chunking policy: chunks of at most 32 KB (so that one chunk fits a
 // shared-memory stage); for small batches more chunks so the grid fills the
 // GPU (at least ~16 CTAs per SM on 152 SMs), but no chunk below 2048
 // elements.  esize is the logit element size; sizing with esize = 4 gives
-// the most chunks, which is what the workspace is sized for.
+// the most chunks, which is what the workspace is sized for.  An override
+// of the chunk length is clamped to [ceil(V / 256), 32 KB of elements] (at
+// most 256 chunks: the draw's select runs one chunk per thread; at most
+// 2^14 elements: its per-chunk fixed-point sums stay below 2^62).
 inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
   Chunking c;
   long long rows = static_cast<long long>(B) * (rows_per_b > 0 ? rows_per_b : 1);
@@ -287,6 +320,13 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
   if (C > 256) C = 256;
   if (C < 1) C = 1;
   long long CH = (V + C - 1) / C;
+  const int ov = g_split.chunk.load(std::memory_order_relaxed);
+  if (ov > 0) {
+    const long long lo = (V + 255) / 256;
+    CH = ov;
+    if (CH < lo) CH = lo;
+    if (CH > max_ch) CH = max_ch;
+  }
   CH = (CH + 7) / 8 * 8;
   C = (V + CH - 1) / CH;
   c.C = static_cast<int>(C);
@@ -335,9 +375,9 @@ inline TreeLayout make_tree_layout(int B, int N, int V, int esize = 4) {
   size_t off = 0;
   L.err = off;                      off = align256(off + 16);
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * L.ch.C);
-  // per tree V + 32768 slots (the walk's thread ranges, padded) when rows
-  // are long enough for the cache to pay; none otherwise
-  L.cache_stride = V >= kTreeCacheMinV ? static_cast<size_t>(V) + 32768 : 0;
+  // per tree V + kTreeCachePad slots (the walk's thread ranges, padded)
+  // when rows are long enough for the cache to pay; none otherwise
+  L.cache_stride = V >= kTreeCacheMinV ? static_cast<size_t>(V) + kTreeCachePad : 0;
   L.cache = off;                    off = align256(off + sizeof(float) * 4 * B * L.cache_stride);
   L.total = off;
   return L;

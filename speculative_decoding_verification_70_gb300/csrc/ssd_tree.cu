@@ -47,7 +47,6 @@
 namespace ssd {
 namespace {
 
-constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr float kFix = 281474976710656.0f;  // 2^48
 
@@ -389,7 +388,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   bool ready = false;                       // acc/comp/last hold a pass for (rho, W)
   float acc = 0.f, comp = 0.f;
   int last = -1;
-  const int nt = cs * kTreeThreads;         // E * nt <= V + 8 nt <= V + 32768
+  const int nt = cs * kTreeThreads;         // E * nt <= V + 8 nt <= V + kTreeCachePad
   const bool use_cache = p.cache_stride > 0;
   float4* cache = use_cache ? p.cache + static_cast<int64_t>(b) * p.cache_stride + g : nullptr;
   int cached = -1;                          // the node whose exponentials the cache holds
@@ -537,9 +536,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
 // SSD_TREE_MAX_CLUSTER.  Oversubscribing balances the trees' unequal pass
 // counts: measured walk times at B = 64 / 128 / 512 were 0.218 / 0.403 /
 // 1.107 ms with 2 per SM, 0.177 / 0.332 / 0.923 ms with 8.
-#ifndef SSD_TREE_MAX_CLUSTER
-#define SSD_TREE_MAX_CLUSTER 8
-#endif
+static_assert(8 * SSD_TREE_MAX_CLUSTER * kTreeThreads <= kTreeCachePad,
+              "the tree cache rows must cover the largest cluster's thread ranges");
 #ifndef SSD_TREE_CTAS_PER_SM
 #define SSD_TREE_CTAS_PER_SM 8
 #endif

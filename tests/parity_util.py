@@ -3,6 +3,9 @@ greedy tokens and accept lengths bit-exact; probabilities within 1e-5
 absolute; sampled decisions identical unless the uniform lies within 1e-6 of
 the decision boundary (p/q for an acceptance, a CDF boundary for a draw);
 top-f and cache results bit-exact."""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 import oracle
@@ -20,6 +23,47 @@ def oracle_rows(inp, bs):
     sel = lambda k: inp[k][bs].cpu()
     return oracle.verify_recover(sel("Z"), sel("D"), sel("x"), sel("T"), sel("u_acc"),
                                  sel("u_smp"))
+
+
+def host_threads():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _slices(B, per_task):
+    return [(b0, min(B, b0 + per_task)) for b0 in range(0, B, per_task)]
+
+
+def oracle_verify_host(cpu, per_task=8, threads=None):
+    """The oracle's verify_recover on every batch row of host tensors `cpu`
+    (Z, D, x, T, u_acc, u_smp), spread over the host cores: the oracle is a
+    C library called through ctypes, which releases the GIL, so each thread
+    runs the oracle on its own slice of rows."""
+    B = cpu["Z"].shape[0]
+    oracle.build()  # compile (if needed) once, before the threads load it
+
+    def one(sl):
+        b0, b1 = sl
+        return oracle.verify_recover(cpu["Z"][b0:b1], cpu["D"][b0:b1], cpu["x"][b0:b1],
+                                     cpu["T"][b0:b1], cpu["u_acc"][b0:b1], cpu["u_smp"][b0:b1])
+    with ThreadPoolExecutor(threads or host_threads()) as ex:
+        parts = list(ex.map(one, _slices(B, per_task)))
+    return {key: np.concatenate([q[key] for q in parts]) for key in parts[0]}
+
+
+def oracle_forks_host(D, f, mask, per_task=8, threads=None):
+    """oracle.forked_topf over every batch row of host tensors, threaded."""
+    B = D.shape[0]
+    oracle.build()
+
+    def one(sl):
+        b0, b1 = sl
+        return oracle.forked_topf(D[b0:b1], f, mask[b0:b1])
+    with ThreadPoolExecutor(threads or host_threads()) as ex:
+        parts = list(ex.map(one, _slices(B, per_task)))
+    return {key: np.concatenate([q[key] for q in parts]) for key in parts[0]}
 
 
 def draw_weights(Zrow, Drow, T, n, k):

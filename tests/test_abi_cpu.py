@@ -15,6 +15,20 @@ PKG = os.path.join(ROOT, "speculative_decoding_verification_70_gb300")
 HEADER = os.path.join(ROOT, "include", "ssd.h")
 
 
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+# The argument-check tests pass made-up device addresses that only the host
+# checks keep from reaching a kernel; they run where no GPU is present, so a
+# regressed check can never launch a kernel on such an address.
+needs_no_gpu = pytest.mark.skipif(not _no_gpu(), reason="fake device pointers: CPU-only host")
+
+
 @pytest.fixture(scope="module")
 def lib():
     from speculative_decoding_verification_70_gb300 import build
@@ -86,6 +100,7 @@ def _call_verify(lib, **kw):
                           args["wsb"], None)
 
 
+@needs_no_gpu
 def test_verify_rejects_bad_arguments_on_host(lib):
     INVALID, DTYPE, WS = 1, 2, 6
     assert _call_verify(lib, Z=None) == INVALID
@@ -103,6 +118,7 @@ def test_verify_rejects_bad_arguments_on_host(lib):
     assert _call_verify(lib, wsb=16) == WS
 
 
+@needs_no_gpu
 def test_fork_and_cache_reject_bad_arguments_on_host(lib):
     P = 1 << 20
     # f >= V, f > 16, M > 64
@@ -157,6 +173,7 @@ def test_oracle_and_cuda_path_share_no_code():
             assert "ssd.h" not in text, f
 
 
+@needs_no_gpu
 def test_next_rows_reject_bad_arguments_on_host(lib):
     """Draft-side sampling, the drafted verify, the filtered verify and the
     fan-out calls refuse bad arguments before touching CUDA."""
@@ -208,6 +225,7 @@ def test_next_rows_reject_bad_arguments_on_host(lib):
                                           None) == INVALID
 
 
+@needs_no_gpu
 def test_tree_rejects_bad_arguments_on_host(lib):
     """ssd_verify_tree refuses bad arguments before touching CUDA."""
     INVALID, DTYPE, WS = 1, 2, 6
@@ -240,3 +258,21 @@ def test_tree_rejects_bad_arguments_on_host(lib):
     n = lib.ssd_tree_workspace_bytes(2, 5, 1000)
     assert n > 0 and n % 256 == 0
     assert lib.ssd_tree_workspace_bytes(4, 5, 1000) > n
+
+
+def test_split_override_is_checked_and_restored(lib):
+    """ssd_set_split refuses negative values, changes the workspace layout
+    while set, and 0 restores the policy."""
+    assert lib.ssd_set_split(-1, 0) == 1
+    assert lib.ssd_set_split(0, -1) == 1
+    n0 = lib.ssd_workspace_bytes(8, 7, 151936, 4)
+    try:
+        assert lib.ssd_set_split(600, 0) == 0    # more chunks than the policy's 19
+        assert lib.ssd_workspace_bytes(8, 7, 151936, 4) > n0
+        assert lib.ssd_set_split(1, 0) == 0      # clamped to ceil(V / 256): 256 chunks
+        n256 = lib.ssd_workspace_bytes(8, 7, 151936, 4)
+        assert lib.ssd_set_split(100000, 0) == 0  # clamped to 32 KB of fp32 logits
+        assert lib.ssd_workspace_bytes(8, 7, 151936, 4) <= n0 < n256
+    finally:
+        assert lib.ssd_set_split(0, 0) == 0
+    assert lib.ssd_workspace_bytes(8, 7, 151936, 4) == n0

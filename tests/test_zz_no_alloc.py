@@ -3,17 +3,18 @@ memory (for example code running inside a framework that owns every
 allocation).  It uses a static device array as its scratch instead of a
 caller-supplied workspace.  These tests call it through the C ABI and check
 that it returns exactly what ssd_verify returns, on two calls in a row (the
-array keeps the previous call's contents), and that sizes beyond the array
-are refused on the host.
+array keeps the previous call's contents), that its results agree with the
+oracle under the parity rules (it runs a one-stream schedule of its own),
+and that sizes beyond the array are refused on the host.
 
 This file is collected last so that a failure here leaves every other test
 already run.
 """
-import ctypes
-
+import numpy as np
 import pytest
 import torch
 
+from parity_util import Report, compare_verify, oracle_rows
 from speculative_decoding_verification_70_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -55,13 +56,23 @@ def test_noalloc_matches_verify_twice(gpu_lib):
         both = ref["accept_len"] >= 0
         assert torch.allclose(got["p_at_x"][both], ref["p_at_x"][both], atol=1e-5, rtol=0)
         assert torch.allclose(got["q_at_x"][both], ref["q_at_x"][both], atol=1e-5, rtol=0)
+        # and directly against the oracle on the same rows
+        bs = np.arange(w.B)
+        rep = compare_verify(inp, got, bs, oracle_rows(inp, bs), Report())
+        assert not rep.failures, rep.failures[:3]
+        assert rep.sampled_mismatch == 0, rep.summary()
 
 
 def test_noalloc_refuses_sizes_beyond_the_array(gpu_lib):
     lib = gpu_lib.load_library()
     B, k, V = 4096, 7, 151936
     assert gpu_lib.workspace_bytes(B, k, V, 0) > SCRATCH_BYTES
-    P = ctypes.c_void_p(1 << 20)  # never dereferenced: the host check refuses first
-    st = lib.ssd_verify_noalloc(P, (k + 1) * V, P, k * V, 0, B, k, V, P, P, P, P, None, None,
-                                None, None, None)
+    # no device pointer at all: the size check refuses first, and were it
+    # ever to pass, the null-pointer check would refuse before any launch
+    st = lib.ssd_verify_noalloc(None, (k + 1) * V, None, k * V, 0, B, k, V, None, None, None,
+                                None, None, None, None, None, None)
     assert st == SSD_ERR_WORKSPACE
+    assert lib.ssd_verify_noalloc(None, 3 * 1000, None, 2 * 1000, 0, 2, 2, 1000, None, None, None,
+                                  None, None, None, None, None, None) == 1  # null pointers
+    assert lib.ssd_verify_noalloc(None, 0, None, 0, 0, 0, 2, 1000, None, None, None, None, None,
+                                  None, None, None, None) == 1              # B = 0
