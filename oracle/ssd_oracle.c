@@ -216,34 +216,47 @@ int oracle_softmax_temp(const void *logits, int dtype, int rows, int64_t V,
     return ORACLE_OK;
 }
 
-/* Top-k / top-p filter of one row's probabilities p (reading R9), in
- * place: the first K tokens in (z descending, index ascending) order, then
- * the shortest prefix of them holding >= top_p of their mass, renormalised;
- * every other token gets 0.  `sel` is scratch for K indices and `taken` for
- * V flags. */
-static void filter_topk_topp(const double *z, double *p, int64_t V, int K, double top_p,
-                             int64_t *sel, char *taken)
+/* One token in the order of readings R6 / R9. */
+typedef struct {
+    double z;
+    int64_t v;
+} ranked_t;
+
+/* Logit descending, then index ascending (qsort comparator). */
+static int rank_cmp(const void *a, const void *b)
 {
-    memset(taken, 0, (size_t)V);
-    int n = 0;
-    for (; n < K; ++n) {
-        int64_t best = -1;
-        for (int64_t v = 0; v < V; ++v)
-            if (!taken[v] && (best < 0 || z[v] > z[best]))
-                best = v;
-        if (best < 0)
-            break;
-        taken[best] = 1;
-        sel[n] = best;
+    const ranked_t *x = (const ranked_t *)a, *y = (const ranked_t *)b;
+    if (x->z > y->z)
+        return -1;
+    if (x->z < y->z)
+        return 1;
+    return (x->v < y->v) ? -1 : (x->v > y->v);
+}
+
+/* Top-k / top-p filter of one row's probabilities p (reading R9), in
+ * place: all V tokens ordered by (z descending, index ascending) -- a sort
+ * serves as the step -- then the first K of them, then the shortest prefix
+ * of those holding >= top_p of their mass, renormalised; every other token
+ * gets 0.  `ord` is scratch for V entries and `taken` for V flags. */
+static void filter_topk_topp(const double *z, double *p, int64_t V, int K, double top_p,
+                             ranked_t *ord, char *taken)
+{
+    if (V < 1)
+        return;
+    for (int64_t v = 0; v < V; ++v) {
+        ord[v].z = z[v];
+        ord[v].v = v;
     }
+    qsort(ord, (size_t)V, sizeof(ranked_t), rank_cmp);
+    const int64_t n = (int64_t)K < V ? (int64_t)K : V;
     double mass = 0.0;
-    for (int j = 0; j < n; ++j)
-        mass += p[sel[j]];
-    int keep = n;
+    for (int64_t j = 0; j < n; ++j)
+        mass += p[ord[j].v];
+    int64_t keep = n;
     if (top_p < 1.0) {
         double c = 0.0;
-        for (int j = 0; j < n; ++j) {
-            c += p[sel[j]];
+        for (int64_t j = 0; j < n; ++j) {
+            c += p[ord[j].v];
             if (c >= top_p * mass) {
                 keep = j + 1;
                 break;
@@ -251,11 +264,12 @@ static void filter_topk_topp(const double *z, double *p, int64_t V, int K, doubl
         }
     }
     double kept = 0.0;
-    for (int j = 0; j < keep; ++j)
-        kept += p[sel[j]];
-    memset(taken, 0, (size_t)V);
-    for (int j = 0; j < keep; ++j)
-        taken[sel[j]] = 1;
+    for (int64_t j = 0; j < keep; ++j)
+        kept += p[ord[j].v];
+    for (int64_t v = 0; v < V; ++v)
+        taken[v] = 0;
+    for (int64_t j = 0; j < keep; ++j)
+        taken[ord[j].v] = 1;
     for (int64_t v = 0; v < V; ++v)
         p[v] = taken[v] ? p[v] / kept : 0.0;
 }
@@ -291,10 +305,10 @@ static int verify_core(const void *Z, int64_t z_bstride, const void *D, int64_t 
     double *q = (double *)malloc((size_t)V * sizeof(double));
     double *w = (double *)malloc((size_t)V * sizeof(double));
     int *accepted = (int *)malloc((size_t)k * sizeof(int));
-    int64_t *sel = (int64_t *)malloc((size_t)(K > 0 ? K : 1) * sizeof(int64_t));
+    ranked_t *ord = (ranked_t *)malloc((size_t)(K > 0 ? V : 1) * sizeof(ranked_t));
     char *taken = (char *)malloc((size_t)V);
-    if (!zrow || !drow || !p || !q || !w || !accepted || !sel || !taken) {
-        free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(sel);
+    if (!zrow || !drow || !p || !q || !w || !accepted || !ord || !taken) {
+        free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(ord);
         free(taken);
         return ORACLE_NO_MEMORY;
     }
@@ -355,8 +369,8 @@ static int verify_core(const void *Z, int64_t z_bstride, const void *D, int64_t 
                 softmax_temp(zrow, V, t, p, &m, &S);
                 softmax_temp(drow, V, t, q, &m, &S);
                 if (K > 0) {
-                    filter_topk_topp(zrow, p, V, K, pb, sel, taken);
-                    filter_topk_topp(drow, q, V, K, pb, sel, taken);
+                    filter_topk_topp(zrow, p, V, K, pb, ord, taken);
+                    filter_topk_topp(drow, q, V, K, pb, ord, taken);
                 }
                 pi = p[xi];
                 qi = q[xi];
@@ -389,12 +403,12 @@ static int verify_core(const void *Z, int64_t z_bstride, const void *D, int64_t 
             double m, S;
             softmax_temp(zrow, V, t, p, &m, &S);
             if (K > 0)
-                filter_topk_topp(zrow, p, V, K, pb, sel, taken);
+                filter_topk_topp(zrow, p, V, K, pb, ord, taken);
             if (n < k) {
                 load_row(D, dtype, (int64_t)b * d_bstride + (int64_t)n * V, V, drow);
                 softmax_temp(drow, V, t, q, &m, &S);
                 if (K > 0)
-                    filter_topk_topp(drow, q, V, K, pb, sel, taken);
+                    filter_topk_topp(drow, q, V, K, pb, ord, taken);
                 double total = 0.0;
                 for (int64_t v = 0; v < V; ++v) {
                     double d = p[v] - q[v];
@@ -417,7 +431,7 @@ static int verify_core(const void *Z, int64_t z_bstride, const void *D, int64_t 
         out[n] = (int32_t)tok;
     }
 
-    free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(sel); free(taken);
+    free(zrow); free(drow); free(p); free(q); free(w); free(accepted); free(ord); free(taken);
     return ORACLE_OK;
 }
 
