@@ -397,9 +397,20 @@ def topk_verify(ssd, w, inp, dev, K=32, top_p=0.9, reps=50):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     nbytes = w.B * (2 * w.k + 1) * w.V * 4
-    return {"K": K, "top_p": top_p, "ms": round(ms, 4),
-            "rows_per_s": round(w.B / (ms / 1e3), 1),
-            "stream_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    res = {"K": K, "top_p": top_p, "ms": round(ms, 4),
+           "rows_per_s": round(w.B / (ms / 1e3), 1),
+           "stream_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+           "path": "per-chunk top-K lists" if min(K, w.V) <= 32 else
+                   "threshold on the token order (histogram, band, exact cut)"}
+    if min(K, w.V) > 32:
+        ssd.profile_begin(16 * reps)
+        for _ in range(reps):
+            call()
+        torch.cuda.synchronize()
+        prof = ssd.profile_end()
+        res["ms_by_kernel"] = {k: round(v["total_ms"] / max(1, v["timed"]), 4)
+                               for k, v in prof.items()}
+    return res
 
 
 def tree_verify(ssd, W, dev, reps=20):
@@ -624,6 +635,8 @@ def gpu_arm(args):
         line["latency_b1"] = b1_latency(ssd, W, dev)
         line["draft_pipeline"] = draft_pipeline(ssd, w, inp, dev)
         line["topk_verify"] = topk_verify(ssd, w, inp, dev)
+        line["topk_verify_k50_p09"] = topk_verify(ssd, w, inp, dev, K=50, top_p=0.9)
+        line["topp_verify_full_vocab_p09"] = topk_verify(ssd, w, inp, dev, K=w.V, top_p=0.9)
         line["tree_verify"] = tree_verify(ssd, W, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(inp, w)
@@ -753,6 +766,7 @@ def main():
                     help="one of the next rows' measurements alone (profiling captures; "
                          "B from --batch, timed calls from --steps)")
     ap.add_argument("--topk-k", type=int, default=32, help="K of --only topk")
+    ap.add_argument("--top-p", type=float, default=0.9, help="top_p of --only topk")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
@@ -784,7 +798,7 @@ def only_arm(args):
         w = W.workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
         inp = W.make_inputs(w, device="cuda", seed=W.default_seed(WORKLOAD))
         if args.only == "topk":
-            res = topk_verify(ssd, w, inp, "cuda", K=args.topk_k, reps=reps)
+            res = topk_verify(ssd, w, inp, "cuda", K=args.topk_k, top_p=args.top_p, reps=reps)
         else:
             res = draft_pipeline(ssd, w, inp, "cuda", reps=reps)
     print(json.dumps(res), flush=True)

@@ -78,6 +78,8 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 #define SSD_DEVERR_BAD_TOKEN 0x4       /* draft token outside [0, V): -2  */
 #define SSD_DEVERR_CACHE_FULL 0x8      /* insert found no free slot       */
 #define SSD_DEVERR_TIMEOUT 0x10        /* reserved: a bounded device wait ran out */
+#define SSD_DEVERR_FILTER_BAND 0x20    /* a filtered row's cut fell outside its collected
+                                          bins; it was cut by bisection (results exact) */
 
 /* Sentinels written to accept_len. */
 #define SSD_ROW_INVALID (-1)
@@ -336,14 +338,29 @@ SSD_API ssd_status ssd_verify_drafted(const void *Z, int64_t z_bstride, const vo
  * logit descending, index ascending; keep the first K; keep the shortest
  * prefix of those holding >= top_p[b] of their probability mass;
  * renormalise), and acceptance, the residual and the bonus draw use the
- * filtered p and q.  Greedy rows (T == 0) are unaffected.  One pass over the
- * 2k+1 rows keeps per-chunk top-K lists (no exponentials); the rest works
- * on at most K candidates per row, in extended precision.
- *   K        : 1 <= K <= 32 (and K <= V).
- *   top_p    : [B] fp32 device array, or NULL for 1 (no cut).
+ * filtered p and q.  Greedy rows (T == 0) are unaffected.
+ *   K        : K >= 1; K >= V keeps every token (top-p over the whole
+ *              vocabulary).  min(K, V) <= 32: one pass over the 2k+1 rows
+ *              keeps per-chunk top-K lists (no exponentials) and the rest
+ *              works on at most K candidates per row.  Larger K: each row's
+ *              kept set is found as a threshold on the token order (a row
+ *              maximum pass, a histogram pass of x = (m - z) log2(e) / T in
+ *              1/16 steps, a pass that sums the exact mass above the bins
+ *              holding the cuts and collects those bins' tokens, an exact
+ *              cut on them; see ssd_filter.cu), three reads of the rows in
+ *              all.  A row whose cut bins hold more than 2048 tokens (e.g.
+ *              thousands of equal logits) is cut by bisection on the token
+ *              order, slower but exact.  V <= 2^21 on this path.
+ *   top_p    : [B] fp32 device array, or NULL for 1 (no cut).  Values >= 1
+ *              or NaN cut nothing.
  *   other arguments and results as ssd_verify (the draft tokens x must have
  *   been drawn from the filtered draft distribution for exactness).
- *   ws       : ssd_topk_workspace_bytes(B, k, V, K) bytes.
+ *   ws       : ssd_topk_workspace_bytes(B, k, V, K) bytes (0 for invalid
+ *              sizes).
+ * Mass sums and the top-p cut are exact to ~1e-12 relative (extended
+ * precision exponentials, fixed-point sums), so a cut differs from an exact
+ * computation only when the cumulative mass at the cut lies that close to
+ * top_p times the kept tokens' mass.
  */
 SSD_API size_t ssd_topk_workspace_bytes(int B, int k, int V, int K);
 SSD_API ssd_status ssd_verify_topk(const void *Z, int64_t z_bstride, const void *D,

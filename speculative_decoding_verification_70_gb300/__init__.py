@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     DEVERR_BAD_TEMPERATURE,
     DEVERR_BAD_TOKEN,
     DEVERR_CACHE_FULL,
+    DEVERR_FILTER_BAND,
     SIGNATURES,
     SSDError,
     SpecCache,

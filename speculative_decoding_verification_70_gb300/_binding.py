@@ -25,6 +25,7 @@ DEVERR_BAD_TEMPERATURE = 0x1
 DEVERR_BAD_LOGITS = 0x2
 DEVERR_BAD_TOKEN = 0x4
 DEVERR_CACHE_FULL = 0x8
+DEVERR_FILTER_BAND = 0x20
 
 # (name, restype, argtypes)
 _P = ctypes.c_void_p
@@ -431,7 +432,8 @@ def ssd_verify_topk(Z: torch.Tensor, D: torch.Tensor, x: torch.Tensor, T: torch.
                     u_smp: Optional[torch.Tensor] = None, *, ws: Optional[torch.Tensor] = None,
                     out: Optional[dict] = None, stream=None) -> Dict[str, torch.Tensor]:
     """ssd_verify over top-K / top-p filtered target and draft distributions
-    (K <= 32; top_p [B] float32 or None)."""
+    (any K >= 1, K >= V for top-p over the whole vocabulary; top_p [B]
+    float32 or None)."""
     lib = load_library()
     B, kp1, V = Z.shape
     k = kp1 - 1

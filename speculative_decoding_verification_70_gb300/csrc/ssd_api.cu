@@ -38,6 +38,15 @@ cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bo
 cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_selftest_exp2(const float* xh, const float* xl, double* out, int n, cudaStream_t s);
 
+cudaError_t launch_filt_rowinit(const FiltParams& p, cudaStream_t s);
+cudaError_t launch_filt_hist(const FiltParams& p, bool vec, cudaStream_t s);
+cudaError_t launch_filt_band(const FiltParams& p, cudaStream_t s);
+cudaError_t launch_filt_collect(const FiltParams& p, bool vec, cudaStream_t s);
+cudaError_t launch_filt_cut(const FiltParams& p, bool vec, cudaStream_t s);
+cudaError_t launch_filt_accept(const FiltParams& p, cudaStream_t s);
+cudaError_t launch_filt_mass(const FiltParams& p, bool vec, cudaStream_t s);
+cudaError_t launch_filt_select(const FiltParams& p, bool vec, cudaStream_t s);
+
 cudaError_t launch_cache_claim(const CacheView& c, const InsertArgs& a, cudaStream_t s);
 cudaError_t launch_cache_write(const CacheView& c, const InsertArgs& a, cudaStream_t s);
 cudaError_t launch_cache_lookup(const CacheView& c, const LookupArgs& a, cudaStream_t s);
@@ -704,9 +713,100 @@ ssd_status ssd_verify_tree(const void* Z, int64_t z_bstride, const void* D, int6
 }
 
 size_t ssd_topk_workspace_bytes(int B, int k, int V, int K) {
-  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || K < 1 || K > kMaxTopK || K > V) return 0;
-  return make_topk_layout(B, k, V, K).total;
+  if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || K < 1) return 0;
+  const int Ke = K < V ? K : V;
+  if (Ke <= kMaxTopK) return make_topk_layout(B, k, V, Ke).total;
+  if (V > kFiltMaxV) return 0;
+  return make_filt_layout(B, k, V).total;
 }
+
+namespace {
+
+// ssd_verify_topk beyond the in-register lists (K > kMaxTopK, top-p over
+// the whole vocabulary): threshold keys per row found from histograms, see
+// ssd_filter.cu.
+ssd_status run_verify_filtered(const void* Z, int64_t zb, const void* D, int64_t db,
+                               ssd_dtype dtype, int B, int k, int V, const int32_t* x,
+                               const float* T, int K, const float* top_p, const float* u_acc,
+                               int32_t* accept_len, float* p_at_x, float* q_at_x,
+                               const float* u_smp, int32_t* out_tok, void* ws, size_t ws_bytes,
+                               cudaStream_t st) {
+  if (V > kFiltMaxV) return SSD_ERR_INVALID_ARG;
+  const FiltLayout L = make_filt_layout(B, k, V, static_cast<int>(esize(dtype)));
+  if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
+  const bool vec = vec_ok(Z, zb, V, dtype) && vec_ok(D, db, V, dtype);
+  const int dt = dtype == SSD_BF16 ? 1 : 0;
+  // 1. row maxima, argmax and NaN flags of the 2k+1 rows (no exponentials)
+  StatsParams sp;
+  memset(&sp, 0, sizeof sp);
+  sp.Z = Z; sp.zb = zb; sp.Pz = k + 1;
+  sp.D = D; sp.db = db; sp.Pds = k; sp.Pdf = 0;
+  sp.T = nullptr;
+  sp.V = V; sp.C = L.ch.C; sp.CH = L.ch.CH; sp.R = L.R; sp.Rp = L.R;
+  sp.part = reinterpret_cast<PartStat*>(wsp(ws, L.part));
+  sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
+  cudaError_t e = run_stats(sp, B, dt, vec, st);
+  if (e != cudaSuccess) return SSD_ERR_CUDA;
+  FiltParams fp;
+  memset(&fp, 0, sizeof fp);
+  fp.Z = Z; fp.zb = zb; fp.D = D; fp.db = db; fp.dtype = dt;
+  fp.B = B; fp.k = k; fp.V = V; fp.C = L.ch.C; fp.CH = L.ch.CH; fp.E = L.ch.E; fp.R = L.R;
+  fp.K = K;
+  fp.total_mode = K >= V ? 1 : 0;
+  fp.G = 1;
+  while (fp.G < fp.C &&
+         static_cast<long long>(B) * L.R * ((fp.C + 2 * fp.G - 1) / (2 * fp.G)) >= 2432)
+    fp.G *= 2;
+  fp.G = split_group(fp.G, fp.C);
+  if (static_cast<long long>(fp.G) * fp.CH > (1 << 19)) fp.G = (1 << 19) / fp.CH;  // 32-bit bin sums
+  fp.T = T; fp.top_p = top_p; fp.x = x; fp.u_acc = u_acc; fp.u_smp = u_smp;
+  fp.accept_len = accept_len; fp.p_at_x = p_at_x; fp.q_at_x = q_at_x; fp.out_tok = out_tok;
+  fp.part = sp.part;
+  fp.rows = reinterpret_cast<FiltRow*>(wsp(ws, L.rows));
+  fp.hcnt = reinterpret_cast<unsigned*>(wsp(ws, L.hcnt));
+  fp.hmass = reinterpret_cast<unsigned long long*>(wsp(ws, L.hmass));
+  fp.cand = reinterpret_cast<unsigned long long*>(wsp(ws, L.cand));
+  fp.bstate = reinterpret_cast<BState*>(wsp(ws, L.bstate));
+  fp.rmass = reinterpret_cast<long long*>(wsp(ws, L.rmass));
+  fp.err = sp.err;
+  {
+    ProfScope ps("filt_rowinit", st);
+    e = launch_filt_rowinit(fp, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("filt_hist", st);
+    e = launch_filt_hist(fp, vec, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("filt_band", st);
+    e = launch_filt_band(fp, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("filt_collect", st);
+    e = launch_filt_collect(fp, vec, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("filt_cut", st);
+    e = launch_filt_cut(fp, vec, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("filt_accept", st);
+    e = launch_filt_accept(fp, st);
+  }
+  if (e == cudaSuccess && u_smp && out_tok) {
+    {
+      ProfScope ps("filt_mass", st);
+      e = launch_filt_mass(fp, vec, st);
+    }
+    if (e == cudaSuccess) {
+      ProfScope ps("filt_select", st);
+      e = launch_filt_select(fp, vec, st);
+    }
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
 
 ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int64_t d_bstride,
                            ssd_dtype dtype, int B, int k, int V, const int32_t* x, const float* T,
@@ -717,21 +817,26 @@ ssd_status ssd_verify_topk(const void* Z, int64_t z_bstride, const void* D, int6
   if (!dtype_ok(dtype)) return SSD_ERR_UNSUPPORTED_DTYPE;
   if (!Z || !D || !x || !T || !u_acc || !accept_len || !ws) return SSD_ERR_INVALID_ARG;
   if (B < 1 || k < 1 || k > SSD_MAX_K || V < 2 || V > (1 << 28)) return SSD_ERR_INVALID_ARG;
-  if (K < 1 || K > kMaxTopK || K > V) return SSD_ERR_INVALID_ARG;
+  if (K < 1) return SSD_ERR_INVALID_ARG;
   if ((p_at_x == nullptr) != (q_at_x == nullptr)) return SSD_ERR_INVALID_ARG;
   if (u_smp && !out_tok) return SSD_ERR_INVALID_ARG;
   if (z_bstride < static_cast<int64_t>(k + 1) * V || d_bstride < static_cast<int64_t>(k) * V)
     return SSD_ERR_INVALID_ARG;
   if (!aligned(Z, esize(dtype)) || !aligned(D, esize(dtype)) || !aligned(ws, 256))
     return SSD_ERR_INVALID_ARG;
-  const TopkLayout L = make_topk_layout(B, k, V, K, static_cast<int>(esize(dtype)));
+  const int Ke = K < V ? K : V;  // more than V tokens: all of them
+  if (Ke > kMaxTopK)
+    return run_verify_filtered(Z, z_bstride, D, d_bstride, dtype, B, k, V, x, T, K, top_p,
+                               u_acc, accept_len, p_at_x, q_at_x, u_smp, out_tok, ws, ws_bytes,
+                               S(stream));
+  const TopkLayout L = make_topk_layout(B, k, V, Ke, static_cast<int>(esize(dtype)));
   if (ws_bytes < L.total) return SSD_ERR_WORKSPACE;
   const bool vec = vec_ok(Z, z_bstride, V, dtype) && vec_ok(D, d_bstride, V, dtype);
   TopkParams tp;
   memset(&tp, 0, sizeof tp);
   tp.Z = Z; tp.zb = z_bstride; tp.D = D; tp.db = d_bstride;
   tp.dtype = dtype == SSD_BF16 ? 1 : 0;
-  tp.B = B; tp.k = k; tp.V = V; tp.C = L.ch.C; tp.CH = L.ch.CH; tp.R = L.R; tp.K = K;
+  tp.B = B; tp.k = k; tp.V = V; tp.C = L.ch.C; tp.CH = L.ch.CH; tp.R = L.R; tp.K = Ke;
   // chunk groups up to a whole row per CTA while the grid keeps ~16 CTAs per
   // SM: the end-of-CTA selection (K rounds) is then paid once per row
   tp.G = 1;

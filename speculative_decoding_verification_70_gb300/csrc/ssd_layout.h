@@ -209,6 +209,67 @@ struct TopkParams {
 
 inline TopkLayout make_topk_layout(int B, int k, int V, int K, int esize = 4);
 
+// Filtered verify beyond the in-register lists: K > kMaxTopK (any K up to V)
+// and top-p over the whole vocabulary.  Each logit row of a T > 0 batch row
+// gets a histogram of x = (m - z) log2(e) / T in kFiltBinsPerUnit bins per
+// unit (x >= kFiltBins / kFiltBinsPerUnit in the last bin), a band of bins
+// that must hold the cut, and the order keys of the band's tokens.
+constexpr int kFiltBins = 1024;
+constexpr int kFiltBinsPerUnit = 16;
+constexpr int kFiltCand = 2048;       // band tokens kept per row (more: bisection fallback)
+constexpr int kFiltMaxV = 1 << 21;    // fixed-point sums of 2^42 units stay below 2^63
+
+// One filtered logit row.  Tokens are ordered by the 64-bit key
+// (order-preserving bits of z) << 32 | ~index: key descending is logit
+// descending, then index ascending.  Kept tokens are those with key >= thr.
+struct FiltRow {
+  unsigned long long thr;    // key of the last kept token (0 keeps every token)
+  unsigned long long above;  // 2^42 fixed point: exact mass of the tokens in bins < band_lo
+  unsigned long long total;  // 2^42 fixed point: exact mass of the row (K >= V only)
+  double P;                  // kept mass, sum of 2^((z - m) c) over kept tokens
+  float m;                   // row maximum
+  float c_hi, c_lo;          // log2(e) / T as a float pair
+  int argmax;                // lowest index attaining m
+  int flags;                 // bit 0: NaN; bit 1: invalid at T > 0; bit 2: T > 0 (filtered)
+  int band_lo, band_hi;      // bins whose tokens are collected
+  int cnt_before;            // tokens in bins < band_lo
+  int n_cand;                // band tokens seen (above kFiltCand: overflow)
+  int keep;                  // kept tokens
+  int pad;
+};
+
+struct FiltLayout {
+  size_t err, part, rows, hcnt, hmass, cand, bstate, rmass, total;
+  int R;          // rows per batch row: k+1 target, k draft
+  Chunking ch;
+};
+
+struct FiltParams {
+  const void* Z; int64_t zb;
+  const void* D; int64_t db;
+  int dtype;           // 0 f32, 1 bf16
+  int B, k, V, C, CH, E, R, K, G;
+  int b0;              // first batch row of this launch
+  int total_mode;      // K >= V: the histogram pass also sums each row's exact mass
+  const float* T;
+  const float* top_p;  // [B] or null (1)
+  const int32_t* x;
+  const float* u_acc;
+  const float* u_smp;  // may be null (no draw)
+  int32_t* accept_len;
+  float* p_at_x;
+  float* q_at_x;
+  int32_t* out_tok;
+  PartStat* part;                 // [B][R][C]
+  FiltRow* rows;                  // [B][R]
+  unsigned* hcnt;                 // [B][R][kFiltBins]
+  unsigned long long* hmass;      // [B][R][kFiltBins] bin-scaled fixed point
+  unsigned long long* cand;       // [B][R][kFiltCand] order keys
+  BState* bstate;                 // [B]
+  long long* rmass;               // [B][C]: the draw's chunk masses (2^60 units)
+  int* err;
+};
+
 // Merge of the draft-side sampling pass: one warp per (b, draft row).
 struct DraftParams {
   int B, V, C, Rp, Pz, Pf, row0, rows;
@@ -392,6 +453,25 @@ inline TopkLayout make_topk_layout(int B, int k, int V, int K, int esize) {
   L.err = off;                      off = align256(off + 16);
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
   L.lists = off;                    off = align256(off + sizeof(TopEntry) * B * L.R * C * K);
+  L.total = off;
+  return L;
+}
+
+inline FiltLayout make_filt_layout(int B, int k, int V, int esize = 4) {
+  FiltLayout L;
+  L.R = 2 * k + 1;
+  L.ch = make_chunking(B, 2 * (k + 1), V, esize);
+  const size_t C = static_cast<size_t>(L.ch.C);
+  const size_t rows = static_cast<size_t>(B) * L.R;
+  size_t off = 0;
+  L.err = off;                      off = align256(off + 16);
+  L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
+  L.rows = off;                     off = align256(off + sizeof(FiltRow) * rows);
+  L.hcnt = off;                     off = align256(off + sizeof(unsigned) * rows * kFiltBins);
+  L.hmass = off;                    off = align256(off + sizeof(unsigned long long) * rows * kFiltBins);
+  L.cand = off;                     off = align256(off + sizeof(unsigned long long) * rows * kFiltCand);
+  L.bstate = off;                   off = align256(off + sizeof(BState) * B);
+  L.rmass = off;                    off = align256(off + sizeof(long long) * B * C);
   L.total = off;
   return L;
 }

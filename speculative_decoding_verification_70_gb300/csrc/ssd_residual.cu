@@ -32,15 +32,17 @@
 
 #include "ssd_device.cuh"
 #include "ssd_layout.h"
+#include "ssd_scan.cuh"
 
 namespace ssd {
 
 struct RowCtx {
   float mz, md;        // row maxima
   float c_hi, c_lo;    // log2(e)/T
-  float iz_hi, iz_lo;  // 1/S_z
-  float id_hi, id_lo;  // 1/S_d
+  float iz_hi, iz_lo;  // 1/S_z (filtered rows: 1/P_z, the kept mass)
+  float id_hi, id_lo;  // 1/S_d (filtered rows: 1/P_d)
   float rho;           // approximate S_z / S_d from the streaming statistics
+  unsigned long long thr_z, thr_d;  // filtered rows: order key of the last kept token
 };
 
 constexpr float kSignMargin = 1e-3f;
@@ -52,12 +54,38 @@ constexpr float kFixAcc = 281474976710656.0f;
 //   Q_NORM_Z : 2^((z - m_z) c)         (unnormalised, for S_z and the p_k draw)
 //   Q_NORM_D : 2^((d - m_d) c)
 //   Q_RESID  : max(0, p - q)
-enum Quantity { Q_NORM_Z = 0, Q_NORM_D = 1, Q_RESID = 2 };
+//   Q_FILT_TARGET : p_f, the filtered target law (0 outside its kept set)
+//   Q_FILT_RESID  : max(0, p_f - q_f) over the filtered laws
+enum Quantity { Q_NORM_Z = 0, Q_NORM_D = 1, Q_RESID = 2, Q_FILT_TARGET = 3, Q_FILT_RESID = 4 };
 
 template <int Q>
-__device__ __forceinline__ void weight(float z, float d, const RowCtx& cx, const float2* tab,
-                                       float& h, float& l) {
+__device__ __forceinline__ void weight(int i, float z, float d, const RowCtx& cx,
+                                       const float2* tab, float& h, float& l) {
   float xh, xl;
+  if (Q == Q_FILT_TARGET || Q == Q_FILT_RESID) {
+    h = 0.f;
+    l = 0.f;
+    if (order_key(z, i) < cx.thr_z) return;  // outside the target's kept set: p_f = 0
+    float ah, al, ph, pl;
+    arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, ah, al);
+    df_mul(ah, al, cx.iz_hi, cx.iz_lo, ph, pl);
+    if (Q == Q_FILT_TARGET || order_key(d, i) < cx.thr_d) {
+      h = ph;
+      l = pl;
+      return;
+    }
+    float bh, bl, qh, ql;
+    arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
+    exp2_df(xh, xl, tab, bh, bl);
+    df_mul(bh, bl, cx.id_hi, cx.id_lo, qh, ql);
+    df_sub(ph, pl, qh, ql, h, l);
+    if (!(h > 0.f)) {
+      h = 0.f;
+      l = 0.f;
+    }
+    return;
+  }
   if (Q == Q_NORM_Z) {
     arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
     exp2_df(xh, xl, tab, h, l);
@@ -95,20 +123,20 @@ __device__ __forceinline__ void range_sum(const typename Tag::Elem* zr,
     for (; i + kV <= hi; i += kV) {
       float z[8], d[8];
       if (Q != Q_NORM_D) Tag::loadv_cached(zr + i, z);
-      if (Q != Q_NORM_Z) Tag::loadv_cached(dr + i, d);
+      if (Q != Q_NORM_Z && Q != Q_FILT_TARGET) Tag::loadv_cached(dr + i, d);
 #pragma unroll
       for (int e = 0; e < kV; ++e) {
         float h, l;
-        weight<Q>(z[e], d[e], cx, tab, h, l);
+        weight<Q>(i + e, z[e], d[e], cx, tab, h, l);
         df_acc(sh, sl, h, l);
       }
     }
   }
   for (; i < hi; ++i) {
     float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
-    float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
+    float d = (Q != Q_NORM_Z && Q != Q_FILT_TARGET) ? Tag::load1(dr + i) : 0.f;
     float h, l;
-    weight<Q>(z, d, cx, tab, h, l);
+    weight<Q>(i, z, d, cx, tab, h, l);
     df_acc(sh, sl, h, l);
   }
 }
@@ -335,9 +363,9 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
       long long wf = 0;
       if (i < phi) {
         const float z = (Q != Q_NORM_D) ? Tag::load1(zr + i) : 0.f;
-        const float d = (Q != Q_NORM_Z) ? Tag::load1(dr + i) : 0.f;
+        const float d = (Q != Q_NORM_Z && Q != Q_FILT_TARGET) ? Tag::load1(dr + i) : 0.f;
         float wh, wl;
-        weight<Q>(z, d, cx, tab, wh, wl);
+        weight<Q>(i, z, d, cx, tab, wh, wl);
         wf = df_to_fix(wh, wl, scale);
       }
       long long c = wf;
@@ -426,7 +454,7 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     for (int q = tid; q < n_amb; q += kThreads) {
       const int i = amb[q];
       float wh, wl;
-      weight<Q_RESID>(Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
+      weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
       atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[i / p.CH]),
                 static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
     }
@@ -482,6 +510,138 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     tok = select_in_chunk<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual, target, sm, &s_pick);
   else
     tok = select_in_chunk<Tag, VEC, Q_NORM_Z>(zr, dr, clo, chi, p.E, cx, tab, kFixMass, target, sm, &s_pick);
+  if (tid == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
+}
+
+// ---------------------------------------------------------------------------
+// The draw over top-k / top-p filtered laws (ssd_verify_topk beyond the
+// in-register lists).  Each filtered row is given by the order key of its
+// last kept token and its kept mass P (FiltRow), so
+// p_f(v) = [key(z_v, v) >= thr_z] 2^((z_v - m_z) c) / P_z, likewise q_f, and
+// the weights are max(0, p_f - q_f) after a rejection, p_f for the bonus
+// token (p_f also when the residual is all zero).  Same numerics as above:
+// double-float weights, per-thread compensated sums, exact fixed point above
+// a thread, the chunk -> thread -> element select.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool filt_ctx(const FiltParams& p, int b, BState& bs, RowCtx* s_cx) {
+  bs = p.bstate[b];
+  if (bs.mode == kModeNone) return false;
+  if (threadIdx.x == 0) {
+    const FiltRow& fz = p.rows[static_cast<int64_t>(b) * p.R + bs.n];
+    RowCtx c;
+    c.mz = fz.m;
+    c.c_hi = fz.c_hi;
+    c.c_lo = fz.c_lo;
+    c.rho = 1.f;
+    split_double(1.0 / fz.P, c.iz_hi, c.iz_lo);
+    c.thr_z = fz.thr;
+    c.md = 0.f;
+    c.id_hi = c.id_lo = 0.f;
+    c.thr_d = ~0ull;
+    if (bs.mode == kModeResidual) {
+      const FiltRow& fd = p.rows[static_cast<int64_t>(b) * p.R + p.k + 1 + bs.n];
+      c.md = fd.m;
+      split_double(1.0 / fd.P, c.id_hi, c.id_lo);
+      c.thr_d = fd.thr;
+    }
+    *s_cx = c;
+  }
+  __syncthreads();
+  return true;
+}
+
+template <typename Tag>
+__device__ __forceinline__ void filt_rows_n(const FiltParams& p, int b, int n,
+                                            const typename Tag::Elem*& zr,
+                                            const typename Tag::Elem*& dr) {
+  zr = static_cast<const typename Tag::Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb +
+       static_cast<int64_t>(n) * p.V;
+  dr = static_cast<const typename Tag::Elem*>(p.D) + static_cast<int64_t>(b) * p.db +
+       static_cast<int64_t>(n < p.k ? n : 0) * p.V;
+}
+
+// grid (C, batch rows of this launch): per-chunk masses of the row's weights
+// (2^60 units), with the thread ranges of select_in_chunk.
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kThreads) filt_mass_kernel(FiltParams p) {
+  __shared__ float2 tab[64];
+  __shared__ long long sm[kWarps];
+  __shared__ RowCtx s_cx;
+  const int c = blockIdx.x, b = blockIdx.y + p.b0;
+  load_exp2_table(tab);
+  BState bs;
+  if (!filt_ctx(p, b, bs, &s_cx)) return;
+  const RowCtx cx = s_cx;
+  const typename Tag::Elem *zr, *dr;
+  filt_rows_n<Tag>(p, b, bs.n, zr, dr);
+  const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
+  const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
+  const int hi = min(chi, lo + p.E);
+  float h, l;
+  if (bs.mode == kModeResidual)
+    range_sum<Tag, VEC, Q_FILT_RESID>(zr, dr, lo, hi, cx, tab, h, l);
+  else
+    range_sum<Tag, VEC, Q_FILT_TARGET>(zr, dr, lo, hi, cx, tab, h, l);
+  const long long t = block_sum_i64(df_to_fix(h, l, kFixResidual), sm);
+  if (threadIdx.x == 0) p.rmass[static_cast<int64_t>(b) * p.C + c] = t;
+}
+
+// grid B: the chunk, then the token.
+template <typename Tag, bool VEC>
+__global__ void __launch_bounds__(kThreads) filt_select_kernel(FiltParams p) {
+  __shared__ float2 tab[64];
+  __shared__ long long sm[kWarps];
+  __shared__ long long s_wt[kThreads];
+  __shared__ int s_pick, s_chunk;
+  __shared__ long long s_target;
+  __shared__ RowCtx s_cx;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  load_exp2_table(tab);
+  BState bs;
+  if (!filt_ctx(p, b, bs, &s_cx)) return;
+  const RowCtx cx = s_cx;
+  const typename Tag::Elem *zr, *dr;
+  filt_rows_n<Tag>(p, b, bs.n, zr, dr);
+  bool resid = bs.mode == kModeResidual;
+  long long wq = tid < p.C ? p.rmass[static_cast<int64_t>(b) * p.C + tid] : 0;
+  long long W;
+  long long incl = block_scan_i64(wq, sm, &W);
+  if (resid && W <= 0) {  // all-zero residual: draw from the filtered p_n
+    resid = false;
+    for (int q = 0; q < p.C; ++q) {
+      const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
+      const int lo = min(chi, clo + tid * p.E), hi = min(chi, lo + p.E);
+      float h, l;
+      range_sum<Tag, VEC, Q_FILT_TARGET>(zr, dr, lo, hi, cx, tab, h, l);
+      const long long t = block_sum_i64(df_to_fix(h, l, kFixResidual), sm);
+      if (tid == 0) s_wt[q] = t;
+    }
+    __syncthreads();
+    wq = tid < p.C ? s_wt[tid] : 0;
+    incl = block_scan_i64(wq, sm, &W);
+  }
+  const long long t =
+      static_cast<long long>(scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]));
+  if (tid == 0) {
+    s_chunk = p.C - 1;
+    s_target = 0;
+  }
+  __syncthreads();
+  if (wq > 0 && incl > t && incl - wq <= t) {
+    s_chunk = tid;
+    s_target = t - (incl - wq);
+  }
+  __syncthreads();
+  const int q = s_chunk;
+  const long long target = s_target;
+  const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
+  int tok;
+  if (resid)
+    tok = select_in_chunk<Tag, VEC, Q_FILT_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual,
+                                                  target, sm, &s_pick);
+  else
+    tok = select_in_chunk<Tag, VEC, Q_FILT_TARGET>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual,
+                                                   target, sm, &s_pick);
   if (tid == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
 }
 
@@ -580,6 +740,35 @@ cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bo
   return SSD_DISPATCH_AFTER(residual_select_kernel, dim3(B));
 }
 #undef SSD_DISPATCH_AFTER
+
+cudaError_t launch_filt_mass(const FiltParams& p0, bool vec, cudaStream_t s) {
+  FiltParams p = p0;
+  for (int b0 = 0; b0 < p0.B; b0 += kMaxGridBatch) {
+    p.b0 = b0;
+    const dim3 grid(p.C, p0.B - b0 < kMaxGridBatch ? p0.B - b0 : kMaxGridBatch);
+    if (p.dtype == 1) {
+      if (vec) filt_mass_kernel<BF16Tag, true><<<grid, kThreads, 0, s>>>(p);
+      else filt_mass_kernel<BF16Tag, false><<<grid, kThreads, 0, s>>>(p);
+    } else {
+      if (vec) filt_mass_kernel<F32Tag, true><<<grid, kThreads, 0, s>>>(p);
+      else filt_mass_kernel<F32Tag, false><<<grid, kThreads, 0, s>>>(p);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_filt_select(const FiltParams& p, bool vec, cudaStream_t s) {
+  if (p.dtype == 1) {
+    if (vec) filt_select_kernel<BF16Tag, true><<<p.B, kThreads, 0, s>>>(p);
+    else filt_select_kernel<BF16Tag, false><<<p.B, kThreads, 0, s>>>(p);
+  } else {
+    if (vec) filt_select_kernel<F32Tag, true><<<p.B, kThreads, 0, s>>>(p);
+    else filt_select_kernel<F32Tag, false><<<p.B, kThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s) {
   residual_prep_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p);

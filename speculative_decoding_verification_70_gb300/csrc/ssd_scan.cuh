@@ -32,6 +32,22 @@ __device__ __forceinline__ float ord2f(unsigned o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
 
+// 64-bit order key of token (z, idx): descending key order is logit
+// descending, then index ascending (the order of top-k / top-p filtering and
+// of the forked recovery).  -0 and +0 compare equal as logits, so -0 is
+// taken as +0.  z must not be NaN.
+__device__ __forceinline__ unsigned long long order_key(float z, int idx) {
+  const float zc = (z == 0.f) ? 0.f : z;
+  return (static_cast<unsigned long long>(f2ord(zc)) << 32) |
+         static_cast<unsigned long long>(~static_cast<unsigned>(idx));
+}
+__device__ __forceinline__ float key_logit(unsigned long long key) {
+  return ord2f(static_cast<unsigned>(key >> 32));
+}
+__device__ __forceinline__ int key_index(unsigned long long key) {
+  return static_cast<int>(~static_cast<unsigned>(key & 0xffffffffull));
+}
+
 // Per-thread running statistics of the streaming pass.
 struct ScanState {
   float m;    // running maximum

@@ -211,12 +211,16 @@ def test_next_rows_reject_bad_arguments_on_host(lib):
                                    P, P, K, None, P, P, None, None, None, None, a["ws"],
                                    a["wsb"], None)
     assert topk(K=0) == INVALID
-    assert topk(K=33) == INVALID                     # K <= 32
-    assert topk(K=8, V=4) == INVALID                 # K > V
+    assert topk(K=33, wsb=16) == WS                  # K > 32: the threshold path's workspace
+    assert topk(K=8, V=4, zb=12, db=8, wsb=16) == WS  # K > V keeps every token
     assert topk(K=8, zb=10) == INVALID
     assert topk(K=8, wsb=16) == WS
-    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 33) == 0
-    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 32) > 0
+    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 0) == 0
+    n32 = lib.ssd_topk_workspace_bytes(2, 2, 1000, 32)
+    n33 = lib.ssd_topk_workspace_bytes(2, 2, 1000, 33)
+    assert n32 > 0 and n33 > 0 and n33 != n32
+    assert lib.ssd_topk_workspace_bytes(2, 2, 1000, 1 << 30) == lib.ssd_topk_workspace_bytes(2, 2, 1000, 1000)
+    assert lib.ssd_topk_workspace_bytes(2, 2, (1 << 21) + 8, 64) == 0   # V beyond the threshold path
     # the drafted verify checks like ssd_verify
     assert lib.ssd_verify_drafted(None, 3000, P, 2000, 0, 2, 2, 1000, P, P, P, P, None, None,
                                   None, None, P, big, None) == INVALID

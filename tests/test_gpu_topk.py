@@ -168,3 +168,108 @@ def test_verify_topk_last_resort(gpu_lib):
     got = {key: out[key][rows] for key in ("accept_len", "out_tok", "p_at_x", "q_at_x")}
     _check(sub, x[rows].cpu(), K, None, got)
     assert gpu_lib.get_device_error(out["ws"]) == 0
+
+
+# ---------------------------------------------------------------------------
+# K above the in-register lists and top-p over the whole vocabulary: each
+# row's kept set is a threshold on the token order, found from histograms
+# (ssd_filter.cu).  Same rules as above: decisions and tokens identical to
+# the oracle, p(x), q(x) within 1e-5.
+# ---------------------------------------------------------------------------
+BIG = [("qwen_b64", {"B": 8}, None, 50, None), ("qwen_b64", {"B": 8}, None, 50, 0.9),
+       ("qwen_b64", {"B": 8}, None, 256, 0.95), ("qwen_b64", {"B": 8}, None, "V", 0.9),
+       ("qwen_b64", {"B": 8}, None, "V", 0.95), ("qwen_b64", {"B": 6}, None, 1024, None),
+       ("mixed512", {"B": 8}, None, 50, 0.9), ("mixed512", {"B": 8}, None, 256, None),
+       ("mixed512", {"B": 8}, None, "V", 0.9), ("mixed512", {"B": 8}, None, "V", 0.95),
+       ("mixed512", {"B": 6}, "stochastic", 2000, 0.5), ("llama_sd", {"B": 4}, "1.0", "V", 0.8),
+       ("tiny", {"B": 12}, "stochastic", 33, None), ("tiny", {"B": 12}, "stochastic", "V", 0.7)]
+
+
+@pytest.mark.parametrize("name,over,temp,K,tp", BIG)
+def test_verify_filtered_large_k_and_nucleus(gpu_lib, name, over, temp, K, tp):
+    w = W.workload(name, **over)
+    K = w.V if K == "V" else K
+    inp = W.make_inputs(w, device=DEV, seed=W.default_seed(name) + 600, temp=temp)
+    x = _draft_tokens_in_topk(inp["D"], w.k, 4, 6)
+    top_p = None if tp is None else torch.full((w.B,), tp, device=DEV)
+    D = inp["D"][:, : w.k].contiguous()
+    out = gpu_lib.ssd_verify_topk(inp["Z"], D, x, inp["T"], K, top_p, inp["u_acc"], inp["u_smp"])
+    torch.cuda.synchronize()
+    ref = _check(dict(inp, D=D), x, K, top_p, out)
+    assert gpu_lib.get_device_error(out["ws"]) == 0
+    if w.B >= 8 and temp != "0":
+        assert (ref["accept_len"] > 0).any()
+
+
+def test_verify_filtered_nucleus_every_row_of_a_batch(gpu_lib):
+    """Top-p 0.9 over the whole vocabulary (K = V) on 256 stochastic rows of
+    the large-batch shape (fp32, V = 151936), per-row top_p, every row
+    against the oracle."""
+    w = W.workload("mixed512", B=256)
+    inp = W.make_inputs(w, device=DEV, seed=6061, temp="stochastic")
+    x = _draft_tokens_in_topk(inp["D"], w.k, 8, 7)
+    top_p = torch.linspace(0.5, 0.99, w.B, device=DEV)
+    D = inp["D"][:, : w.k].contiguous()
+    out = gpu_lib.ssd_verify_topk(inp["Z"], D, x, inp["T"], w.V, top_p, inp["u_acc"],
+                                  inp["u_smp"])
+    torch.cuda.synchronize()
+    _check(dict(inp, D=D), x, w.V, top_p, out)
+    assert gpu_lib.get_device_error(out["ws"]) == 0
+
+
+def test_verify_filtered_no_filter_equals_plain_verify(gpu_lib):
+    """K >= V and no top-p keeps every token: the threshold path then gives
+    what ssd_verify gives (same draws: the kept mass is the row's exact
+    mass)."""
+    w = W.workload("qwen_b64", B=16)
+    inp = W.make_inputs(w, device=DEV, seed=71)
+    D = inp["D"][:, : w.k].contiguous()
+    a = gpu_lib.ssd_verify_topk(inp["Z"], D, inp["x"], inp["T"], 10 * w.V, None, inp["u_acc"],
+                                inp["u_smp"])
+    b = gpu_lib.ssd_verify(inp["Z"], D, inp["x"], inp["T"], inp["u_acc"], inp["u_smp"])
+    assert torch.equal(a["accept_len"], b["accept_len"])
+    assert torch.equal(a["out_tok"], b["out_tok"])
+    assert torch.allclose(a["p_at_x"], b["p_at_x"], atol=1e-6)
+
+
+def test_verify_filtered_edges(gpu_lib):
+    """Rows the threshold path must get right: thousands of equal logits
+    (the cut's bins overflow the candidate buffer: bisection), ties at the
+    cut, -0 and +0 logits, rows with fewer finite logits than K, NaN and
+    +inf rows, a bad token, greedy rows, top_p = 0 (one token kept), top_p
+    just below 1, K just below V; an unaligned row length takes the scalar
+    path."""
+    for V in (5000, 5001):
+        B, k = 10, 3
+        g = torch.Generator().manual_seed(V)
+        Z = torch.randn((B, k + 1, V), generator=g) * 2
+        D = Z[:, :k] + torch.randn((B, k, V), generator=g) * 0.7
+        Z[0] = 1.5                                            # constant rows
+        D[0] = 1.5
+        Z[1] = torch.randint(-2, 3, (k + 1, V), generator=g).float()  # five values: ties
+        D[1] = torch.randint(-2, 3, (k, V), generator=g).float()
+        Z[2, :, ::2] = 0.0                                    # +0 and -0
+        Z[2, :, 1::2] = -0.0
+        D[2, :, ::3] = -0.0
+        Z[3, :, 40:] = float("-inf")                           # 40 finite logits
+        D[3, :, 60:] = float("-inf")
+        Z[4, 1, 17] = float("nan")
+        D[5, 0, 3] = float("inf")
+        x = torch.randint(0, 40, (B, k), generator=g, dtype=torch.int32)
+        x[6, 1] = V                                           # bad token
+        T = torch.tensor([1.0, 0.9, 1.1, 0.8, 1.0, 1.0, 1.0, 0.0, 0.7, 1.3])
+        ua = torch.rand((B, k), generator=g)
+        us = torch.rand(B, generator=g)
+        inp = {"Z": Z, "D": D, "T": T, "u_acc": ua, "u_smp": us}
+        for K, tp in ((V, 0.9), (1000, None), (V - 1, 0.3), (100, 0.999999), (64, 0.0),
+                      (V, float(np.nextafter(np.float32(1), np.float32(0))))):
+            top_p = None if tp is None else torch.full((B,), tp)
+            out = gpu_lib.ssd_verify_topk(Z.to(DEV), D.to(DEV), x.to(DEV), T.to(DEV), K,
+                                          None if top_p is None else top_p.to(DEV),
+                                          ua.to(DEV), us.to(DEV))
+            torch.cuda.synchronize()
+            ref = _check(inp, x, K, top_p, out)
+            assert ref["accept_len"][4] == -1 and ref["accept_len"][5] == -1
+            assert ref["accept_len"][6] == -2
+            err = gpu_lib.get_device_error(out["ws"], clear=True)
+            assert not err & gpu_lib.DEVERR_FILTER_BAND, (V, K, tp, err)
