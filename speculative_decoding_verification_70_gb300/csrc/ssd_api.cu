@@ -198,18 +198,25 @@ ssd_status check_common(const VerifyCall& c, bool fork) {
 // the draft rows that feed the forked recovery in another ("stats_topf").
 // When s_plain != s_topf, the target rows and the draft rows go to the two
 // streams and run concurrently.
+// Chunks per statistics CTA: the largest power of two (a whole row at most)
+// that still leaves two waves of CTAs (2 x 6 resident x 152 SMs).  Longer
+// CTAs pay their set-up, block reduction and (top-f) selection once per
+// more bytes: measured at B = 512, k = 7, V = 151936 fp32 the pass took
+// 743 us with 4 chunks per CTA and 700 us with a whole row; at B = 64,
+// k = 5 bf16, 87 us with 1 chunk and 78 us with 2.
+inline int stats_group(long long rows, int C) {
+  int G = 1;
+  while (G < C && rows * ((C + 2 * G - 1) / (2 * G)) >= 1824) G *= 2;
+  return G;
+}
+
 cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s_plain,
                        cudaStream_t s_topf) {
   StatsParams sp = sp0;
   const bool topf = sp.Pdf > 0 && sp.f > 0;
   const bool split = s_plain != s_topf;
-  // plain rows: up to 4 chunks (128 KB) per CTA while the grid still has
-  // at least ~16 CTAs per SM
   const int rows_plain = topf ? sp.Pz : (split ? sp.Pz : sp.R);
-  sp.G = 1;
-  while (sp.G < 4 && static_cast<long long>(B) * rows_plain * ((sp.C + 2 * sp.G - 1) / (2 * sp.G)) >= 2432)
-    sp.G *= 2;
-  sp.G = split_group(sp.G, sp.C);
+  sp.G = split_group(stats_group(static_cast<long long>(B) * rows_plain, sp.C), sp.C);
   cudaError_t e = cudaSuccess;
   if (rows_plain > 0) {
     ProfScope ps("stats", s_plain);
@@ -225,10 +232,7 @@ cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaS
   }
   ProfScope ps("stats_topf", s_topf);
   StatsParams pt = sp;
-  pt.G = 1;
-  while (pt.G < 4 && static_cast<long long>(B) * sp.Pdf * ((sp.C + 2 * pt.G - 1) / (2 * pt.G)) >= 2432)
-    pt.G *= 2;
-  pt.G = split_group(pt.G, sp.C);
+  pt.G = split_group(stats_group(static_cast<long long>(B) * sp.Pdf, sp.C), sp.C);
   return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s_topf);
 }
 

@@ -105,6 +105,41 @@ __device__ __forceinline__ float ex2_fast(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs (add / sub / mul / fma .f32x2 of sm_100+): two IEEE
+// binary32 operations per instruction, each lane rounded as its scalar
+// counterpart.  A pair lives in one 64-bit register (low lane first).
+// ---------------------------------------------------------------------------
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void up2(f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start before its predecessor in the stream has
 // finished; pdl_wait() blocks until the predecessor has completed and its
@@ -170,6 +205,75 @@ __device__ __forceinline__ void exp2_df(float xh, float xl, const float2* tab, f
   const float e = __fsub_rn(l, __fsub_rn(s, t.x));
   hi = __fmul_rn(s, scale);
   lo = __fmul_rn(e, scale);
+}
+
+// ---------------------------------------------------------------------------
+// The same operations on two independent lanes at once (packed fp32 pairs):
+// each lane computes exactly what the scalar function computes, bit for bit.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum2(f32x2 a, f32x2 b, f32x2& s, f32x2& e) {
+  s = add2(a, b);
+  const f32x2 bb = sub2(s, a);
+  e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+// arg_df for lanes (z0, m0) and (z1, m1) with one coefficient pair c.
+__device__ __forceinline__ void arg_df2(f32x2 z, f32x2 m, f32x2 c_hi, f32x2 c_lo, f32x2& xh,
+                                        f32x2& xl) {
+  f32x2 dh, dl;
+  const f32x2 neg = pk2(-0.0f, -0.0f);
+  float m0, m1;
+  up2(m, m0, m1);
+  two_sum2(z, pk2(-m0, -m1), dh, dl);
+  xh = mul2(dh, c_hi);
+  xl = fma2(dh, c_hi, sub2(neg, xh));  // dh c_hi - xh, exact
+  xl = fma2(dh, c_lo, xl);
+  xl = fma2(dl, c_hi, xl);
+}
+
+// exp2_df for two lanes; a lane with xh <= -125 (or NaN) gives 0.
+__device__ __forceinline__ void exp2_df2(f32x2 xh, f32x2 xl, const float2* tab, f32x2& hi,
+                                         f32x2& lo) {
+  const float kMagic = 12582912.0f;
+  const f32x2 magic = pk2(kMagic, kMagic);
+  const f32x2 tj = fma2(xh, pk2(64.0f, 64.0f), magic);
+  const f32x2 Jf = sub2(tj, magic);
+  float tj0, tj1;
+  up2(tj, tj0, tj1);
+  const int J0 = __float_as_int(tj0) - 0x4B400000, J1 = __float_as_int(tj1) - 0x4B400000;
+  f32x2 g = fma2(Jf, pk2(-0.015625f, -0.015625f), xh);
+  g = add2(g, xl);
+  f32x2 P = fma2(g, pk2(SSD_EXP2_C3, SSD_EXP2_C3), pk2(SSD_EXP2_C2, SSD_EXP2_C2));
+  P = fma2(g, P, pk2(SSD_LN2_LO, SSD_LN2_LO));
+  P = mul2(g, P);
+  P = fma2(g, pk2(SSD_LN2_HI, SSD_LN2_HI), P);
+  const float2 t0 = tab[J0 & 63], t1 = tab[J1 & 63];
+  const f32x2 tx = pk2(t0.x, t1.x), ty = pk2(t0.y, t1.y);
+  const f32x2 l = fma2(tx, P, fma2(ty, P, ty));
+  const f32x2 sc = pk2(__int_as_float(((J0 >> 6) + 127) << 23), __int_as_float(((J1 >> 6) + 127) << 23));
+  const f32x2 sm = add2(tx, l);
+  const f32x2 e = sub2(l, sub2(sm, tx));
+  hi = mul2(sm, sc);
+  lo = mul2(e, sc);
+  float xh0, xh1, h0, h1, l0, l1;
+  up2(xh, xh0, xh1);
+  up2(hi, h0, h1);
+  up2(lo, l0, l1);
+  const bool ok0 = xh0 > -125.0f, ok1 = xh1 > -125.0f;
+  hi = pk2(ok0 ? h0 : 0.f, ok1 ? h1 : 0.f);
+  lo = pk2(ok0 ? l0 : 0.f, ok1 ? l1 : 0.f);
+}
+
+// comp_acc for two lanes.
+__device__ __forceinline__ void comp_acc2(f32x2& acc, f32x2& comp, f32x2 vh, f32x2 vl) {
+  float a0, a1, v0, v1;
+  up2(acc, a0, a1);
+  up2(vh, v0, v1);
+  const f32x2 big = pk2(fmaxf(a0, v0), fmaxf(a1, v1));
+  const f32x2 small = pk2(fminf(a0, v0), fminf(a1, v1));
+  const f32x2 t = add2(big, small);
+  comp = add2(comp, add2(add2(sub2(big, t), small), vl));
+  acc = t;
 }
 
 // Copy the exp2 table to shared memory (call before the first exp2_df; a

@@ -93,11 +93,13 @@ __device__ __forceinline__ void weight(int i, float z, float d, const RowCtx& cx
     arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
     exp2_df(xh, xl, tab, h, l);
   } else {
+    // a = 2^((z - m_z) c) and b = 2^((d - m_d) c) as one packed pair
     float ah, al, bh, bl, ph, pl, qh, ql;
-    arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
-    exp2_df(xh, xl, tab, ah, al);
-    arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
-    exp2_df(xh, xl, tab, bh, bl);
+    f32x2 x2h, x2l, e2h, e2l;
+    arg_df2(pk2(z, d), pk2(cx.mz, cx.md), pk2(cx.c_hi, cx.c_hi), pk2(cx.c_lo, cx.c_lo), x2h, x2l);
+    exp2_df2(x2h, x2l, tab, e2h, e2l);
+    up2(e2h, ah, bh);
+    up2(e2l, al, bl);
     df_mul(ah, al, cx.iz_hi, cx.iz_lo, ph, pl);
     df_mul(bh, bl, cx.id_hi, cx.id_lo, qh, ql);
     df_sub(ph, pl, qh, ql, h, l);
@@ -187,29 +189,32 @@ __device__ __forceinline__ void row_ptrs(const ResidualParams& p, int b, int n,
        static_cast<int64_t>(n) * p.V;
 }
 
-// One element of the fused pass: a (and b) added to the normaliser sums; in
-// residual mode the sign split against rho~.
-__device__ __forceinline__ void pass_element(float z, float d, int idx, bool resid,
-                                             const RowCtx& cx, const float2* tab, float& sah,
-                                             float& sal, float& sbh, float& sbl, float& ah,
-                                             float& al, float& bh, float& bl, int* amb_cnt,
-                                             int* amb_idx, int amb_cap) {
-  float xh, xl, a_h, a_l;
-  arg_df(z, cx.mz, cx.c_hi, cx.c_lo, xh, xl);
-  exp2_df(xh, xl, tab, a_h, a_l);
-  comp_acc(sah, sal, a_h, a_l);
-  if (!resid) return;
-  float b_h, b_l;
-  arg_df(d, cx.md, cx.c_hi, cx.c_lo, xh, xl);
-  exp2_df(xh, xl, tab, b_h, b_l);
-  comp_acc(sbh, sbl, b_h, b_l);
+// Running sums of one thread of the norm pass, as packed pairs (lane 0: the
+// target row's a, lane 1: the draft row's b): the normalisers (S_z, S_d)
+// and the positive side of the sign split (A, B), each with its
+// compensation term.
+struct NormAcc {
+  f32x2 sh, sl;   // S_z, S_d
+  f32x2 ph, pl;   // A, B
+};
+
+// One element of the residual pass: a and b (one packed exponential pair)
+// added to the normaliser sums, then the sign split against rho~.
+__device__ __forceinline__ void pass_pair(float z, float d, int idx, const RowCtx& cx,
+                                          const float2* tab, NormAcc& na, int* amb_cnt,
+                                          int* amb_idx, int amb_cap) {
+  f32x2 xh, xl, eh, el;
+  arg_df2(pk2(z, d), pk2(cx.mz, cx.md), pk2(cx.c_hi, cx.c_hi), pk2(cx.c_lo, cx.c_lo), xh, xl);
+  exp2_df2(xh, xl, tab, eh, el);
+  comp_acc2(na.sh, na.sl, eh, el);
+  float a_h, b_h;
+  up2(eh, a_h, b_h);
   // the pairs are normalised: hi alone is good to 2^-24 against the margin
   const float rb = cx.rho * b_h;
   const float diff = a_h - rb;
   const float lim = kSignMargin * fmaxf(a_h, rb);
   if (diff > lim) {
-    comp_acc(ah, al, a_h, a_l);
-    comp_acc(bh, bl, b_h, b_l);
+    comp_acc2(na.ph, na.pl, eh, el);
   } else if (diff >= -lim && (a_h > 0.f || rb > 0.f)) {
     const int q = atomicAdd(amb_cnt, 1);
     if (q < amb_cap) amb_idx[q] = idx;
@@ -236,29 +241,66 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   const int hi = min(chi, lo + p.E);
   int* amb_cnt = p.amb_cnt + b;
   int* amb_idx = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
-  float sah = 0.f, sal = 0.f, sbh = 0.f, sbl = 0.f, ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
   constexpr int kV = Tag::kVec;
+  const f32x2 zero = pk2(0.f, 0.f);
+  NormAcc na = {zero, zero, zero, zero};
   int i = lo;
-  if (VEC) {
-    for (; i + kV <= hi; i += kV) {
-      float z[8], d[8];
-      Tag::loadv_cached(zr + i, z);
-      if (resid) Tag::loadv_cached(dr + i, d);
+  if (resid) {
+    if (VEC) {
+      for (; i + kV <= hi; i += kV) {
+        float z[8], d[8];
+        Tag::loadv_cached(zr + i, z);
+        Tag::loadv_cached(dr + i, d);
 #pragma unroll
-      for (int e = 0; e < kV; ++e)
-        pass_element(z[e], resid ? d[e] : 0.f, i + e, resid, cx, tab, sah, sal, sbh, sbl, ah, al,
-                     bh, bl, amb_cnt, amb_idx, p.amb_cap);
+        for (int e = 0; e < kV; ++e)
+          pass_pair(z[e], d[e], i + e, cx, tab, na, amb_cnt, amb_idx, p.amb_cap);
+      }
+    }
+    for (; i < hi; ++i)
+      pass_pair(Tag::load1(zr + i), Tag::load1(dr + i), i, cx, tab, na, amb_cnt, amb_idx,
+                p.amb_cap);
+  } else {
+    // bonus draw: S_z only, two consecutive elements per packed pair (the
+    // lanes are summed at the end)
+    const f32x2 mz = pk2(cx.mz, cx.mz), ch = pk2(cx.c_hi, cx.c_hi), cl = pk2(cx.c_lo, cx.c_lo);
+    if (VEC) {
+      for (; i + kV <= hi; i += kV) {
+        float z[8];
+        Tag::loadv_cached(zr + i, z);
+#pragma unroll
+        for (int e = 0; e < kV; e += 2) {
+          f32x2 xh, xl, eh, el;
+          arg_df2(pk2(z[e], z[e + 1]), mz, ch, cl, xh, xl);
+          exp2_df2(xh, xl, tab, eh, el);
+          comp_acc2(na.sh, na.sl, eh, el);
+        }
+      }
+    }
+    for (; i < hi; ++i) {
+      float xh, xl, a_h, a_l;
+      arg_df(Tag::load1(zr + i), cx.mz, cx.c_hi, cx.c_lo, xh, xl);
+      exp2_df(xh, xl, tab, a_h, a_l);
+      float s0, s1, c0, c1;
+      up2(na.sh, s0, s1);
+      up2(na.sl, c0, c1);
+      comp_acc(s0, c0, a_h, a_l);
+      na.sh = pk2(s0, s1);
+      na.sl = pk2(c0, c1);
     }
   }
-  for (; i < hi; ++i)
-    pass_element(Tag::load1(zr + i), resid ? Tag::load1(dr + i) : 0.f, i, resid, cx, tab, sah,
-                 sal, sbh, sbl, ah, al, bh, bl, amb_cnt, amb_idx, p.amb_cap);
-  long long tz = block_sum_i64(df_to_fix(sah, sal, kFixMass), sm);
-  long long td = 0, ta = 0, tb = 0;
+  float sah, sbh, sal, sbl, ah, bh, al, bl;
+  up2(na.sh, sah, sbh);
+  up2(na.sl, sal, sbl);
+  up2(na.ph, ah, bh);
+  up2(na.pl, al, bl);
+  long long tz, td = 0, ta = 0, tb = 0;
   if (resid) {
+    tz = block_sum_i64(df_to_fix(sah, sal, kFixMass), sm);
     td = block_sum_i64(df_to_fix(sbh, sbl, kFixMass), sm);
     ta = block_sum_i64(df_to_fix(ah, al, kFixAcc), sm);
     tb = block_sum_i64(df_to_fix(bh, bl, kFixAcc), sm);
+  } else {  // the two lanes hold the even and odd elements' sums of a
+    tz = block_sum_i64(df_to_fix(sah, sal, kFixMass) + df_to_fix(sbh, sbl, kFixMass), sm);
   }
   if (threadIdx.x == 0) {
     const int64_t o = (static_cast<int64_t>(b) * p.C + c) * 2;

@@ -51,10 +51,11 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 // Per-thread running statistics of the streaming pass.
 struct ScanState {
   float m;    // running maximum
-  float s;    // running sum of 2^((z - m) c)
+  float s;    // running sum of 2^((z - m) c) (with sb: two lanes of a packed pair)
   int idx;    // lowest index attaining m
   int nan;    // a NaN was seen
   float m2;   // second largest value -- kept only for top-f rows
+  float sb;   // second lane of the running sum (pairs of elements)
 };
 
 __device__ __forceinline__ void scan_init(ScanState& st) {
@@ -63,7 +64,11 @@ __device__ __forceinline__ void scan_init(ScanState& st) {
   st.idx = kIdxNone;
   st.nan = 0;
   st.m2 = -INFINITY;
+  st.sb = 0.f;
 }
+
+// The running sum: both lanes.
+__device__ __forceinline__ float scan_sum(const ScanState& st) { return st.s + st.sb; }
 
 // Max / argmax / NaN / (optionally) the online exponential sum over one
 // vector of n logits starting at index base_idx.  vm is the vector maximum
@@ -103,15 +108,29 @@ __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], 
       // rescale the running sum to the new maximum
       float f = (st.m == vm) ? 1.f : ex2_fast((st.m - vm) * c);
       st.s = st.s * f;
+      st.sb = st.sb * f;
     }
     st.m = vm;
     st.idx = base_idx + e_star;
   }
   if (DO_EXP) {
     float base = (st.m == -INFINITY) ? 0.f : st.m;
+    if (n == 1) {
+      st.s += ex2_fast((z[0] - base) * c);
+    } else {
+      // pairs of elements: (z - base) * c and the sum in packed fp32 (the
+      // exponent arguments are those of the scalar form, bit for bit)
+      const f32x2 b2 = pk2(base, base), c2 = pk2(c, c);
+      f32x2 s2 = pk2(st.s, st.sb);
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (e < n) st.s += ex2_fast((z[e] - base) * c);
+      for (int e = 0; e < 8; e += 2)
+        if (e + 1 < n) {
+          float x0, x1;
+          up2(mul2(sub2(pk2(z[e], z[e + 1]), b2), c2), x0, x1);
+          s2 = add2(s2, pk2(ex2_fast(x0), ex2_fast(x1)));
+        }
+      up2(s2, st.s, st.sb);
+    }
   }
 }
 
@@ -162,7 +181,7 @@ __device__ __forceinline__ void block_stats_write(const ScanState& st, float c, 
                                                   float* sm_m, float* sm_s, int* sm_i,
                                                   int* sm_n, PartStat* out_part) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float m = st.m, s = st.s;
+  float m = st.m, s = scan_sum(st);
   int idx = st.idx, nan = st.nan;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
