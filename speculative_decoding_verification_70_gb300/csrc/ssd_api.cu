@@ -33,7 +33,6 @@ cudaError_t launch_tree_walk(const TreeParams& p, int dtype, bool vec, cudaStrea
 cudaError_t launch_softmax_finalize(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_softmax_probs(const SoftmaxParams& p, cudaStream_t s);
 cudaError_t launch_residual_norm(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
-cudaError_t launch_residual_mass(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s);
 cudaError_t launch_residual_prep(const PrepParams& p, cudaStream_t s);
 cudaError_t launch_selftest_exp2(const float* xh, const float* xl, double* out, int n, cudaStream_t s);
@@ -251,20 +250,25 @@ cudaError_t cache_insert(const CacheView& v, const InsertArgs& a, cudaStream_t s
   return launch_cache_write(v, a, s);
 }
 
-cudaError_t run_residual(const ResidualParams& rp, int B, int dtype, bool vec, cudaStream_t s) {
+// The draw: the norm pass, then (after `between`, if given: work that must
+// precede the select) the select.
+template <typename Between>
+cudaError_t run_residual(const ResidualParams& rp, int B, int dtype, bool vec, cudaStream_t s,
+                         Between&& between) {
   cudaError_t e;
   {
     ProfScope ps("residual_norm", s);
     e = launch_residual_norm(rp, B, dtype, vec, s);
   }
   if (e != cudaSuccess) return e;
-  {
-    ProfScope ps("residual_mass", s);
-    e = launch_residual_mass(rp, B, dtype, vec, s);
-  }
+  e = between();
   if (e != cudaSuccess) return e;
   ProfScope ps("residual_select", s);
   return launch_residual_select(rp, B, dtype, vec, s);
+}
+
+cudaError_t run_residual(const ResidualParams& rp, int B, int dtype, bool vec, cudaStream_t s) {
+  return run_residual(rp, B, dtype, vec, s, [] { return cudaSuccess; });
 }
 
 // ---------------------------------------------------------------------------
@@ -314,6 +318,10 @@ DevStreams* device_streams() {
 // draft-row statistics concurrently, the cache insert beside the draw).
 // Measured at B = 1 (ssd_fork step with the cache): 67 / 53 us eager / as a
 // graph on one stream, 49 / 43 us on two.
+// Smallest batch whose cache lookup runs inside the draw's select kernel.
+#ifndef SSD_FUSE_LOOKUP_MIN_B
+#define SSD_FUSE_LOOKUP_MIN_B 16
+#endif
 #ifndef SSD_MIN_STREAMED_B
 #define SSD_MIN_STREAMED_B 1
 #endif
@@ -385,7 +393,7 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   rp.T = c.T + b0; rp.u_smp = c.u_smp ? c.u_smp + b0 : nullptr;
   rp.rowstat = rowstat; rp.bstate = bstate;
   rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm)) + static_cast<size_t>(b0) * C * 2;
-  rp.rmass = reinterpret_cast<long long*>(wsp(c.ws, L.rmass)) + static_cast<size_t>(b0) * C;
+  rp.rthr = reinterpret_cast<long long*>(wsp(c.ws, L.rthr)) + static_cast<size_t>(b0) * C * 3 * kDrawThreads;
   rp.racc = reinterpret_cast<long long*>(wsp(c.ws, L.racc)) + static_cast<size_t>(b0) * C * 2;
   rp.amb_cnt = reinterpret_cast<int*>(wsp(c.ws, L.amb_cnt)) + b0;
   rp.amb_cap = amb_cap(c.V);
@@ -443,10 +451,31 @@ cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool
     if (e == cudaSuccess) e = cudaEventRecord(ev_ins, side);
     if (e != cudaSuccess) return e;
   }
-  if (c.u_smp) e = run_residual(q.rp, Bs, q.fp.dtype, vec, s);
-  if (e != cudaSuccess || !cache) return e;
-  if (overlap) e = cudaStreamWaitEvent(s, ev_ins, 0);
-  else e = cache_forks(c, s);
+  // the forks must be in the cache before any row's outcome is looked up
+  auto inserted = [&]() -> cudaError_t {
+    if (!cache) return cudaSuccess;
+    return overlap ? cudaStreamWaitEvent(s, ev_ins, 0) : cache_forks(c, s);
+  };
+  if (c.u_smp) {
+    // one slice holding every row: the select kernel looks up each row's
+    // outcome as soon as its token is final (no separate lookup launch);
+    // it then waits for the insert instead of overlapping the norm pass's
+    // tail, so small batches, whose insert outlasts the norm pass, keep
+    // the separate lookup
+    const bool fuse = cache && Bs == c.B && c.B >= SSD_FUSE_LOOKUP_MIN_B;
+    ResidualParams rp = q.rp;
+    if (fuse) {
+      rp.lookup = 1;
+      rp.cache = *c.cache;
+      rp.hit = c.hit;
+      rp.tok_out = c.tok_out;
+    }
+    e = run_residual(rp, Bs, q.fp.dtype, vec, s, inserted);
+    if (e != cudaSuccess || !cache || fuse) return e;
+    return cache_lookup_outcome(c, s);
+  }
+  if (!cache) return e;
+  e = inserted();
   if (e == cudaSuccess) e = cache_lookup_outcome(c, s);
   return e;
 }
@@ -957,7 +986,7 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
   rp.T = T; rp.u_smp = u_smp;
   rp.rowstat = pp.rowstat; rp.bstate = pp.bstate;
   rp.rnorm = reinterpret_cast<long long*>(wsp(ws, L.rnorm));
-  rp.rmass = reinterpret_cast<long long*>(wsp(ws, L.rmass));
+  rp.rthr = reinterpret_cast<long long*>(wsp(ws, L.rthr));
   rp.racc = reinterpret_cast<long long*>(wsp(ws, L.racc));
   rp.amb_cnt = reinterpret_cast<int*>(wsp(ws, L.amb_cnt));
   rp.amb_idx = reinterpret_cast<int*>(wsp(ws, L.amb_idx));

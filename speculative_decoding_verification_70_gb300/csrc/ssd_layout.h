@@ -10,10 +10,11 @@
 namespace ssd {
 
 constexpr int kMaxMask = 64;        // masked tokens per (b, position)
-constexpr int kAmbCap = 2048;       // ambiguous-sign elements kept per row (draw), at most
+constexpr int kAmbCap = 8192;       // ambiguous-sign elements kept per row (draw), at most
                                     // V (amb_cap(V) below)
 constexpr int kMaxGridBatch = 65535;  // batch rows per launch (grid y / z limit)
 constexpr int kMaxChunkBytes = 32768;  // a chunk fits one shared-memory stage
+constexpr int kDrawThreads = 256;      // threads per CTA of the draw kernels
 
 // Partial statistics of one chunk of one logit row.
 struct PartStat {
@@ -62,7 +63,7 @@ struct Chunking {
 
 // Workspace of the verify / fork / residual calls.
 struct WsLayout {
-  size_t err, part, topk, rowstat, bstate, rnorm, rmass, racc, amb_cnt, amb_idx, gpart, total;
+  size_t err, part, topk, rowstat, bstate, rnorm, rthr, racc, amb_cnt, amb_idx, gpart, total;
   int B, R, Pf, f;
   Chunking ch;
 };
@@ -119,6 +120,17 @@ struct FinalizeParams {
   int* amb_cnt;        // [B], zeroed here for the draw
 };
 
+struct CacheView {
+  unsigned long long* keys;
+  unsigned long long* winner;
+  int32_t* payload;
+  int* err;                  // device error word
+  unsigned long long* calls; // inserts completed so far (device counter)
+  unsigned* done;            // finished CTAs of the running insert's write kernel
+  int capacity;
+  int depth;
+};
+
 struct ResidualParams {
   const void* Z; int64_t zb; int Pz;
   const void* D; int64_t db;
@@ -128,7 +140,7 @@ struct ResidualParams {
   const RowStat* rowstat;
   const BState* bstate;
   long long* rnorm;    // [B][C][2]
-  long long* rmass;    // [B][C]
+  long long* rthr;     // [B][C][3][kThreads]: each norm-pass thread's S_z, A, B
   long long* racc;     // [B][C][2]
   int* amb_cnt;        // [B]
   int* amb_idx;        // [B][amb_cap]
@@ -136,6 +148,12 @@ struct ResidualParams {
   int b0;              // first batch row of this launch (grids hold <= 65535)
   int B;               // batch rows of this call (row-strided kernels)
   int32_t* out_tok;    // [B][k+1]
+  // the SSD round step: the select kernel looks up each row's realised
+  // outcome (b, n, out_tok[b][n]) once its token is final
+  int lookup;
+  CacheView cache;
+  int32_t* hit;        // [B]
+  int32_t* tok_out;    // [B][depth]
 };
 
 // Token-tree verification (ssd_verify_tree).
@@ -311,16 +329,6 @@ struct PrepParams {
   int* amb_cnt;
 };
 
-struct CacheView {
-  unsigned long long* keys;
-  unsigned long long* winner;
-  int32_t* payload;
-  int* err;                  // device error word
-  unsigned long long* calls; // inserts completed so far (device counter)
-  unsigned* done;            // finished CTAs of the running insert's write kernel
-  int capacity;
-  int depth;
-};
 
 struct InsertArgs {
   const int32_t* b;
@@ -419,7 +427,7 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * B * L.R);
   L.bstate = off;                   off = align256(off + sizeof(BState) * B);
   L.rnorm = off;                    off = align256(off + sizeof(long long) * 2 * B * C);
-  L.rmass = off;                    off = align256(off + sizeof(long long) * B * C);
+  L.rthr = off;                     off = align256(off + sizeof(long long) * 3 * kDrawThreads * B * C);
   L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * C);
   L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
@@ -490,7 +498,7 @@ inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
   L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
   L.topk = off;
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * rows);
-  L.bstate = off; L.rnorm = off; L.rmass = off; L.racc = off; L.amb_cnt = off; L.amb_idx = off;
+  L.bstate = off; L.rnorm = off; L.rthr = off; L.racc = off; L.amb_cnt = off; L.amb_idx = off;
   L.gpart = off;
   L.total = off;
   return L;

@@ -25,11 +25,17 @@
 //                   rho = S_z/S_d is known; clearly negative ones add
 //                   nothing; the few ambiguous ones are listed and evaluated
 //                   exactly by the select kernel.
-//   residual_mass   the direct W_c = sum max(0, p - q), run only for rows
-//                   whose ambiguous list overflowed
-//   residual_select chunk -> thread -> element select, writes out_tok[b, n]
+//                   Every thread also stores its own fixed-point S_z, A, B,
+//                   so that the select finds the thread without
+//                   recomputing the chunk.
+//   residual_select chunk -> thread -> element select, writes out_tok[b, n];
+//                   rows whose ambiguous list overflowed take the direct
+//                   W_c = sum max(0, p - q) (computed here, one pass over
+//                   the row); in the SSD round step it also looks up the
+//                   row's realised outcome in the speculation cache
 #include <math.h>
 
+#include "ssd_cache.cuh"
 #include "ssd_device.cuh"
 #include "ssd_layout.h"
 #include "ssd_scan.cuh"
@@ -294,54 +300,29 @@ __global__ void __launch_bounds__(kThreads) residual_norm_kernel(ResidualParams 
   up2(na.ph, ah, bh);
   up2(na.pl, al, bl);
   long long tz, td = 0, ta = 0, tb = 0;
+  long long oz, oa = 0, ob = 0;  // this thread's own S_z, A, B
   if (resid) {
-    tz = block_sum_i64(df_to_fix(sah, sal, kFixMass), sm);
+    oz = df_to_fix(sah, sal, kFixMass);
+    oa = df_to_fix(ah, al, kFixAcc);
+    ob = df_to_fix(bh, bl, kFixAcc);
+    tz = block_sum_i64(oz, sm);
     td = block_sum_i64(df_to_fix(sbh, sbl, kFixMass), sm);
-    ta = block_sum_i64(df_to_fix(ah, al, kFixAcc), sm);
-    tb = block_sum_i64(df_to_fix(bh, bl, kFixAcc), sm);
+    ta = block_sum_i64(oa, sm);
+    tb = block_sum_i64(ob, sm);
   } else {  // the two lanes hold the even and odd elements' sums of a
-    tz = block_sum_i64(df_to_fix(sah, sal, kFixMass) + df_to_fix(sbh, sbl, kFixMass), sm);
+    oz = df_to_fix(sah, sal, kFixMass) + df_to_fix(sbh, sbl, kFixMass);
+    tz = block_sum_i64(oz, sm);
   }
+  long long* own = p.rthr + (static_cast<int64_t>(b) * p.C + c) * 3 * kDrawThreads + threadIdx.x;
+  own[0] = oz;
+  own[kDrawThreads] = oa;
+  own[2 * kDrawThreads] = ob;
   if (threadIdx.x == 0) {
     const int64_t o = (static_cast<int64_t>(b) * p.C + c) * 2;
     p.rnorm[o + 0] = tz;
     p.rnorm[o + 1] = td;
     p.racc[o + 0] = ta;
     p.racc[o + 1] = tb;
-  }
-}
-
-// Direct per-chunk residual masses (2^60 units) of the rows whose ambiguous
-// list overflowed (p ~ q on more than amb_cap elements, e.g. bf16 drafts
-// that equal the target on many logits).  Grid (C, at most 128 row slots):
-// each CTA walks the batch rows slot, slot + 128, ..., so the launch costs a
-// few microseconds when no row overflowed.
-constexpr int kMassRowSlots = 128;
-
-template <typename Tag, bool VEC>
-__global__ void __launch_bounds__(kThreads) residual_mass_kernel(ResidualParams p) {
-  __shared__ float2 tab[64];
-  __shared__ long long sm[kWarps];
-  __shared__ RowCtx s_cx;
-  pdl_wait();     // the norm kernel has completed
-  pdl_trigger();  // the select kernel may be scheduled
-  const int c = blockIdx.x;
-  load_exp2_table(tab);
-  for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-    if (p.bstate[b].mode != kModeResidual || p.amb_cnt[b] <= p.amb_cap) continue;
-    BState bs;
-    RowCtx cx;
-    load_ctx(p, b, bs, cx, &s_cx, true);  // holds a __syncthreads()
-    const typename Tag::Elem *zr, *dr;
-    row_ptrs<Tag>(p, b, bs.n, zr, dr);
-    const int clo = c * p.CH, chi = min(p.V, clo + p.CH);
-    const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * p.E);
-    const int hi = min(chi, lo + p.E);
-    float h, l;
-    range_sum<Tag, VEC, Q_RESID>(zr, dr, lo, hi, cx, tab, h, l);
-    long long fw = df_to_fix(h, l, kFixResidual);
-    long long tw = block_sum_i64(fw, sm);  // its barriers also retire s_cx
-    if (threadIdx.x == 0) p.rmass[static_cast<int64_t>(b) * p.C + c] = tw;
   }
 }
 
@@ -362,16 +343,16 @@ __device__ __forceinline__ unsigned long long scale_by_uniform(unsigned long lon
   return (lo >> shift) | (shift ? (hi << (64 - shift)) : 0ull);
 }
 
+// The thread, then the element, holding fixed-point mass `target` of chunk
+// [clo, chi): every thread passes `own`, the mass of its range [clo + t E,
+// + E) in units of `scale`; warp 0 then walks the picked range with the
+// exact per-element weights.
 template <typename Tag, bool VEC, int Q>
-__device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag::Elem* dr,
+__device__ int select_from_own(const typename Tag::Elem* zr, const typename Tag::Elem* dr,
                                int clo, int chi, int E, const RowCtx& cx, const float2* tab,
-                               float scale, long long target, long long* sm, int* s_pick) {
+                               float scale, long long target, long long own, long long* sm,
+                               int* s_pick) {
   const int tid = threadIdx.x;
-  const int lo = min(chi, clo + tid * E);
-  const int hi = min(chi, lo + E);
-  float h, l;
-  range_sum<Tag, VEC, Q>(zr, dr, lo, hi, cx, tab, h, l);
-  long long own = df_to_fix(h, l, scale);
   long long tot;
   long long incl = block_scan_i64(own, sm, &tot);
   // a chunk mass taken from the sign split can exceed this chunk's direct
@@ -429,16 +410,50 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
   return -1 - *s_pick;
 }
 
+// The same with every thread's mass computed here from the exact weights.
+template <typename Tag, bool VEC, int Q>
+__device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag::Elem* dr,
+                               int clo, int chi, int E, const RowCtx& cx, const float2* tab,
+                               float scale, long long target, long long* sm, int* s_pick) {
+  const int lo = min(chi, clo + static_cast<int>(threadIdx.x) * E);
+  const int hi = min(chi, lo + E);
+  float h, l;
+  range_sum<Tag, VEC, Q>(zr, dr, lo, hi, cx, tab, h, l);
+  return select_from_own<Tag, VEC, Q>(zr, dr, clo, chi, E, cx, tab, scale, target,
+                                      df_to_fix(h, l, scale), sm, s_pick);
+}
+
+// (A_t - rho B_t) / S_z in 2^60 units from 2^48 fixed-point A, B (rho and
+// 2^12 / S_z as float pairs), clamped at 0: the sign split's residual mass
+// of a chunk (or of one thread's range).
+__device__ __forceinline__ long long split_mass(long long a, long long b, float2 rho,
+                                                float2 inv4096) {
+  float ah, al, bh, bl, th, tl, vh, vl;
+  i64_to_df(a, ah, al);
+  i64_to_df(b, bh, bl);
+  df_mul(rho.x, rho.y, bh, bl, th, tl);   // rho B
+  df_sub(ah, al, th, tl, vh, vl);         // A - rho B
+  df_mul(vh, vl, inv4096.x, inv4096.y, vh, vl);
+  const long long w = vh > 0.f ? __float2ll_rn(vh) + __float2ll_rn(vl) : 0;
+  return w < 0 ? 0 : w;
+}
+
 // grid B.  One CTA per batch row; every chunk-level step runs one chunk per
 // thread (C <= kThreads): the chunk weights are formed in parallel, an int64
 // block scan places the target, and one 128-bit product gives
-// floor(u * W).  Only the two normaliser inverses are taken by one thread.
+// floor(u * W).  Within the chunk the thread level reads the norm pass's
+// per-thread sums (no exponentials); only the picked thread's range is
+// walked element by element.  Only the two normaliser inverses are taken by
+// one thread.  Rows whose ambiguous-sign list overflowed evaluate the
+// residual directly (chunk masses and the thread level, one pass over the
+// row in this CTA).  With p.lookup every row, drawn or not, then looks up
+// its realised outcome in the speculation cache.
 template <typename Tag, bool VEC>
 __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParams p) {
-  pdl_wait();  // the mass kernel has completed
+  pdl_wait();  // the norm kernel has completed
   __shared__ float2 tab[64];
   __shared__ long long sm[kWarps];
-  __shared__ long long s_amb[kThreads];  // per-chunk exact mass of the ambiguous elements (2^60)
+  __shared__ long long s_amb[kThreads];  // exact mass of the ambiguous elements (2^60) by chunk, then by thread
   __shared__ int s_pick;
   __shared__ int s_chunk;
   __shared__ long long s_target;
@@ -446,113 +461,138 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
   __shared__ float2 s_acc[2];            // rho = S_z / S_d and 2^12 / S_z, float pairs
   const int b = blockIdx.x, tid = threadIdx.x;
   const BState bs = p.bstate[b];
-  if (bs.mode == kModeNone) return;
-  load_exp2_table(tab);
-  const bool resid_row = bs.mode == kModeResidual;
-  const int64_t rb = static_cast<int64_t>(b) * p.C;
-  long long cz = 0, cd = 0, ca = 0, cb = 0;
-  if (tid < p.C) {
-    cz = p.rnorm[(rb + tid) * 2 + 0];
-    if (resid_row) {
-      cd = p.rnorm[(rb + tid) * 2 + 1];
-      ca = p.racc[(rb + tid) * 2 + 0];
-      cb = p.racc[(rb + tid) * 2 + 1];
+  if (bs.mode != kModeNone) {
+    load_exp2_table(tab);
+    const bool resid_row = bs.mode == kModeResidual;
+    const int64_t rb = static_cast<int64_t>(b) * p.C;
+    long long cz = 0, cd = 0, ca = 0, cb = 0;
+    if (tid < p.C) {
+      cz = p.rnorm[(rb + tid) * 2 + 0];
+      if (resid_row) {
+        cd = p.rnorm[(rb + tid) * 2 + 1];
+        ca = p.racc[(rb + tid) * 2 + 0];
+        cb = p.racc[(rb + tid) * 2 + 1];
+      }
     }
-  }
-  s_amb[tid] = 0;
-  const long long sz = block_sum_i64(cz, sm);
-  const long long sd = resid_row ? block_sum_i64(cd, sm) : 1;
-  if (tid == 0) {
-    RowCtx c;
-    c.mz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n].m;
-    c.md = resid_row ? p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m : 0.f;
-    c.rho = 1.f;
-    c.c_hi = bs.c_hi;
-    c.c_lo = bs.c_lo;
-    // normalisers and their inverses in double-float (no FP64 on this
-    // thread's chain); the 2^-42 unit scaling is exact
-    constexpr float kMass = 2.2737367544323206e-13f;  // 2^-42
-    float szh, szl, sdh, sdl;
-    i64_to_df(sz, szh, szl);
-    i64_to_df(sd, sdh, sdl);
-    szh *= kMass; szl *= kMass;
-    sdh *= kMass; sdl *= kMass;
-    df_recip(szh, szl, c.iz_hi, c.iz_lo);
-    df_recip(sdh, sdl, c.id_hi, c.id_lo);
-    s_cx = c;
-    float rh, rl;
-    df_mul(szh, szl, c.id_hi, c.id_lo, rh, rl);
-    s_acc[0] = make_float2(rh, rl);
-    s_acc[1] = make_float2(c.iz_hi * 4096.f, c.iz_lo * 4096.f);
-  }
-  __syncthreads();
-  const RowCtx cx = s_cx;
-  const typename Tag::Elem *zr, *dr;
-  row_ptrs<Tag>(p, b, bs.n, zr, dr);
-  const int n_amb = resid_row ? p.amb_cnt[b] : 0;
-  const bool split = resid_row && n_amb <= p.amb_cap;
-  if (split) {
-    const int* amb = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
-    for (int q = tid; q < n_amb; q += kThreads) {
-      const int i = amb[q];
-      float wh, wl;
-      weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
-      atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[i / p.CH]),
-                static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
+    s_amb[tid] = 0;
+    const long long sz = block_sum_i64(cz, sm);
+    const long long sd = resid_row ? block_sum_i64(cd, sm) : 1;
+    if (tid == 0) {
+      RowCtx c;
+      c.mz = p.rowstat[static_cast<int64_t>(b) * p.R + bs.n].m;
+      c.md = resid_row ? p.rowstat[static_cast<int64_t>(b) * p.R + p.Pz + bs.n].m : 0.f;
+      c.rho = 1.f;
+      c.c_hi = bs.c_hi;
+      c.c_lo = bs.c_lo;
+      // normalisers and their inverses in double-float (no FP64 on this
+      // thread's chain); the 2^-42 unit scaling is exact
+      constexpr float kMass = 2.2737367544323206e-13f;  // 2^-42
+      float szh, szl, sdh, sdl;
+      i64_to_df(sz, szh, szl);
+      i64_to_df(sd, sdh, sdl);
+      szh *= kMass; szl *= kMass;
+      sdh *= kMass; sdl *= kMass;
+      df_recip(szh, szl, c.iz_hi, c.iz_lo);
+      df_recip(sdh, sdl, c.id_hi, c.id_lo);
+      s_cx = c;
+      float rh, rl;
+      df_mul(szh, szl, c.id_hi, c.id_lo, rh, rl);
+      s_acc[0] = make_float2(rh, rl);
+      s_acc[1] = make_float2(c.iz_hi * 4096.f, c.iz_lo * 4096.f);
     }
     __syncthreads();
-  }
-  // chunk weights in the units select_in_chunk sums: residual mass in 2^60
-  // (W_c = (A_c - rho B_c) / S_z plus the ambiguous part, or the direct
-  // masses when the ambiguous list overflowed), target mass a in 2^42
-  long long wq = 0;
-  if (tid < p.C) {
+    const RowCtx cx = s_cx;
+    const typename Tag::Elem *zr, *dr;
+    row_ptrs<Tag>(p, b, bs.n, zr, dr);
+    const int n_amb = resid_row ? p.amb_cnt[b] : 0;
+    const bool split = resid_row && n_amb <= p.amb_cap;
+    const int* amb = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
     if (split) {
-      float ah, al, bh, bl, th, tl, vh, vl, mh, ml;
-      i64_to_df(ca, ah, al);
-      i64_to_df(cb, bh, bl);
-      df_mul(s_acc[0].x, s_acc[0].y, bh, bl, th, tl);       // rho B_c
-      df_sub(ah, al, th, tl, vh, vl);                       // A_c - rho B_c
-      df_mul(vh, vl, s_acc[1].x, s_acc[1].y, vh, vl);       // / S_z, in 2^60 units
-      i64_to_df(s_amb[tid], mh, ml);
-      df_acc(vh, vl, mh, ml);
-      wq = vh > 0.f ? __float2ll_rn(vh) + __float2ll_rn(vl) : 0;
-      if (wq < 0) wq = 0;
-    } else if (resid_row) {
-      wq = p.rmass[rb + tid];
+      for (int q = tid; q < n_amb; q += kThreads) {
+        const int i = amb[q];
+        float wh, wl;
+        weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[i / p.CH]),
+                  static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
+      }
+      __syncthreads();
+    }
+    // chunk weights in the units of the thread level: residual mass in
+    // 2^60 (W_c = (A_c - rho B_c) / S_z plus the ambiguous part, or the
+    // direct masses when the ambiguous list overflowed), target mass a in
+    // 2^42
+    long long wq = 0;
+    if (split) {
+      if (tid < p.C) wq = split_mass(ca, cb, s_acc[0], s_acc[1]) + s_amb[tid];
+    } else if (resid_row) {  // direct masses, chunk by chunk
+      for (int q = 0; q < p.C; ++q) {
+        const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
+        const int lo = min(chi, clo + tid * p.E), hi = min(chi, lo + p.E);
+        float h, l;
+        range_sum<Tag, VEC, Q_RESID>(zr, dr, lo, hi, cx, tab, h, l);
+        const long long m = block_sum_i64(df_to_fix(h, l, kFixResidual), sm);
+        if (tid == q) wq = m;
+      }
     } else {
       wq = cz;
     }
+    long long W;
+    long long incl = block_scan_i64(wq, sm, &W);
+    bool resid = resid_row;
+    if (resid && W <= 0) {  // all-zero residual: draw from p_n
+      resid = false;
+      wq = tid < p.C ? cz : 0;
+      incl = block_scan_i64(wq, sm, &W);
+    }
+    const long long t =
+        static_cast<long long>(scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]));
+    if (tid == 0) {
+      s_chunk = p.C - 1;  // unreachable default: t < W always finds a chunk
+      s_target = 0;
+    }
+    __syncthreads();
+    if (wq > 0 && incl > t && incl - wq <= t) {  // exactly one thread
+      s_chunk = tid;
+      s_target = t - (incl - wq);
+    }
+    __syncthreads();
+    const int q = s_chunk;
+    const long long target = s_target;
+    const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
+    const long long* own = p.rthr + (rb + q) * 3 * kDrawThreads + tid;
+    int tok;
+    if (!resid) {  // the norm pass's per-thread S_z of this chunk
+      tok = select_from_own<Tag, VEC, Q_NORM_Z>(zr, dr, clo, chi, p.E, cx, tab, kFixMass, target,
+                                                own[0], sm, &s_pick);
+    } else if (split) {
+      // per-thread sign-split masses plus each thread's ambiguous elements
+      s_amb[tid] = 0;
+      __syncthreads();
+      for (int r = tid; r < n_amb; r += kThreads) {
+        const int i = amb[r];
+        if (i >= clo && i < chi) {
+          float wh, wl;
+          weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
+          atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[(i - clo) / p.E]),
+                    static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
+        }
+      }
+      __syncthreads();
+      const long long w =
+          split_mass(own[kDrawThreads], own[2 * kDrawThreads], s_acc[0], s_acc[1]) + s_amb[tid];
+      tok = select_from_own<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual,
+                                               target, w, sm, &s_pick);
+    } else {
+      tok = select_in_chunk<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual,
+                                               target, sm, &s_pick);
+    }
+    if (tid == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
   }
-  long long W;
-  long long incl = block_scan_i64(wq, sm, &W);
-  bool resid = resid_row;
-  if (resid && W <= 0) {  // all-zero residual: draw from p_n
-    resid = false;
-    wq = tid < p.C ? cz : 0;
-    incl = block_scan_i64(wq, sm, &W);
+  if (p.lookup && tid == 0) {  // the row's outcome: (b, n, out_tok[b][n])
+    const int n = bs.n;
+    const int tok = (n >= 0 && n <= p.k) ? p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + n] : -1;
+    cache_lookup_one(p.cache, b, n, tok, p.hit + b, p.tok_out + static_cast<int64_t>(b) * p.cache.depth);
   }
-  const long long t =
-      static_cast<long long>(scale_by_uniform(static_cast<unsigned long long>(W), p.u_smp[b]));
-  if (tid == 0) {
-    s_chunk = p.C - 1;  // unreachable default: t < W always finds a chunk
-    s_target = 0;
-  }
-  __syncthreads();
-  if (wq > 0 && incl > t && incl - wq <= t) {  // exactly one thread
-    s_chunk = tid;
-    s_target = t - (incl - wq);
-  }
-  __syncthreads();
-  const int q = s_chunk;
-  const long long target = s_target;
-  const int clo = q * p.CH, chi = min(p.V, clo + p.CH);
-  int tok;
-  if (resid)
-    tok = select_in_chunk<Tag, VEC, Q_RESID>(zr, dr, clo, chi, p.E, cx, tab, kFixResidual, target, sm, &s_pick);
-  else
-    tok = select_in_chunk<Tag, VEC, Q_NORM_Z>(zr, dr, clo, chi, p.E, cx, tab, kFixMass, target, sm, &s_pick);
-  if (tid == 0) p.out_tok[static_cast<int64_t>(b) * (p.k + 1) + bs.n] = tok;
 }
 
 // ---------------------------------------------------------------------------
@@ -771,12 +811,6 @@ static cudaError_t launch_after(Kernel kernel, dim3 grid, cudaStream_t s, const 
                      : launch_after(KERNEL<BF16Tag, false>, GRID, s, p))              \
               : (vec ? launch_after(KERNEL<F32Tag, true>, GRID, s, p)                 \
                      : launch_after(KERNEL<F32Tag, false>, GRID, s, p)))
-
-cudaError_t launch_residual_mass(const ResidualParams& p0, int B, int dtype, bool vec, cudaStream_t s) {
-  ResidualParams p = p0;
-  p.B = B;
-  return SSD_DISPATCH_AFTER(residual_mass_kernel, dim3(p.C, B < kMassRowSlots ? B : kMassRowSlots));
-}
 
 cudaError_t launch_residual_select(const ResidualParams& p, int B, int dtype, bool vec, cudaStream_t s) {
   return SSD_DISPATCH_AFTER(residual_select_kernel, dim3(B));
