@@ -542,6 +542,24 @@ SSD_API ssd_status ssd_profile_end(ssd_profile_entry *out, int cap, int *n_out);
 SSD_API ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta);
 
 /*
+ * Small-batch schedule override (tuning and tests; not part of the method).
+ * After the statistics pass, a verify call of at most max_b batch rows
+ * (default 16) runs its finalisation, recovery / bonus draw and, in
+ * ssd_verify_fork_cache, the cache insert and outcome lookup as one
+ * cluster kernel: one thread-block cluster of up to 8 CTAs per batch row,
+ * the row merges and the draw's pass over the vocabulary split over the
+ * cluster, partial sums exchanged through distributed shared memory.
+ * Larger batches launch the finalisation, draw and cache kernels
+ * separately.  max_b = 0 disables the cluster kernel; negative restores the
+ * default.  Process-wide, read at each call.  Accept lengths, p_at_x,
+ * q_at_x and forks are the same bits on both schedules; a drawn token is
+ * the same except where u falls within ~1e-12 relative of a boundary of the
+ * inverse CDF (the two schedules round their fixed-point partial masses
+ * over different ranges).  Returns SSD_OK.
+ */
+SSD_API ssd_status ssd_set_chain_batch(int max_b);
+
+/*
  * Self-test hook for the library's extended-precision exponential (used by
  * the recovery draw): out[i] = 2^(x_hi[i] + x_lo[i]) in double, for
  * x_hi <= 0.  Device pointers, n >= 0.  Not part of the verify path.

@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     profile_end,
     selftest_exp2,
     set_split,
+    set_chain_batch,
     softmax_workspace_bytes,
     ssd_draft_sample,
     ssd_forked_recovery,

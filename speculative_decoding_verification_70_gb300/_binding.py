@@ -77,6 +77,7 @@ SIGNATURES = [
     ("ssd_verify_noalloc", _I, [_P, _L, _P, _L, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                 _P, _P]),
     ("ssd_set_split", _I, [_I, _I]),
+    ("ssd_set_chain_batch", _I, [_I]),
     ("ssd_profile_begin", _I, [_I]),
     ("ssd_profile_end", _I, [_P, _I, _P]),
 ]
@@ -586,6 +587,13 @@ def set_split(chunk_elems: int = 0, chunks_per_cta: int = 0):
     statistics CTA; 0 = the library's policy) for later calls in this
     process.  Integer results do not depend on it."""
     _check("ssd_set_split", load_library().ssd_set_split(int(chunk_elems), int(chunks_per_cta)))
+
+
+def set_chain_batch(max_b: int = -1):
+    """Largest batch whose verify tail (finalisation, draw, cache step) runs
+    as the one cluster kernel; 0 disables it, negative restores the default
+    (16).  Process-wide, for later calls."""
+    _check("ssd_set_chain_batch", load_library().ssd_set_chain_batch(int(max_b)))
 
 
 def profile_begin(max_launches: int = 4096):

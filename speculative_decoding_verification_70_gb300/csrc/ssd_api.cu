@@ -49,6 +49,7 @@ cudaError_t launch_filt_select(const FiltParams& p, bool vec, cudaStream_t s);
 cudaError_t launch_cache_claim(const CacheView& c, const InsertArgs& a, cudaStream_t s);
 cudaError_t launch_cache_write(const CacheView& c, const InsertArgs& a, cudaStream_t s);
 cudaError_t launch_cache_lookup(const CacheView& c, const LookupArgs& a, cudaStream_t s);
+cudaError_t launch_chain(ChainParams p, int dtype, bool vec, cudaStream_t s);
 }  // namespace ssd
 
 using namespace ssd;
@@ -429,13 +430,53 @@ cudaError_t cache_lookup_outcome(const VerifyCall& c, cudaStream_t s) {
   return launch_cache_lookup(*c.cache, a, s);
 }
 
+// Largest batch whose verify after the statistics pass runs as the one
+// cluster kernel (finalisation, draw and the SSD round step's cache work in
+// one launch, ssd_chain.cu); larger batches take the batched kernels, whose
+// grids spread the draw's passes over the whole GPU.  ssd_set_chain_batch
+// overrides it.
+#ifndef SSD_CHAIN_MAX_B
+#define SSD_CHAIN_MAX_B 16
+#endif
+std::atomic<int> g_chain_max_b{-1};
+
+bool use_chain(int B) {
+  const int ov = g_chain_max_b.load(std::memory_order_relaxed);
+  return B <= (ov >= 0 ? ov : SSD_CHAIN_MAX_B);
+}
+
+// The whole tail of a one-slice call as the cluster kernel.
+cudaError_t enqueue_chain(const VerifyCall& c, const SliceParams& q, bool vec, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (c.cache && c.cache_clear) {
+    const size_t kb = sizeof(unsigned long long) * c.cache->capacity;
+    e = cudaMemsetAsync(c.cache->keys, 0xff, kb, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c.cache->winner, 0, kb, s);
+    if (e != cudaSuccess) return e;
+  }
+  ChainParams cp;
+  memset(&cp, 0, sizeof cp);
+  cp.f = q.fp;
+  cp.u_smp = q.rp.u_smp;
+  if (c.cache) {
+    cp.cache_on = 1;
+    cp.cache = *c.cache;
+    cp.payload = c.payload;
+    cp.hit = c.hit;
+    cp.tok_out = c.tok_out;
+  }
+  ProfScope ps("chain", s);
+  return launch_chain(cp, q.fp.dtype, vec, s);
+}
+
 // finalize + (optional) draw of one slice on stream s.  With a cache step
 // and a side stream, the last slice's forks go into the cache on the side
 // stream while the draw runs (side waits on the finalize, s on the insert
-// before the lookup).
+// before the lookup).  A small batch in one slice takes the cluster kernel.
 cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool vec,
                          cudaStream_t s, bool last = true, cudaStream_t side = nullptr,
                          cudaEvent_t ev_fin = nullptr, cudaEvent_t ev_ins = nullptr) {
+  if (Bs == c.B && use_chain(c.B)) return enqueue_chain(c, q, vec, s);
   cudaError_t e;
   {
     ProfScope ps("finalize", s);
@@ -1235,6 +1276,11 @@ ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta) {
   if (chunk_elems < 0 || chunks_per_cta < 0) return SSD_ERR_INVALID_ARG;
   g_split.chunk.store(chunk_elems, std::memory_order_relaxed);
   g_split.group.store(chunks_per_cta, std::memory_order_relaxed);
+  return SSD_OK;
+}
+
+ssd_status ssd_set_chain_batch(int max_b) {
+  g_chain_max_b.store(max_b < 0 ? -1 : max_b, std::memory_order_relaxed);
   return SSD_OK;
 }
 

@@ -156,6 +156,23 @@ struct ResidualParams {
   int32_t* tok_out;    // [B][depth]
 };
 
+// The verify step of a small batch after the statistics pass in one kernel
+// (ssd_chain.cu): one cluster of up to kChainMaxCluster CTAs per batch row
+// does the finalisation, the draw and, in the SSD round step, the cache
+// insert of the row's forks and the lookup of its outcome.
+constexpr int kChainMaxCluster = 8;
+
+struct ChainParams {
+  FinalizeParams f;
+  const float* u_smp;      // [B] or null (no draw)
+  int E;                   // elements per thread of the cluster's draw pass (multiple of 8)
+  int cache_on;            // SSD round step
+  CacheView cache;
+  const int32_t* payload;  // [B][k+1][f][depth]
+  int32_t* hit;            // [B]
+  int32_t* tok_out;        // [B][depth]
+};
+
 // Token-tree verification (ssd_verify_tree).
 constexpr int kMaxTreeNodes = 64;
 

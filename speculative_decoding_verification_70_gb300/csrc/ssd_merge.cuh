@@ -1,7 +1,8 @@
 // ssd_merge.cuh -- merge of a logit row's per-chunk partial records (the
 // statistics pass writes one record per chunk: maximum, lowest index
-// attaining it, NaN flag and the chunk's sum of 2^((z - m_c) c)).  Shared by
-// the finalisation of the chain step and by the token-tree walk.
+// attaining it, NaN flag and the chunk's sum of 2^((z - m_c) c)) and of its
+// per-chunk top-f lists.  Shared by the finalisation of the chain step, the
+// small-batch cluster kernel and the token-tree walk.
 #pragma once
 
 #include "ssd_device.cuh"
@@ -68,6 +69,54 @@ inline __device__ void merge_row(const PartStat* parts, int C, float c_hi, float
   int bad = nan;
   if (do_exp && !(sh > 0.f && sh < INFINITY)) bad = 1;  // +inf, NaN or all -inf at T > 0
   rs.flags = (nan ? 1 : 0) | (bad ? 2 : 0);
+}
+
+// Top-f of one fork row from its C chunk lists (one warp).  Only the first
+// `keep` picks are written; slots keep .. f-1 get (token -1, logit -inf).
+inline __device__ void merge_topf_row(const TopEntry* lists, int C, int f, int keep, bool nan,
+                               int32_t* tok_out, float* logit_out, int* heads) {
+  const int lane = threadIdx.x & 31;
+  for (int q = lane; q < C; q += 32) heads[q] = 0;
+  __syncwarp();
+  for (int r = 0; r < f; ++r) {
+    float bv = -INFINITY;
+    int bi = kIdxNone, bq = -1;
+    for (int q = lane; q < C; q += 32) {
+      int h = heads[q];
+      if (h < f) {
+        TopEntry e = lists[q * f + h];
+        if (bq < 0 || ranks_before(e.v, e.i, bv, bi)) {
+          bv = e.v; bi = e.i; bq = q;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(kFull, bv, o);
+      int oi = __shfl_xor_sync(kFull, bi, o);
+      int oq = __shfl_xor_sync(kFull, bq, o);
+      bool take = (oq >= 0) && (bq < 0 || ranks_before(ov, oi, bv, bi) ||
+                                (ov == bv && oi == bi && oq < bq));
+      if (take) { bv = ov; bi = oi; bq = oq; }
+    }
+    if (bq >= 0 && (bq & 31) == lane) heads[bq] += 1;
+    __syncwarp();
+    if (lane == 0) {
+      if (r >= keep) {
+        tok_out[r] = -1;
+        logit_out[r] = -INFINITY;
+      } else if (nan) {
+        tok_out[r] = -1;
+        logit_out[r] = NAN;
+      } else if (bq < 0 || bi == kIdxNone) {
+        tok_out[r] = -1;
+        logit_out[r] = -INFINITY;
+      } else {
+        tok_out[r] = bi;
+        logit_out[r] = bv;
+      }
+    }
+  }
 }
 
 }  // namespace ssd

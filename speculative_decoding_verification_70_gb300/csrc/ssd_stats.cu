@@ -654,54 +654,6 @@ __global__ void __launch_bounds__(kThreads) draft_finalize_kernel(DraftParams p)
 // Finalisation.
 // ---------------------------------------------------------------------------
 
-// Top-f of one fork row from its C chunk lists (one warp).  Only the first
-// `keep` picks are written; slots keep .. f-1 get (token -1, logit -inf).
-__device__ void merge_topf_row(const TopEntry* lists, int C, int f, int keep, bool nan,
-                               int32_t* tok_out, float* logit_out, int* heads) {
-  const int lane = threadIdx.x & 31;
-  for (int q = lane; q < C; q += 32) heads[q] = 0;
-  __syncwarp();
-  for (int r = 0; r < f; ++r) {
-    float bv = -INFINITY;
-    int bi = kIdxNone, bq = -1;
-    for (int q = lane; q < C; q += 32) {
-      int h = heads[q];
-      if (h < f) {
-        TopEntry e = lists[q * f + h];
-        if (bq < 0 || ranks_before(e.v, e.i, bv, bi)) {
-          bv = e.v; bi = e.i; bq = q;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(kFull, bv, o);
-      int oi = __shfl_xor_sync(kFull, bi, o);
-      int oq = __shfl_xor_sync(kFull, bq, o);
-      bool take = (oq >= 0) && (bq < 0 || ranks_before(ov, oi, bv, bi) ||
-                                (ov == bv && oi == bi && oq < bq));
-      if (take) { bv = ov; bi = oi; bq = oq; }
-    }
-    if (bq >= 0 && (bq & 31) == lane) heads[bq] += 1;
-    __syncwarp();
-    if (lane == 0) {
-      if (r >= keep) {
-        tok_out[r] = -1;
-        logit_out[r] = -INFINITY;
-      } else if (nan) {
-        tok_out[r] = -1;
-        logit_out[r] = NAN;
-      } else if (bq < 0 || bi == kIdxNone) {
-        tok_out[r] = -1;
-        logit_out[r] = -INFINITY;
-      } else {
-        tok_out[r] = bi;
-        logit_out[r] = bv;
-      }
-    }
-  }
-}
-
 __device__ __forceinline__ float logit_at(const void* base, int dtype, int64_t i) {
   if (dtype == 1)
     return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(base) + i)) << 16);
