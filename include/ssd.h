@@ -77,7 +77,7 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 #define SSD_DEVERR_BAD_LOGITS 0x2      /* NaN (or +inf / all -inf at T>0) */
 #define SSD_DEVERR_BAD_TOKEN 0x4       /* draft token outside [0, V): -2  */
 #define SSD_DEVERR_CACHE_FULL 0x8      /* insert found no free slot       */
-#define SSD_DEVERR_TIMEOUT 0x10        /* reserved: a bounded device wait ran out */
+#define SSD_DEVERR_TIMEOUT 0x10        /* a bounded device wait ran out   */
 #define SSD_DEVERR_FILTER_BAND 0x20    /* a filtered row's cut fell outside its collected
                                           bins; it was cut by bisection (results exact) */
 
@@ -558,6 +558,25 @@ SSD_API ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta);
  * over different ranges).  Returns SSD_OK.
  */
 SSD_API ssd_status ssd_set_chain_batch(int max_b);
+
+/*
+ * Whole-call schedule override for the smallest batches (tuning and tests;
+ * not part of the method).  A verify call of at most max_b batch rows
+ * (default 4, at most 8) runs as one cooperative kernel: the statistics
+ * pass, row merges and forks, acceptance, the draw's two exact passes over
+ * rows n and the select, separated by grid-wide barriers among CTAs that
+ * are all resident; in ssd_verify_fork_cache also the cache clear, insert
+ * and outcome lookup.  max_b = 0 disables it, negative restores the default;
+ * max_grid > 0 caps the CTAs of that kernel (0: as many as the GPU holds at
+ * once).  If the launch is refused the call takes the launch-by-launch
+ * schedule.  Every barrier wait is bounded: one that runs out sets
+ * SSD_DEVERR_TIMEOUT and the kernel returns without finishing the call.
+ * Accept lengths, p_at_x, q_at_x and forks are the same bits on every
+ * schedule; a drawn token is the same except where u falls within ~1e-12
+ * relative of a boundary of the inverse CDF.  Returns SSD_ERR_INVALID_ARG
+ * for max_grid < 0, else SSD_OK.  Process-wide, read at each call.
+ */
+SSD_API ssd_status ssd_set_step_schedule(int max_b, int max_grid);
 
 /*
  * Self-test hook for the library's extended-precision exponential (used by

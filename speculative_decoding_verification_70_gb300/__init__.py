@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     DEVERR_BAD_TOKEN,
     DEVERR_CACHE_FULL,
     DEVERR_FILTER_BAND,
+    DEVERR_TIMEOUT,
     SIGNATURES,
     SSDError,
     SpecCache,
@@ -22,6 +23,7 @@ from ._binding import (  # noqa: F401
     selftest_exp2,
     set_split,
     set_chain_batch,
+    set_step_schedule,
     softmax_workspace_bytes,
     ssd_draft_sample,
     ssd_forked_recovery,

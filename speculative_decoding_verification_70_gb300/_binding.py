@@ -25,6 +25,7 @@ DEVERR_BAD_TEMPERATURE = 0x1
 DEVERR_BAD_LOGITS = 0x2
 DEVERR_BAD_TOKEN = 0x4
 DEVERR_CACHE_FULL = 0x8
+DEVERR_TIMEOUT = 0x10
 DEVERR_FILTER_BAND = 0x20
 
 # (name, restype, argtypes)
@@ -78,6 +79,7 @@ SIGNATURES = [
                                 _P, _P]),
     ("ssd_set_split", _I, [_I, _I]),
     ("ssd_set_chain_batch", _I, [_I]),
+    ("ssd_set_step_schedule", _I, [_I, _I]),
     ("ssd_profile_begin", _I, [_I]),
     ("ssd_profile_end", _I, [_P, _I, _P]),
 ]
@@ -594,6 +596,15 @@ def set_chain_batch(max_b: int = -1):
     as the one cluster kernel; 0 disables it, negative restores the default
     (16).  Process-wide, for later calls."""
     _check("ssd_set_chain_batch", load_library().ssd_set_chain_batch(int(max_b)))
+
+
+def set_step_schedule(max_b: int = -1, max_grid: int = 0):
+    """Largest batch whose whole verify call runs as the one cooperative
+    kernel (0 disables it, negative restores the default of 4; at most 8),
+    and a cap on that kernel's CTAs (0: as many as the GPU holds).
+    Process-wide, for later calls."""
+    _check("ssd_set_step_schedule",
+           load_library().ssd_set_step_schedule(int(max_b), int(max_grid)))
 
 
 def profile_begin(max_launches: int = 4096):

@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libssd_gb300.so")
 SOURCES = ["ssd_stats.cu", "ssd_residual.cu", "ssd_topk.cu", "ssd_filter.cu", "ssd_tree.cu",
-           "ssd_cache.cu", "ssd_chain.cu", "ssd_api.cu"]
-HEADERS = ["ssd_device.cuh", "ssd_scan.cuh", "ssd_merge.cuh", "ssd_cache.cuh", "ssd_draw.cuh",
+           "ssd_cache.cu", "ssd_chain.cu", "ssd_step.cu", "ssd_api.cu"]
+HEADERS = ["ssd_device.cuh", "ssd_scan.cuh", "ssd_merge.cuh", "ssd_cache.cuh", "ssd_draw.cuh", "ssd_pass.cuh",
            "ssd_layout.h", "exp2_table.inc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

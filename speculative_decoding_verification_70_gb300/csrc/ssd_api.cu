@@ -50,6 +50,7 @@ cudaError_t launch_cache_claim(const CacheView& c, const InsertArgs& a, cudaStre
 cudaError_t launch_cache_write(const CacheView& c, const InsertArgs& a, cudaStream_t s);
 cudaError_t launch_cache_lookup(const CacheView& c, const LookupArgs& a, cudaStream_t s);
 cudaError_t launch_chain(ChainParams p, int dtype, bool vec, cudaStream_t s);
+cudaError_t launch_step(const StepParams& q, int dtype, bool vec, int max_grid, cudaStream_t s);
 }  // namespace ssd
 
 using namespace ssd;
@@ -210,13 +211,15 @@ inline int stats_group(long long rows, int C) {
   return G;
 }
 
+// group > 0 fixes the chunks per CTA of both launches.
 cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s_plain,
-                       cudaStream_t s_topf) {
+                       cudaStream_t s_topf, int group = 0) {
   StatsParams sp = sp0;
   const bool topf = sp.Pdf > 0 && sp.f > 0;
   const bool split = s_plain != s_topf;
   const int rows_plain = topf ? sp.Pz : (split ? sp.Pz : sp.R);
-  sp.G = split_group(stats_group(static_cast<long long>(B) * rows_plain, sp.C), sp.C);
+  sp.G = group > 0 ? group
+                   : split_group(stats_group(static_cast<long long>(B) * rows_plain, sp.C), sp.C);
   cudaError_t e = cudaSuccess;
   if (rows_plain > 0) {
     ProfScope ps("stats", s_plain);
@@ -232,12 +235,33 @@ cudaError_t run_stats2(const StatsParams& sp0, int B, int dtype, bool vec, cudaS
   }
   ProfScope ps("stats_topf", s_topf);
   StatsParams pt = sp;
-  pt.G = split_group(stats_group(static_cast<long long>(B) * sp.Pdf, sp.C), sp.C);
+  pt.G = group > 0 ? group
+                   : split_group(stats_group(static_cast<long long>(B) * sp.Pdf, sp.C), sp.C);
   return launch_stats_rows(pt, B, dtype, vec, sp.Pz, sp.Pdf, true, s_topf);
 }
 
-cudaError_t run_stats(const StatsParams& sp, int B, int dtype, bool vec, cudaStream_t s) {
-  return run_stats2(sp, B, dtype, vec, s, s);
+cudaError_t run_stats(const StatsParams& sp, int B, int dtype, bool vec, cudaStream_t s,
+                      int group = 0) {
+  return run_stats2(sp, B, dtype, vec, s, s, group);
+}
+
+// Chunks per statistics CTA of a verify call: the policy for the target
+// rows' launch of the two-stream schedule (whose draft-row launch uses the
+// same value), so that every schedule streams the same chunk groups and the
+// partial sums, hence p(x) and q(x), are the same bits.
+inline int verify_group(const StatsParams& sp, int B) {
+  return split_group(stats_group(static_cast<long long>(B) * sp.Pz, sp.C), sp.C);
+}
+
+// Every row in one launch (the top-f variant, whose target and
+// statistics-only rows take the plain path): small batches, where a second
+// launch costs more than the rows it would run concurrently.
+cudaError_t run_stats_one(const StatsParams& sp0, int B, int dtype, bool vec, cudaStream_t s) {
+  StatsParams sp = sp0;
+  sp.G = verify_group(sp, B);
+  const bool topf = sp.Pdf > 0 && sp.f > 0;
+  ProfScope ps(topf ? "stats_topf" : "stats", s);
+  return launch_stats_rows(sp, B, dtype, vec, 0, sp.R, topf, s);
 }
 
 cudaError_t cache_insert(const CacheView& v, const InsertArgs& a, cudaStream_t s) {
@@ -445,15 +469,9 @@ bool use_chain(int B) {
   return B <= (ov >= 0 ? ov : SSD_CHAIN_MAX_B);
 }
 
-// The whole tail of a one-slice call as the cluster kernel.
+// The whole tail of a one-slice call as the cluster kernel (the cache, if
+// any, already cleared when the call asks for it).
 cudaError_t enqueue_chain(const VerifyCall& c, const SliceParams& q, bool vec, cudaStream_t s) {
-  cudaError_t e = cudaSuccess;
-  if (c.cache && c.cache_clear) {
-    const size_t kb = sizeof(unsigned long long) * c.cache->capacity;
-    e = cudaMemsetAsync(c.cache->keys, 0xff, kb, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(c.cache->winner, 0, kb, s);
-    if (e != cudaSuccess) return e;
-  }
   ChainParams cp;
   memset(&cp, 0, sizeof cp);
   cp.f = q.fp;
@@ -476,7 +494,6 @@ cudaError_t enqueue_chain(const VerifyCall& c, const SliceParams& q, bool vec, c
 cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool vec,
                          cudaStream_t s, bool last = true, cudaStream_t side = nullptr,
                          cudaEvent_t ev_fin = nullptr, cudaEvent_t ev_ins = nullptr) {
-  if (Bs == c.B && use_chain(c.B)) return enqueue_chain(c, q, vec, s);
   cudaError_t e;
   {
     ProfScope ps("finalize", s);
@@ -521,6 +538,52 @@ cudaError_t enqueue_tail(const VerifyCall& c, const SliceParams& q, int Bs, bool
   return e;
 }
 
+// Largest batch whose whole call runs as the one cooperative kernel
+// (ssd_step.cu; at most kStepMaxB); ssd_set_step_schedule overrides it and
+// can cap the kernel's grid.
+#ifndef SSD_STEP_MAX_B
+#define SSD_STEP_MAX_B 0
+#endif
+std::atomic<int> g_step_max_b{-1};
+std::atomic<int> g_step_grid{0};
+
+bool use_step(int B) {
+  const int ov = g_step_max_b.load(std::memory_order_relaxed);
+  const int lim = ov >= 0 ? ov : SSD_STEP_MAX_B;
+  return B <= lim && B <= kStepMaxB;
+}
+
+// The call as the cooperative kernel.  Returns false (nothing enqueued) if
+// the launch was refused, e.g. because the grid cannot be made resident;
+// the caller then takes the launch-by-launch schedule.
+bool enqueue_step(const VerifyCall& c, bool fork, const WsLayout& L, bool vec, int dtype) {
+  const SliceParams sl = slice_params(c, fork, L, 0, c.B);
+  StepParams q;
+  memset(&q, 0, sizeof q);
+  q.sp = sl.sp;
+  q.sp.G = verify_group(sl.sp, c.B);
+  q.f = sl.fp;
+  q.u_smp = sl.rp.u_smp;
+  q.units = c.B * sl.sp.R * ((sl.sp.C + q.sp.G - 1) / q.sp.G);
+  q.rows = reinterpret_cast<StepRow*>(wsp(c.ws, L.srows));
+  q.cta = reinterpret_cast<long long*>(wsp(c.ws, L.scta));
+  q.bar = reinterpret_cast<StepBar*>(wsp(c.ws, L.sbar));
+  if (c.cache) {
+    q.cache_on = 1;
+    q.cache_clear = c.cache_clear ? 1 : 0;
+    q.cache = *c.cache;
+    q.payload = c.payload;
+    q.hit = c.hit;
+    q.tok_out = c.tok_out;
+  }
+  ProfScope ps("step", c.stream);
+  if (launch_step(q, dtype, vec, g_step_grid.load(std::memory_order_relaxed), c.stream) ==
+      cudaSuccess)
+    return true;
+  (void)cudaGetLastError();
+  return false;
+}
+
 // Schedule: for B >= SSD_MIN_STREAMED_B (every batch by default) the batch
 // is cut into S = max(1, B / SSD_SLICE_ROWS) slices (one slice up to 2047
 // rows).  The target-row and draft-row statistics of each slice run on two
@@ -536,11 +599,27 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
   if (!aligned(c.ws, 256)) return SSD_ERR_INVALID_ARG;
   const bool vec = vec_ok(c.Z, c.zb, c.V, c.dt) && vec_ok(c.D, c.db, c.V, c.dt);
   const int dtype = c.dt == SSD_BF16 ? 1 : 0;
+  if (use_step(c.B) && enqueue_step(c, fork, L, vec, dtype)) return SSD_OK;
+  if (use_chain(c.B)) {
+    // one statistics launch over every row (and the cache clear), then the
+    // cluster kernel: two launches on the caller's stream
+    const SliceParams q = slice_params(c, fork, L, 0, c.B);
+    StatsParams sp = q.sp;
+    if (c.cache && c.cache_clear) {
+      sp.clr_keys = c.cache->keys;
+      sp.clr_winner = c.cache->winner;
+      sp.clr_n = c.cache->capacity;
+    }
+    cudaError_t e = run_stats_one(sp, c.B, dtype, vec, c.stream);
+    if (e == cudaSuccess) e = enqueue_chain(c, q, vec, c.stream);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  }
   const int S = c.single_stream ? 0 : verify_slices(c.B);
   DevStreams* ds = S > 0 ? device_streams() : nullptr;
   if (!ds) {
     const SliceParams q = slice_params(c, fork, L, 0, c.B);
-    if (run_stats(q.sp, c.B, dtype, vec, c.stream) != cudaSuccess) return SSD_ERR_CUDA;
+    if (run_stats(q.sp, c.B, dtype, vec, c.stream, verify_group(q.sp, c.B)) != cudaSuccess)
+      return SSD_ERR_CUDA;
     return enqueue_tail(c, q, c.B, vec, c.stream) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lk(ds->mu);
@@ -553,7 +632,7 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
     const int b0 = static_cast<int>(static_cast<long long>(c.B) * i / S);
     const int b1 = static_cast<int>(static_cast<long long>(c.B) * (i + 1) / S);
     const SliceParams q = slice_params(c, fork, L, b0, b1 - b0);
-    e = run_stats2(q.sp, b1 - b0, dtype, vec, ds->s1, ds->s2);
+    e = run_stats2(q.sp, b1 - b0, dtype, vec, ds->s1, ds->s2, verify_group(q.sp, b1 - b0));
     if (e == cudaSuccess) e = cudaEventRecord(ds->ev[1 + 2 * i], ds->s1);
     if (e == cudaSuccess) e = cudaEventRecord(ds->ev[2 + 2 * i], ds->s2);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[1 + 2 * i], 0);
@@ -1276,6 +1355,13 @@ ssd_status ssd_set_split(int chunk_elems, int chunks_per_cta) {
   if (chunk_elems < 0 || chunks_per_cta < 0) return SSD_ERR_INVALID_ARG;
   g_split.chunk.store(chunk_elems, std::memory_order_relaxed);
   g_split.group.store(chunks_per_cta, std::memory_order_relaxed);
+  return SSD_OK;
+}
+
+ssd_status ssd_set_step_schedule(int max_b, int max_grid) {
+  if (max_grid < 0) return SSD_ERR_INVALID_ARG;
+  g_step_max_b.store(max_b < 0 ? -1 : max_b, std::memory_order_relaxed);
+  g_step_grid.store(max_grid, std::memory_order_relaxed);
   return SSD_OK;
 }
 

@@ -41,16 +41,71 @@ __device__ __forceinline__ int find_slot(const CacheView& c, unsigned long long 
   return -1;
 }
 
+// Insert of one entry by one thread: claim a slot for `key` (bounded linear
+// probe), record the sequence number call << 32 | input index in the slot's
+// winner word and copy the payload.  For callers whose keys are distinct
+// within the call (so this entry's number is the largest the slot has
+// seen): the forks of one verify call.  A full table drops the entry and
+// sets SSD_DEVERR_CACHE_FULL.  The first 8 payload words are loaded before
+// the claim, so the two round trips overlap.
+__device__ __forceinline__ void cache_insert_unique(const CacheView& c, unsigned long long key,
+                                                    unsigned long long seq_idx,
+                                                    const int32_t* src) {
+  int32_t head[8];
+#pragma unroll
+  for (int d = 0; d < 8; ++d)
+    if (d < c.depth) head[d] = src[d];
+  const unsigned mask = static_cast<unsigned>(c.capacity - 1);
+  unsigned h = static_cast<unsigned>(splitmix64(key)) & mask;
+  for (int probe = 0; probe < c.capacity; ++probe) {
+    const unsigned long long prev = atomicCAS(&c.keys[h], kEmptyKey, key);
+    if (prev == kEmptyKey || prev == key) {
+      atomicMax(&c.winner[h], seq_idx);
+      int32_t* dst = c.payload + static_cast<int64_t>(h) * c.depth;
+#pragma unroll
+      for (int d = 0; d < 8; ++d)
+        if (d < c.depth) dst[d] = head[d];
+      for (int d = 8; d < c.depth; ++d) dst[d] = src[d];
+      return;
+    }
+    h = (h + 1) & mask;
+  }
+  atomicOr(c.err, 0x8);
+}
+
 // The realised outcome of batch row b: key (b, pos, tok); hit flag and the
-// entry's depth payload tokens (-1 on a miss).
+// entry's depth payload tokens (-1 on a miss).  The home slot's key and its
+// first 8 payload words are loaded together (one round trip when the key
+// sits in its home slot, the common case).
 __device__ __forceinline__ void cache_lookup_one(const CacheView& c, int b, int pos, int tok,
                                                  int32_t* hit, int32_t* tok_out) {
   unsigned long long key;
   int s = -1;
-  if (make_key(b, pos, tok, key)) s = find_slot(c, key);
+  int32_t head[8];
+  if (make_key(b, pos, tok, key)) {
+    const unsigned mask = static_cast<unsigned>(c.capacity - 1);
+    unsigned h = static_cast<unsigned>(splitmix64(key)) & mask;
+    const int32_t* home = c.payload + static_cast<int64_t>(h) * c.depth;
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+      if (d < c.depth) head[d] = home[d];
+    const unsigned long long k0 = c.keys[h];
+    if (k0 == key) {
+      s = static_cast<int>(h);
+    } else if (k0 != kEmptyKey) {
+      s = find_slot(c, key);
+      const int32_t* src = c.payload + static_cast<int64_t>(s < 0 ? 0 : s) * c.depth;
+#pragma unroll
+      for (int d = 0; d < 8; ++d)
+        if (d < c.depth) head[d] = src[d];
+    }
+  }
   *hit = s >= 0 ? 1 : 0;
   const int32_t* src = c.payload + static_cast<int64_t>(s < 0 ? 0 : s) * c.depth;
-  for (int d = 0; d < c.depth; ++d) tok_out[d] = s >= 0 ? src[d] : -1;
+#pragma unroll
+  for (int d = 0; d < 8; ++d)
+    if (d < c.depth) tok_out[d] = s >= 0 ? head[d] : -1;
+  for (int d = 8; d < c.depth; ++d) tok_out[d] = s >= 0 ? src[d] : -1;
 }
 
 }  // namespace ssd

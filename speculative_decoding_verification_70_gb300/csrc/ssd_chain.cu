@@ -42,6 +42,7 @@ constexpr int kChainThreads = 512;
 constexpr int kChainWarps = kChainThreads / 32;
 constexpr int kChainAmbCap = 1024;   // ambiguous-sign elements kept per CTA
 constexpr int kChainRows = 64;       // 2 (k + 1) <= 64 logit rows per batch row
+constexpr int kAccWarp = 1;          // the warp that takes the acceptance decisions
 
 struct ChainSmem {
   float2 tab[64];
@@ -54,7 +55,10 @@ struct ChainSmem {
   int fl[kChainRows];
   int heads[kChainWarps][256];       // top-f merges
   long long red[kChainWarps];        // block sums and scans
-  long long tot[4];                  // this CTA's S_z, S_d, ambiguous overflow, W
+  // every CTA's S_z, S_d, ambiguous overflow and draw mass, pushed by its
+  // warp 0 into every CTA of the cluster before a cluster barrier (remote
+  // stores: no round trip on the pushing side, local reads after it)
+  long long tot[kChainMaxCluster][4];
   int amb_n;
   int amb[kChainAmbCap];
   long long amb_w[kChainThreads];    // exact residual mass of each thread's ambiguous elements
@@ -101,42 +105,63 @@ __device__ __forceinline__ long long chain_scan(long long v, long long* red, lon
 // the call's sequence number in the slot's winner word as the batched
 // insert does, so that later calls of either path resolve duplicates by
 // call order.
-__device__ void chain_insert(const ChainParams& cp, int b, unsigned long long seq, int rank,
-                             int cs) {
+__device__ void chain_insert(const ChainParams& cp, int b, int rank, int cs) {
   const FinalizeParams& p = cp.f;
   const CacheView& c = cp.cache;
+  // the call's sequence number: no cluster advances the counter before
+  // every cluster has inserted and looked up (the ticket at the end)
+  const unsigned long long seq = (__ldcg(c.calls) + 1ull) << 32;
   const int P = p.k + 1, f = p.f;
   const int per_cta = kChainThreads - 32;
-  const unsigned mask = static_cast<unsigned>(c.capacity - 1);
   for (int e = rank * per_cta + (static_cast<int>(threadIdx.x) - 32); e < P * f; e += cs * per_cta) {
     const int j = e / f;
     const int64_t idx = static_cast<int64_t>(b) * P * f + e;
     unsigned long long key;
     if (!make_key(b, j, p.fork_tok[idx], key)) continue;
-    unsigned h = static_cast<unsigned>(splitmix64(key)) & mask;
-    int slot = -1;
-    for (int probe = 0; probe < c.capacity; ++probe) {
-      const unsigned long long prev = atomicCAS(&c.keys[h], kEmptyKey, key);
-      if (prev == kEmptyKey || prev == key) {
-        slot = static_cast<int>(h);
-        break;
-      }
-      h = (h + 1) & mask;
-    }
-    if (slot < 0) {
-      atomicOr(c.err, 0x8);  // table full: the entry is dropped
-      continue;
-    }
-    atomicMax(&c.winner[slot], seq | static_cast<unsigned long long>(idx));
-    const int32_t* src = cp.payload + idx * c.depth;
-    int32_t* dst = c.payload + static_cast<int64_t>(slot) * c.depth;
-    for (int d = 0; d < c.depth; ++d) dst[d] = src[d];
+    cache_insert_unique(c, key, seq | static_cast<unsigned long long>(idx),
+                        cp.payload + idx * c.depth);
   }
   __threadfence();
 }
 
+// Push v into slot `slot` of this CTA's row of every CTA's tot table (lanes
+// 0 .. cs-1 of warp 0; every lane must hold v).  A cluster barrier follows.
+__device__ __forceinline__ void push_total(cg::cluster_group& cl, ChainSmem& sm, int cs, int rank,
+                                           int slot, long long v) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32 && lane < cs) cl.map_shared_rank(&sm.tot[rank][slot], lane)[0] = v;
+}
+
+// The cluster's total of slot `slot` and the part of the CTAs ranked before
+// this one, from the local copies.
+__device__ __forceinline__ void cluster_prefix(const ChainSmem& sm, int cs, int rank, int slot,
+                                               long long& W, long long& before) {
+  W = 0;
+  before = 0;
+#pragma unroll
+  for (int r = 0; r < kChainMaxCluster; ++r) {
+    const long long v = r < cs ? sm.tot[r][slot] : 0;
+    W += v;
+    if (r < rank) before += v;
+  }
+}
+
+// The cluster's totals of slots 0..2 (S_z, S_d, ambiguous overflow).
+__device__ __forceinline__ void cluster_sums3(const ChainSmem& sm, int cs, long long& a,
+                                              long long& d, long long& o) {
+  a = d = o = 0;
+#pragma unroll
+  for (int r = 0; r < kChainMaxCluster; ++r) {
+    if (r < cs) {
+      a += sm.tot[r][0];
+      d += sm.tot[r][1];
+      o += sm.tot[r][2];
+    }
+  }
+}
+
 template <typename Tag, bool VEC>
-__global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
+__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp) {
   using Elem = typename Tag::Elem;
   const FinalizeParams& p = cp.f;
   __shared__ ChainSmem sm;
@@ -146,29 +171,31 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
   const int b = blockIdx.x / cs;
   const int k = p.k, Pz = p.Pz;
 
-  // what acceptance reads besides the statistics, fetched now so that the
-  // loads overlap the row merges
+  // inputs the statistics pass does not write, fetched before waiting for
+  // it: the temperature (thread 0 turns it into log2(e)/T while the rest
+  // loads the exp2 table) and what acceptance reads besides the statistics
+  // (warp kAccWarp, lane i < k)
+  const float T = p.T[b];
   int xi = -1;
   float zx = 0.f, dx = 0.f, ux = 0.f;
-  if (warp == 0 && lane < k) {
+  if (warp == kAccWarp && lane < k) {
     xi = p.x[static_cast<int64_t>(b) * k + lane];
+    ux = p.u_acc[static_cast<int64_t>(b) * k + lane];
     if (xi >= 0 && xi < p.V) {
       zx = chain_logit(p.Z, p.dtype, static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(lane) * p.V + xi);
       dx = chain_logit(p.D, p.dtype, static_cast<int64_t>(b) * p.db + static_cast<int64_t>(lane) * p.V + xi);
     }
-    ux = p.u_acc[static_cast<int64_t>(b) * k + lane];
   }
-  const unsigned long long seq = cp.cache_on ? ((__ldcg(cp.cache.calls) + 1ull) << 32) : 0ull;
   load_exp2_table(sm.tab);
   if (tid == 0) {
     sm.amb_n = 0;
     sm.res = -1;
   }
-  const float T = p.T[b];
   const bool t_bad = isnan(T) || T < 0.f;
   const bool greedy = !(T > 0.f);
   const float2 c2 = cta_temp_coeff(greedy || t_bad ? 1.f : T, &sm.c2);  // holds a barrier
   const float c_hi = (greedy || t_bad) ? 0.f : c2.x, c_lo = (greedy || t_bad) ? 0.f : c2.y;
+  pdl_wait();  // the statistics pass has completed and its partials are visible
 
   // 1. row merges: cluster-wide warp gw merges row gw (and its forks)
   const int gw = rank * kChainWarps + warp;
@@ -207,51 +234,22 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
   }
   cl.sync();  // every row's statistics in every CTA; the forks in global memory
 
-  // the forks into the cache (every warp but warp 0, beside acceptance)
-  if (cp.cache_on && warp > 0) chain_insert(cp, b, seq, rank, cs);
 
-  // 2. acceptance at each draft position (lane i of warp 0, in every CTA)
-  if (warp == 0) {
-    bool tok_bad = false;
-    if (lane < k) tok_bad = xi < 0 || xi >= p.V;
-    const bool any_tok_bad = __any_sync(kFull, tok_bad);
-    bool row_bad = false;
-    if (lane <= k) row_bad |= (sm.fl[lane] & 2) != 0;
-    if (lane < k) row_bad |= (sm.fl[Pz + lane] & 2) != 0;
-    const bool any_row_bad = __any_sync(kFull, row_bad);
-    int status = 0;
-    if (t_bad) status = -1;
-    else if (any_tok_bad) status = -2;
-    else if (any_row_bad) status = -1;
-    float pv = NAN, qv = NAN;
-    bool acc = false;
-    if (status == 0 && lane < k) {
-      if (greedy) {
-        acc = xi == sm.am[lane];
-        pv = acc ? 1.f : 0.f;
-        qv = xi == sm.am[Pz + lane] ? 1.f : 0.f;
-      } else {
-        float xh, xl, ezh, ezl, edh, edl;
-        arg_df(zx, sm.m[lane], c_hi, c_lo, xh, xl);
-        exp2_df(xh, xl, sm.tab, ezh, ezl);
-        arg_df(dx, sm.m[Pz + lane], c_hi, c_lo, xh, xl);
-        exp2_df(xh, xl, sm.tab, edh, edl);
-        const float Szh = sm.sh[lane], Szl = sm.sl[lane];
-        const float Sdh = sm.sh[Pz + lane], Sdl = sm.sl[Pz + lane];
-        // u < p/q  <=>  u e_d S_z < e_z S_d  (p = e_z / S_z, q = e_d / S_d)
-        float lh, ll, rh, rl;
-        df_mul(edh, edl, Szh, Szl, lh, ll);
-        df_mul(lh, ll, ux, 0.f, lh, ll);
-        df_mul(ezh, ezl, Sdh, Sdl, rh, rl);
-        acc = (edh == 0.f) ? (ezh > 0.f) : (lh < rh || (lh == rh && ll < rl));
-        pv = __fdiv_rn(__fadd_rn(ezh, ezl), __fadd_rn(Szh, Szl));
-        qv = __fdiv_rn(__fadd_rn(edh, edl), __fadd_rn(Sdh, Sdl));
-      }
+  // 2. acceptance at each draft position (lane i of warp kAccWarp, in every CTA)
+  if (warp == kAccWarp) {
+    float mz = 0.f, szh = 0.f, szl = 0.f, md = 0.f, sdh = 0.f, sdl = 0.f;
+    int amz = 0, flz = 0, amd = 0, fld = 0;
+    if (lane <= k) {
+      mz = sm.m[lane]; szh = sm.sh[lane]; szl = sm.sl[lane]; amz = sm.am[lane]; flz = sm.fl[lane];
     }
-    const unsigned ball = __ballot_sync(kFull, acc);
-    const unsigned rej = ~ball & ((1u << k) - 1u);
-    int n = rej ? (__ffs(rej) - 1) : k;
-    if (status != 0) n = status;
+    if (lane < k) {
+      md = sm.m[Pz + lane]; sdh = sm.sh[Pz + lane]; sdl = sm.sl[Pz + lane];
+      amd = sm.am[Pz + lane]; fld = sm.fl[Pz + lane];
+    }
+    const AcceptOut ao = accept_warp(k, p.V, greedy, t_bad, c_hi, c_lo, sm.tab, xi, zx, dx, ux,
+                                     mz, szh, szl, amz, flz, md, sdh, sdl, amd, fld);
+    const int status = ao.status, n = ao.n;
+    const float pv = ao.pv, qv = ao.qv;
     const int mode = (n < 0 || greedy || !cp.u_smp || !p.out_tok)
                          ? kModeNone : (n < k ? kModeResidual : kModeTarget);
     if (rank == 0) {
@@ -278,11 +276,7 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
         bs.pad0 = bs.pad1 = bs.pad2 = 0;
         p.bstate[b] = bs;
         if (p.amb_cnt) p.amb_cnt[b] = 0;
-        int e = 0;
-        if (t_bad) e |= 0x1;
-        else if (any_tok_bad) e |= 0x4;
-        else if (any_row_bad) e |= 0x2;
-        if (e) atomicOr(p.err, e);
+        if (ao.err) atomicOr(p.err, ao.err);
       }
     }
     if (lane == 0) {
@@ -374,20 +368,13 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
     long long tz, td = 0;
     chain_scan(oz, sm.red, &tz);
     if (resid_row) chain_scan(od, sm.red, &td);
-    if (tid == 0) {
-      sm.tot[0] = tz;
-      sm.tot[1] = td;
-      sm.tot[2] = sm.amb_n > kChainAmbCap ? 1 : 0;
-    }
+    push_total(cl, sm, cs, rank, 0, tz);
+    push_total(cl, sm, cs, rank, 1, td);
+    push_total(cl, sm, cs, rank, 2, sm.amb_n > kChainAmbCap ? 1 : 0);
     cl.sync();  // the CTAs' normaliser totals
-    long long Sz = 0, Sd = 0;
-    bool overflow = false;
-    for (int r = 0; r < cs; ++r) {
-      const long long* t = cl.map_shared_rank(sm.tot, r);
-      Sz += t[0];
-      Sd += t[1];
-      overflow = overflow || t[2] != 0;
-    }
+    long long Sz, Sd, ovf;
+    cluster_sums3(sm, cs, Sz, Sd, ovf);
+    const bool overflow = ovf != 0;
     if (tid == 0) {
       // normalisers and their inverses in double-float; the 2^-42 unit
       // scaling is exact
@@ -432,28 +419,18 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
     }
     long long ctot;
     long long incl = chain_scan(own, sm.red, &ctot);
-    if (tid == 0) sm.tot[3] = ctot;
+    push_total(cl, sm, cs, rank, 3, ctot);
     cl.sync();  // the CTAs' masses
-    long long W = 0, before = 0;
-    for (int r = 0; r < cs; ++r) {
-      const long long v = cl.map_shared_rank(sm.tot, r)[3];
-      W += v;
-      if (r < rank) before += v;
-    }
+    long long W, before;
+    cluster_prefix(sm, cs, rank, 3, W, before);
     if (resid && W <= 0) {  // all-zero residual: draw from p_n (uniform over the cluster)
       resid = false;
       own = oz;
       incl = chain_scan(own, sm.red, &ctot);
-      cl.sync();  // every CTA has read the residual totals
-      if (tid == 0) sm.tot[3] = ctot;
+      cl.sync();  // every CTA has read the residual masses
+      push_total(cl, sm, cs, rank, 3, ctot);
       cl.sync();
-      W = 0;
-      before = 0;
-      for (int r = 0; r < cs; ++r) {
-        const long long v = cl.map_shared_rank(sm.tot, r)[3];
-        W += v;
-        if (r < rank) before += v;
-      }
+      cluster_prefix(sm, cs, rank, 3, W, before);
     }
     long long t =
         static_cast<long long>(scale_by_uniform(static_cast<unsigned long long>(W), cp.u_smp[b]));
@@ -467,6 +444,8 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
       sm.base = gincl - own;
     }
     __syncthreads();
+    // the forks into the cache (every warp but warp 0, beside the walk)
+    if (cp.cache_on && warp > 0) chain_insert(cp, b, rank, cs);
     if (sm.pick >= 0 && warp == 0) {  // walk the picked range, one lane per element
       const float scale = resid ? kFixResidual : kFixMass;
       const int gp = rank * kChainThreads + sm.pick;
@@ -503,6 +482,7 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
     cl.sync();  // the token is in rank 0's shared memory
     if (rank == 0 && tid == 0) p.out_tok[static_cast<int64_t>(b) * (k + 1) + n] = sm.res;
   } else {
+    if (cp.cache_on && warp > 0) chain_insert(cp, b, rank, cs);
     cl.sync();  // the insert precedes the lookup (rank 0)
   }
 
@@ -516,7 +496,7 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
     __threadfence();
     if (atomicAdd(cp.cache.done, 1u) == static_cast<unsigned>(p.B) - 1u) {
       *cp.cache.done = 0u;
-      *cp.cache.calls = seq >> 32;
+      *cp.cache.calls = __ldcg(cp.cache.calls) + 1ull;
       __threadfence();
     }
   }
@@ -525,19 +505,38 @@ __global__ void __launch_bounds__(kChainThreads) chain_kernel(ChainParams cp) {
 
 template <typename Tag, bool VEC>
 cudaError_t launch_chain_t(const ChainParams& p, int cs, cudaStream_t s) {
+  static const bool attrs_ok =
+      cudaFuncSetAttribute(chain_kernel<Tag, VEC>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           1) == cudaSuccess;
+  if (!attrs_ok && cs > 8) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.f.B) * cs, 1, 1);
   cfg.blockDim = dim3(kChainThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // the launch overlaps the statistics kernel's tail; the kernel waits
+  // (griddepcontrol.wait) before it reads the partials
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, chain_kernel<Tag, VEC>, p);
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = v;
+  }
+  return n;
 }
 
 }  // namespace
@@ -551,11 +550,15 @@ int chain_elems_per_thread(int V, int cs) {
   return static_cast<int>(E);
 }
 
-// One cluster of up to kChainMaxCluster CTAs per batch row (a smaller
-// cluster when that size cannot be placed).
+// One cluster per batch row: 16 CTAs while the clusters of the batch fit the
+// GPU at one CTA per SM (the kernel's register budget allows no second), else
+// 8 (a smaller cluster again when a size cannot be placed).
 cudaError_t launch_chain(ChainParams p, int dtype, bool vec, cudaStream_t s) {
   if (p.f.B <= 0) return cudaSuccess;
-  for (int cs = kChainMaxCluster;; cs /= 2) {
+  const long long sms = sm_count();
+  int cs = kChainMaxCluster;
+  while (cs > 8 && static_cast<long long>(p.f.B) * cs > sms) cs /= 2;
+  for (;; cs /= 2) {
     p.E = chain_elems_per_thread(p.f.V, cs);
     cudaError_t e;
     if (dtype == 1)

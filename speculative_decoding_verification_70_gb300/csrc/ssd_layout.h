@@ -61,9 +61,37 @@ struct Chunking {
   int E;   // elements per thread in the recovery kernels (multiple of 8)
 };
 
+// The whole verify call of a small batch as one cooperative kernel
+// (ssd_step.cu): the statistics pass, the row merges and forks, acceptance,
+// the two exact passes of the draw over rows n and the select, separated by
+// grid-wide barriers.  At most kStepMaxB batch rows (one warp of a CTA per
+// row at acceptance) and kStepMaxGrid CTAs.
+constexpr int kStepMaxB = 8;
+constexpr int kStepMaxGrid = 2048;
+constexpr int kStepSubBars = 8;
+
+// Merged statistics of one row as the step kernel's acceptance reads them.
+struct StepRow {
+  float m, sh, sl;   // maximum, S as a float pair
+  int argmax, flags;
+  int pad[3];
+};
+
+// Grid barrier words (each on its own 128-byte line): eight arrival
+// sub-counters, the top counter, the generation the waiters poll, the exit
+// ticket and the abort word.  All zero between calls.
+struct StepBar {
+  unsigned sub[kStepSubBars][32];
+  unsigned top[32];
+  unsigned gen[32];
+  unsigned exit_[32];
+  unsigned abort_[32];
+};
+
 // Workspace of the verify / fork / residual calls.
 struct WsLayout {
   size_t err, part, topk, rowstat, bstate, rnorm, rthr, racc, amb_cnt, amb_idx, gpart, total;
+  size_t srows, scta, sbar;   // the step kernel (batches of at most kStepMaxB rows)
   int B, R, Pf, f;
   Chunking ch;
 };
@@ -94,6 +122,11 @@ struct StatsParams {
   // token trees: draft row j is read only if node j has a child (null: all)
   const int32_t* tree_parent;  // [B][tree_N]
   int tree_N;
+  // the SSD round step's cache clear, done by the statistics kernel's CTAs
+  // (the insert runs in a later kernel): clr_n slots of keys / winner words
+  unsigned long long* clr_keys;
+  unsigned long long* clr_winner;
+  int clr_n;
 };
 
 struct FinalizeParams {
@@ -160,13 +193,30 @@ struct ResidualParams {
 // (ssd_chain.cu): one cluster of up to kChainMaxCluster CTAs per batch row
 // does the finalisation, the draw and, in the SSD round step, the cache
 // insert of the row's forks and the lookup of its outcome.
-constexpr int kChainMaxCluster = 8;
+constexpr int kChainMaxCluster = 16;
 
 struct ChainParams {
   FinalizeParams f;
   const float* u_smp;      // [B] or null (no draw)
   int E;                   // elements per thread of the cluster's draw pass (multiple of 8)
   int cache_on;            // SSD round step
+  CacheView cache;
+  const int32_t* payload;  // [B][k+1][f][depth]
+  int32_t* hit;            // [B]
+  int32_t* tok_out;        // [B][depth]
+};
+
+struct StepParams {
+  StatsParams sp;          // the statistics pass (one chunk per unit)
+  FinalizeParams f;        // merges, acceptance, forks, outputs
+  const float* u_smp;      // [B] or null (no draw)
+  int E;                   // elements per thread of the draw passes (multiple of 8)
+  int units;               // statistics units B * sp.R * C, chunk fastest
+  StepRow* rows;           // [B][f.R]
+  long long* cta;          // [3][B][kStepMaxGrid]: per-CTA S_z, S_d and draw mass
+  StepBar* bar;
+  int cache_on;            // SSD round step
+  int cache_clear;         // clear the cache first
   CacheView cache;
   const int32_t* payload;  // [B][k+1][f][depth]
   int32_t* hit;            // [B]
@@ -405,6 +455,10 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
   if (C < c0) C = c0;
   if (C > 256) C = 256;
   if (C < 1) C = 1;
+  // a grid a little above one wave of the statistics kernel (6 CTAs per SM
+  // on 152 SMs) is cut to one wave: the few CTAs of a second wave would
+  // cost a whole CTA latency (e.g. B = 1, 16 rows: 57 chunks, not 63)
+  if (rows * C > 912 && rows * C < 1824 && 912 / rows >= c0) C = 912 / rows;
   long long CH = (V + C - 1) / C;
   const int ov = g_split.chunk.load(std::memory_order_relaxed);
   if (ov > 0) {
@@ -425,6 +479,15 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Every workspace layout starts with the same header: the device error word
+// at offset 0 and the step kernel's barrier words at kWsStepBar.  No other
+// region of any layout overlaps the header, so the barrier words, zero when
+// the workspace is first zero-filled and left zero by every step kernel,
+// stay zero whatever other calls (other shapes, other entry points) use the
+// same workspace in between.
+constexpr size_t kWsStepBar = 256;
+constexpr size_t kWsHeader = (kWsStepBar + sizeof(StepBar) + 255) & ~static_cast<size_t>(255);
+
 // Ambiguous-sign elements kept per row of the draw: a row holds at most V.
 inline int amb_cap(int V) { return V < kAmbCap ? V : kAmbCap; }
 
@@ -437,7 +500,7 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.ch = make_chunking(B, L.R, V, esize);
   const size_t C = static_cast<size_t>(L.ch.C);
   size_t off = 0;
-  L.err = off;                      off = align256(off + 16);
+  L.err = off;                      off = kWsHeader;
   // every region but the forked top-f lists is independent of f, so a
   // workspace sized for (B, k, V, f) serves the f = 0 calls too
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
@@ -449,6 +512,10 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
   L.gpart = off;                    off = align256(off + sizeof(GumbelPart) * B * L.Pf * C);
+  const size_t sb = static_cast<size_t>(B < kStepMaxB ? B : kStepMaxB);
+  L.sbar = kWsStepBar;
+  L.srows = off;                    off = align256(off + sizeof(StepRow) * sb * L.R);
+  L.scta = off;                     off = align256(off + sizeof(long long) * 3 * sb * kStepMaxGrid);
   L.topk = off;                     off = align256(off + sizeof(TopEntry) * B * L.Pf * C * (f > 0 ? f : 0));
   L.total = off;
   return L;
@@ -459,7 +526,7 @@ inline TreeLayout make_tree_layout(int B, int N, int V, int esize = 4) {
   L.R = 2 * N;
   L.ch = make_chunking(B, L.R, V, esize);
   size_t off = 0;
-  L.err = off;                      off = align256(off + 16);
+  L.err = off;                      off = kWsHeader;
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * L.ch.C);
   // per tree V + kTreeCachePad slots (the walk's thread ranges, padded)
   // when rows are long enough for the cache to pay; none otherwise
@@ -475,7 +542,7 @@ inline TopkLayout make_topk_layout(int B, int k, int V, int K, int esize) {
   L.ch = make_chunking(B, 2 * (k + 1), V, esize);
   const size_t C = static_cast<size_t>(L.ch.C);
   size_t off = 0;
-  L.err = off;                      off = align256(off + 16);
+  L.err = off;                      off = kWsHeader;
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
   L.lists = off;                    off = align256(off + sizeof(TopEntry) * B * L.R * C * K);
   L.total = off;
@@ -489,7 +556,7 @@ inline FiltLayout make_filt_layout(int B, int k, int V, int esize = 4) {
   const size_t C = static_cast<size_t>(L.ch.C);
   const size_t rows = static_cast<size_t>(B) * L.R;
   size_t off = 0;
-  L.err = off;                      off = align256(off + 16);
+  L.err = off;                      off = kWsHeader;
   L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
   L.rows = off;                     off = align256(off + sizeof(FiltRow) * rows);
   L.hcnt = off;                     off = align256(off + sizeof(unsigned) * rows * kFiltBins);
@@ -511,12 +578,13 @@ inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
   L.ch = make_chunking(rows, 1, V, esize);
   const size_t C = static_cast<size_t>(L.ch.C);
   size_t off = 0;
-  L.err = off;                      off = align256(off + 16);
+  L.err = off;                      off = kWsHeader;
   L.part = off;                     off = align256(off + sizeof(PartStat) * rows * C);
   L.topk = off;
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * rows);
   L.bstate = off; L.rnorm = off; L.rthr = off; L.racc = off; L.amb_cnt = off; L.amb_idx = off;
-  L.gpart = off;
+  L.gpart = off; L.srows = off; L.scta = off;
+  L.sbar = kWsStepBar;
   L.total = off;
   return L;
 }

@@ -22,390 +22,11 @@
 #include "ssd_device.cuh"
 #include "ssd_layout.h"
 #include "ssd_merge.cuh"
+#include "ssd_pass.cuh"
 #include "ssd_scan.cuh"
 
 
 namespace ssd {
-
-struct StatsSmem {
-  float m[kWarps], s[kWarps];
-  int i[kWarps], n[kWarps];
-  float gy[kWarps];
-  int gi[kWarps];
-  int mask[kMaxMask];
-};
-
-// ---------------------------------------------------------------------------
-// Draft-side sampling: Gumbel-max draws argmax_v (z_v / T - ln(-ln u_v)),
-// an exact draw from softmax(z / T) (the Gumbel-max trick), with u_v from
-// the counter-based generator Philox4x32-10 (Salmon, Moraes, Dror & Shaw
-// 2011): element v of draft row i of batch row b takes word v mod 4 of the
-// generator at counter (v / 4, i, b, offset) under key (seed_lo, seed_hi),
-// and u = (w >> 9 + 1/2) / 2^23 (23 bits: u and 1 - u are exact floats).
-// ---------------------------------------------------------------------------
-struct GumbelArgs {
-  uint32_t k0, k1, row, b, offset;
-  float invT;
-};
-
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-  }
-  return c;
-}
-
-__device__ __forceinline__ float lg2_fast(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// z / T + G for one element: G = -ln(E), E = -ln u.  E is taken from the
-// series v + v^2/2 + ... + v^5/5 of -ln(1 - v), v = 1 - u, when v < 1/16
-// (truncation below v^6/6 relative, < 1e-8), else as -ln 2 * log2(u); both
-// logarithms use the MUFU log2 (absolute error ~2^-22 in log2), so G is off
-// by at most ~2e-6 -- a token can differ from an exact computation only when
-// two perturbed logits tie that closely.
-__device__ __forceinline__ float gumbel_key(float z, float invT, uint32_t w) {
-  const uint32_t m = w >> 9;
-  const float v = (static_cast<float>(8388607u - m) + 0.5f) * 1.1920928955078125e-7f;  // 1 - u
-  constexpr float kLn2 = 0.693147180559945309f;
-  const float u = (static_cast<float>(m) + 0.5f) * 1.1920928955078125e-7f;
-  float s = fmaf(v, 0.2f, 0.25f);
-  s = fmaf(v, s, 0.333333333f);
-  s = fmaf(v, s, 0.5f);
-  s = fmaf(v, s, 1.0f);
-  const float e = v < 0.0625f ? v * s : -kLn2 * lg2_fast(u);
-  return fmaf(z, invT, -kLn2 * lg2_fast(e));
-}
-
-// Fold the kv elements z[0..kv) starting at index `base` into the thread's
-// best (gy, gi); elements arrive in increasing index order, so a strict
-// compare keeps the lowest index on ties.
-template <int KV>
-__device__ __forceinline__ void gumbel_vector(const GumbelArgs& g, const float (&z)[8], int base,
-                                              float& gy, int& gi) {
-  if (KV == 1) {
-    const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(base) >> 2, g.row, g.b, g.offset),
-                                  g.k0, g.k1);
-    const int q = base & 3;
-    const uint32_t word = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
-    const float y = gumbel_key(z[0], g.invT, word);
-    if (y > gy) {
-      gy = y;
-      gi = base;
-    }
-  } else {
-#pragma unroll
-    for (int h = 0; h < KV / 4; ++h) {
-      const uint4 w = philox4x32_10(
-          make_uint4((static_cast<uint32_t>(base) >> 2) + h, g.row, g.b, g.offset), g.k0, g.k1);
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float y = gumbel_key(z[4 * h + e], g.invT, ws[e]);
-        if (y > gy) {
-          gy = y;
-          gi = base + 4 * h + e;
-        }
-      }
-    }
-  }
-}
-
-constexpr int kMaxF = 16;
-
-// Top-f scratch: every thread's maximum, the warps' largest second values
-// and the selection.
-constexpr int kTopfSecond = 256;  // entries of the second-chance buffer
-
-struct TopfScratch {
-  float cv[kThreads];
-  int ci[kThreads];
-  float xv[kTopfSecond];           // second chance: elements of overflowing threads
-  int xi[kTopfSecond];
-  int nx;
-  float w2[kWarps];
-  float sv[kMaxF];
-  int si[kMaxF];
-  float bv[kWarps];
-  int bi[kWarps];
-};
-
-// Best (value, index) among this thread's elements of [lo, hi) (vectors t,
-// t+256, ...) that rank after (pv, pi), skipping masked tokens and NaN.
-template <typename Tag, bool VEC>
-__device__ __forceinline__ void best_after(const typename Tag::Elem* row, int lo, int hi, float pv,
-                                           int pi, const int* msk, int M, float& bv, int& bi) {
-  constexpr int kV = VEC ? Tag::kVec : 1;
-  bv = -INFINITY;
-  bi = kIdxNone;
-  const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
-  for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
-    float z[8];
-    if (VEC) Tag::loadv_cached(row + static_cast<int64_t>(v) * kV, z);
-    else z[0] = Tag::load1(row + v);
-#pragma unroll
-    for (int e = 0; e < kV; ++e) {
-      const int idx = v * kV + e;
-      if (z[e] == z[e] && ranks_before(pv, pi, z[e], idx) && ranks_before(z[e], idx, bv, bi) &&
-          !is_masked(idx, msk, M)) {
-        bv = z[e];
-        bi = idx;
-      }
-    }
-  }
-}
-
-// First half of the top-f selection, before the block reduction of the
-// statistics (whose barrier publishes it): each thread posts its maximum as a
-// candidate (none if masked) and each warp the largest "second value" of its
-// threads -- m2, every element of a thread except its maximum is at most m2;
-// a thread that saw a NaN posts NaN, which sends the CTA to the exact path.
-__device__ __forceinline__ void topf_post(const ScanState& st, const int* msk, int M,
-                                          TopfScratch& ts) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const bool ok = st.idx != kIdxNone && !is_masked(st.idx, msk, M);
-  ts.cv[tid] = ok ? st.m : -INFINITY;
-  ts.ci[tid] = ok ? st.idx : kIdxNone;
-  float w2 = st.nan ? NAN : st.m2;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) w2 = max_nan(w2, __shfl_xor_sync(kFull, w2, o));
-  if (lane == 0) ts.w2[tid >> 5] = w2;
-}
-
-// Top f of the CTA's elements (logit descending, index ascending, masked
-// tokens and NaN skipped).  Warp 0 picks the f best of the 256 posted thread
-// maxima.  Certified: with M2 the largest second value of any thread, every
-// element that is not a thread maximum is at most M2, so if at least f
-// unmasked maxima exceed M2 the picks are exact.  Otherwise (a few percent
-// of CTAs; e.g. several top logits in one vector) a second chance: with tau
-// the f-th pick, every missing element ranks before tau and sits in a thread
-// whose second value is >= tau, so only those threads re-read their own
-// elements and add the ones ranking before tau; the f best of the picks and
-// these extras are exact.  A NaN, fewer than f picks or an overflowing
-// buffer take the last resort: f rounds of a block-wide arg-max.  Needs
-// topf_post and a barrier before it.
-template <typename Tag, bool VEC>
-__device__ void topf_select(const StatsParams& p, const ScanState& st,
-                            const typename Tag::Elem* row, int lo, int hi, const int* msk,
-                            TopEntry* out_top, int n_slots, TopfScratch& ts) {
-  constexpr int kV = VEC ? Tag::kVec : 1;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int f = p.f, M = p.M;
-  float M2 = ts.w2[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) M2 = max_nan(M2, ts.w2[w]);
-  const bool cand = ts.ci[tid] != kIdxNone && ts.cv[tid] > M2;  // false when M2 is NaN
-  if (tid == 0) ts.nx = 0;
-  const bool certified = __syncthreads_count(cand) >= f;
-  if (warp == 0) {
-    float pv = INFINITY;
-    int pi = -1;
-    for (int r = 0; r < f; ++r) {
-      float bv = -INFINITY;
-      int bi = kIdxNone;
-#pragma unroll
-      for (int q = lane; q < kThreads; q += 32) {
-        const float v = ts.cv[q];
-        const int i = ts.ci[q];
-        if (ranks_before(pv, pi, v, i) && ranks_before(v, i, bv, bi)) {
-          bv = v;
-          bi = i;
-        }
-      }
-      warp_argmax(bv, bi);
-      if (lane == 0) {
-        ts.sv[r] = bv;
-        ts.si[r] = bi;
-      }
-      pv = bv;
-      pi = bi;
-    }
-  }
-  // the group's list goes to its first chunk slot; the other slots of the
-  // group get empty entries, which rank last in the merge
-  if (certified) {
-    if (warp != 0) return;
-    __syncwarp();
-    for (int q = lane; q < n_slots * f; q += 32) {
-      const int slot = q / f, r = q % f;
-      out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
-      out_top[q].i = slot == 0 ? ts.si[r] : kIdxNone;
-    }
-    return;
-  }
-  __syncthreads();
-  const float tv = ts.sv[f - 1];
-  const int ti = ts.si[f - 1];
-  const bool second = ti != kIdxNone && M2 == M2;
-  if (second && st.m2 >= tv) {
-    const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
-    for (int v = v0 + tid; v < v1; v += kThreads) {
-      float z[8];
-      if (VEC) Tag::loadv_cached(row + static_cast<int64_t>(v) * kV, z);
-      else z[0] = Tag::load1(row + v);
-#pragma unroll
-      for (int e = 0; e < kV; ++e) {
-        const int idx = v * kV + e;
-        if (idx != ts.ci[tid] && z[e] == z[e] && ranks_before(z[e], idx, tv, ti) &&
-            !is_masked(idx, msk, M)) {
-          const int q = atomicAdd(&ts.nx, 1);
-          if (q < kTopfSecond) {
-            ts.xv[q] = z[e];
-            ts.xi[q] = idx;
-          }
-        }
-      }
-    }
-  }
-  __syncthreads();
-  const int nx = ts.nx;
-  if (second && nx <= kTopfSecond) {
-    if (warp != 0) return;
-    float pv = INFINITY;
-    int pi = -1;
-    float keep_v = -INFINITY;
-    int keep_i = kIdxNone;
-    for (int r = 0; r < f; ++r) {
-      float bv = -INFINITY;
-      int bi = kIdxNone;
-      for (int q = lane; q < f + nx; q += 32) {
-        const float v = q < f ? ts.sv[q] : ts.xv[q - f];
-        const int i = q < f ? ts.si[q] : ts.xi[q - f];
-        if (i != kIdxNone && ranks_before(pv, pi, v, i) && ranks_before(v, i, bv, bi)) {
-          bv = v;
-          bi = i;
-        }
-      }
-      warp_argmax(bv, bi);
-      if (lane == r) {
-        keep_v = bv;
-        keep_i = bi;
-      }
-      pv = bv;
-      pi = bi;
-    }
-    __syncwarp();
-    if (lane < f) {
-      ts.sv[lane] = keep_i == kIdxNone ? -INFINITY : keep_v;
-      ts.si[lane] = keep_i;
-    }
-    __syncwarp();
-    for (int q = lane; q < n_slots * f; q += 32) {
-      const int slot = q / f, r = q % f;
-      out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
-      out_top[q].i = slot == 0 ? ts.si[r] : kIdxNone;
-    }
-    return;
-  }
-  // last resort: f rounds of a block-wide arg-max over [lo, hi)
-  float pv = INFINITY;
-  int pi = -1;
-  for (int r = 0; r < f; ++r) {
-    float bv;
-    int bi;
-    best_after<Tag, VEC>(row, lo, hi, pv, pi, msk, M, bv, bi);
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      ts.bv[warp] = bv;
-      ts.bi[warp] = bi;
-    }
-    __syncthreads();
-    bv = ts.bv[0];
-    bi = ts.bi[0];
-    for (int w = 1; w < kWarps; ++w)
-      if (ranks_before(ts.bv[w], ts.bi[w], bv, bi)) {
-        bv = ts.bv[w];
-        bi = ts.bi[w];
-      }
-    __syncthreads();
-    if (tid == 0) {
-      ts.sv[r] = bv;
-      ts.si[r] = bi;
-    }
-    pv = bv;
-    pi = bi;
-  }
-  __syncthreads();
-  for (int q = tid; q < n_slots * f; q += kThreads) {
-    const int slot = q / f, r = q % f;
-    out_top[q].v = slot == 0 ? ts.sv[r] : -INFINITY;
-    out_top[q].i = slot == 0 ? ts.si[r] : kIdxNone;
-  }
-}
-
-template <typename Tag, bool VEC, bool DO_EXP, bool TOPF, bool GUMBEL = false>
-__device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row, int lo, int hi,
-                            float c, PartStat* out_part, TopEntry* out_top, int n_slots,
-                            StatsSmem& sm, TopfScratch* ts, const GumbelArgs* ga = nullptr,
-                            GumbelPart* out_g = nullptr) {
-  constexpr int kV = VEC ? Tag::kVec : 1;
-  constexpr int U = 4;
-  const int tid = threadIdx.x;
-  ScanState st;
-  scan_init(st);
-  float gy = -INFINITY;
-  int gi = kIdxNone;
-  const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
-  for (int vb = v0 + tid; vb < v1; vb += kThreads * U) {
-    typename Tag::Raw raw[U];
-    float sc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = vb + u * kThreads;
-      if (vi < v1) {
-        if (VEC) raw[u] = Tag::loadraw(row + static_cast<int64_t>(vi) * kV);
-        else sc[u] = Tag::load1(row + vi);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = vb + u * kThreads;
-      if (vi < v1) {
-        float z[8];
-        if (VEC) Tag::unpackraw(raw[u], z);
-        else z[0] = sc[u];
-        float m = z[0];
-#pragma unroll
-        for (int e = 1; e < kV; ++e) m = max_nan(m, z[e]);
-        scan_vector<DO_EXP, TOPF>(st, z, kV, m, vi * kV, c);
-        if constexpr (GUMBEL) gumbel_vector<kV>(*ga, z, vi * kV, gy, gi);
-      }
-    }
-  }
-  if constexpr (GUMBEL) {
-    warp_argmax(gy, gi);
-    if ((tid & 31) == 0) {
-      sm.gy[tid >> 5] = gy;
-      sm.gi[tid >> 5] = gi;
-    }
-  }
-  if constexpr (TOPF) topf_post(st, sm.mask, p.M, *ts);
-  block_stats_write(st, c, DO_EXP, sm.m, sm.s, sm.i, sm.n, out_part);  // holds a barrier
-  if constexpr (GUMBEL) {
-    if (tid == 0) {
-      GumbelPart g;
-      g.y = sm.gy[0];
-      g.idx = sm.gi[0];
-      for (int w = 1; w < kWarps; ++w)
-        if (ranks_before(sm.gy[w], sm.gi[w], g.y, g.idx)) {
-          g.y = sm.gy[w];
-          g.idx = sm.gi[w];
-        }
-      *out_g = g;
-    }
-  }
-  if constexpr (TOPF) topf_select<Tag, VEC>(p, st, row, lo, hi, sm.mask, out_top, n_slots, *ts);
-}
 
 // grid: (C, rows of this launch, B).  Resident CTAs per SM requested from
 // the register allocator: enough 16-byte loads in flight to saturate HBM.
@@ -425,6 +46,16 @@ __global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : 6)
   const int hi = min(p.V, lo + G * p.CH);
   const int n_slots = min(G, p.C - c);
   __shared__ StatsSmem sm;
+  pdl_trigger();  // a dependent kernel launched with programmatic serialization may start
+  if (p.clr_n > 0) {  // the speculation cache's clear, spread over the grid
+    const long long cta = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                           (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+    const long long nt = static_cast<long long>(gridDim.x) * gridDim.y * gridDim.z * kThreads;
+    for (long long i = cta * kThreads + threadIdx.x; i < p.clr_n; i += nt) {
+      p.clr_keys[i] = 0xffffffffffffffffull;
+      p.clr_winner[i] = 0ull;
+    }
+  }
 
   const Elem* row;
   bool need_stats, need_top = false;
@@ -717,55 +348,29 @@ __global__ void __launch_bounds__(NW * 32) finalize_kernel(FinalizeParams p) {
   // 2. acceptance at each draft position (lane i), first-reject prefix
   const int k = p.k;
   int xi = -1;
-  bool tok_bad = false;
+  float zx = 0.f, dx = 0.f, ux = 0.f;
   if (lane < k) {
     xi = p.x[static_cast<int64_t>(b) * k + lane];
-    tok_bad = xi < 0 || xi >= p.V;
-  }
-  bool any_tok_bad = __any_sync(kFull, tok_bad);
-  bool row_bad = false;
-  if (lane <= k) row_bad |= (rs[lane].flags & 2) != 0;                 // target rows 0..k
-  if (lane < k) row_bad |= (rs[p.Pz + lane].flags & 2) != 0;           // draft rows 0..k-1
-  bool any_row_bad = __any_sync(kFull, row_bad);
-
-  int status = 0;  // 0 ok, -1 invalid, -2 bad token
-  if (t_bad) status = -1;
-  else if (any_tok_bad) status = -2;
-  else if (any_row_bad) status = -1;
-
-  float pv = NAN, qv = NAN;
-  bool acc = false;
-  if (status == 0 && lane < k) {
-    const RowStat& tz = rs[lane];
-    const RowStat& td = rs[p.Pz + lane];
-    if (greedy) {
-      acc = (xi == tz.argmax);
-      pv = acc ? 1.f : 0.f;
-      qv = (xi == td.argmax) ? 1.f : 0.f;
-    } else {
-      float zx = logit_at(p.Z, p.dtype, static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(lane) * p.V + xi);
-      float dx = logit_at(p.D, p.dtype, static_cast<int64_t>(b) * p.db + static_cast<int64_t>(lane) * p.V + xi);
-      float xh, xl, ezh, ezl, edh, edl;
-      arg_df(zx, tz.m, c_hi, c_lo, xh, xl);
-      exp2_df(xh, xl, tab, ezh, ezl);
-      arg_df(dx, td.m, c_hi, c_lo, xh, xl);
-      exp2_df(xh, xl, tab, edh, edl);
-      const float2 Sz = rsum[lane], Sd = rsum[p.Pz + lane];
-      const float u = p.u_acc[static_cast<int64_t>(b) * k + lane];
-      // u < p/q  <=>  u e_d S_z < e_z S_d  (p = e_z / S_z, q = e_d / S_d)
-      float lh, ll, rh, rl;
-      df_mul(edh, edl, Sz.x, Sz.y, lh, ll);
-      df_mul(lh, ll, u, 0.f, lh, ll);
-      df_mul(ezh, ezl, Sd.x, Sd.y, rh, rl);
-      acc = (edh == 0.f) ? (ezh > 0.f) : (lh < rh || (lh == rh && ll < rl));
-      pv = __fdiv_rn(__fadd_rn(ezh, ezl), __fadd_rn(Sz.x, Sz.y));
-      qv = __fdiv_rn(__fadd_rn(edh, edl), __fadd_rn(Sd.x, Sd.y));
+    ux = p.u_acc[static_cast<int64_t>(b) * k + lane];
+    if (!greedy && xi >= 0 && xi < p.V) {
+      zx = logit_at(p.Z, p.dtype, static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(lane) * p.V + xi);
+      dx = logit_at(p.D, p.dtype, static_cast<int64_t>(b) * p.db + static_cast<int64_t>(lane) * p.V + xi);
     }
   }
-  unsigned ball = __ballot_sync(kFull, acc);
-  unsigned rej = ~ball & ((1u << k) - 1u);
-  int n = rej ? (__ffs(rej) - 1) : k;
-  if (status != 0) n = status;
+  float mz = 0.f, md = 0.f;
+  float2 sz = make_float2(0.f, 0.f), sd = make_float2(0.f, 0.f);
+  int amz = 0, flz = 0, amd = 0, fld = 0;
+  if (lane <= k) {
+    mz = rs[lane].m; amz = rs[lane].argmax; flz = rs[lane].flags; sz = rsum[lane];
+  }
+  if (lane < k) {
+    md = rs[p.Pz + lane].m; amd = rs[p.Pz + lane].argmax; fld = rs[p.Pz + lane].flags;
+    sd = rsum[p.Pz + lane];
+  }
+  const AcceptOut ao = accept_warp(k, p.V, greedy, t_bad, c_hi, c_lo, tab, xi, zx, dx, ux, mz,
+                                   sz.x, sz.y, amz, flz, md, sd.x, sd.y, amd, fld);
+  const int status = ao.status, n = ao.n;
+  const float pv = ao.pv, qv = ao.qv;
 
   if (lane < k && p.p_at_x) {
     p.p_at_x[static_cast<int64_t>(b) * k + lane] = (status == 0) ? pv : NAN;
@@ -790,11 +395,7 @@ __global__ void __launch_bounds__(NW * 32) finalize_kernel(FinalizeParams p) {
     bs.pad0 = bs.pad1 = bs.pad2 = 0;
     p.bstate[b] = bs;
     if (p.amb_cnt) p.amb_cnt[b] = 0;
-    int e = 0;
-    if (t_bad) e |= 0x1;
-    else if (any_tok_bad) e |= 0x4;
-    else if (any_row_bad) e |= 0x2;
-    if (e) atomicOr(p.err, e);
+    if (ao.err) atomicOr(p.err, ao.err);
   }
 }
 

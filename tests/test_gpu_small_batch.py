@@ -1,19 +1,24 @@
-"""The small-batch schedule of the verify step.
+"""The small-batch schedules of the verify step.
 
-After the statistics pass, a batch of at most a few rows runs its
-finalisation (row merges, acceptance min(1, p/q), the first-reject prefix,
-the forked top-f), the recovery / bonus draw and, in the SSD round step, the
-cache insert of its forks and the lookup of its realised outcome as one
-kernel: one thread-block cluster per batch row.  Larger batches run the
-same steps as separate batched kernels.
+A verify call of a few batch rows moves a few MB; its time is its chain of
+dependent launches.  Two schedules shorten that chain:
+  - step: the whole call (statistics pass, row merges and forks, acceptance,
+    the draw's exact passes, select, cache clear / insert / lookup) as one
+    cooperative kernel whose CTAs meet at grid-wide barriers (B <= 8);
+  - chain: after the statistics pass, one thread-block cluster per batch
+    row does the finalisation, the draw and the cache step (one launch).
+Larger batches run the same steps as separate batched kernels.
 
-These tests run both schedules on the same inputs (ssd_set_chain_batch picks
-one) and check that accept lengths, p(x), q(x), forks, drawn tokens and cache
-lookups are the same bits, and that both agree with the oracle: on short and
-long vocabularies, unaligned rows, the largest k and f, batches of more
-clusters than fit the GPU at once, CUDA graph replays of the B = 1 round
-step, and the draw's degenerate rows (near-equal target and draft rows, whose
-sign split overflows; u at the ends; greedy, invalid and NaN rows).
+These tests run every schedule on the same inputs (ssd_set_step_schedule
+and ssd_set_chain_batch pick one) and check that accept lengths, p(x), q(x),
+forks, drawn tokens and cache lookups are the same bits as the batched
+kernels', and that they agree with the oracle: on short and long
+vocabularies, unaligned rows, the largest k and f, batches of more clusters
+than fit the GPU at once, a step grid far smaller than the work (many units
+per CTA), CUDA graph replays of the B = 1 round step, the draw's degenerate
+rows (near-equal target and draft rows; u at the ends; greedy, invalid and
+NaN rows), and a barrier wait that runs out (the kernel reports
+SSD_DEVERR_TIMEOUT and leaves the workspace usable).
 """
 import numpy as np
 import pytest
@@ -25,12 +30,24 @@ from speculative_decoding_verification_70_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-CHAIN, BATCHED = 1 << 20, 0
+
+# (step max batch, step grid cap, chain max batch)
+SCHEDULES = {
+    "step": (8, 0, 0),
+    "step_g40": (8, 40, 0),      # 40 CTAs: several statistics units per CTA, long ranges
+    "chain": (0, 0, 1 << 20),
+    "batched": (0, 0, 0),
+}
 
 
 @pytest.fixture
 def schedule(gpu_lib):
-    yield gpu_lib.set_chain_batch
+    def pick(name):
+        mb, grid, chain = SCHEDULES[name]
+        gpu_lib.set_step_schedule(mb, grid)
+        gpu_lib.set_chain_batch(chain)
+    yield pick
+    gpu_lib.set_step_schedule(-1, 0)
     gpu_lib.set_chain_batch(-1)
 
 
@@ -38,9 +55,9 @@ def _bits(t):
     return t.view(torch.int32) if t.dtype == torch.float32 else t
 
 
-def _same(a, b, keys):
+def _same(a, b, keys, label=""):
     for key in keys:
-        assert torch.equal(_bits(a[key]), _bits(b[key])), key
+        assert torch.equal(_bits(a[key]), _bits(b[key])), (label, key)
 
 
 def _verify(gpu_lib, w, inp):
@@ -77,21 +94,23 @@ CASES = [
 
 
 @pytest.mark.parametrize("name,over,temp", CASES)
-def test_chain_equals_batched_and_oracle(gpu_lib, schedule, name, over, temp):
+def test_schedules_agree_and_match_oracle(gpu_lib, schedule, name, over, temp):
     w = W.workload(name, **over)
     inp = W.make_inputs(w, device=DEV, seed=W.default_seed(name) + 311, temp=temp)
-    schedule(CHAIN)
-    a = _verify(gpu_lib, w, inp)
-    schedule(BATCHED)
-    b = _verify(gpu_lib, w, inp)
-    _same(a, b, KEYS + (FORK_KEYS if w.f > 0 else ()))
-    assert a["err"] == b["err"]
+    outs = {}
+    for sched in SCHEDULES:
+        schedule(sched)
+        outs[sched] = _verify(gpu_lib, w, inp)
+    ref = outs["batched"]
+    for sched, o in outs.items():
+        _same(o, ref, KEYS + (FORK_KEYS if w.f > 0 else ()), sched)
+        assert o["err"] == ref["err"], sched
     bs = np.arange(w.B)
-    rep = compare_verify(inp, a, bs, oracle_rows(inp, bs), Report())
+    rep = compare_verify(inp, ref, bs, oracle_rows(inp, bs), Report())
     assert not rep.failures, rep.failures[:3]
     if w.f > 0:
         rf = oracle.forked_topf(inp["D"].cpu(), w.f, inp["mask"].cpu())
-        compare_forks(rf, a["fork_tok"], a["fork_logit"], name)
+        compare_forks(rf, ref["fork_tok"], ref["fork_logit"], name)
 
 
 def _round(gpu_lib, w, inp, cache, payload, clear):
@@ -104,10 +123,10 @@ def _round(gpu_lib, w, inp, cache, payload, clear):
 
 @pytest.mark.parametrize("name,over", [("ssd_fork", {}), ("qwen_b64", {"B": 8}),
                                        ("tiny", {"B": 8, "V": 8000, "temp": "mixed"})])
-def test_chain_round_step_equals_batched(gpu_lib, schedule, name, over):
+def test_round_step_schedules_agree(gpu_lib, schedule, name, over):
     """Two SSD round steps into one cache, the second without a clear: the
     later call's payload wins for keys both calls insert, whichever schedule
-    ran each call."""
+    ran each call (the schedules share the cache's call counter)."""
     w = W.workload(name, **over)
     inp = W.make_inputs(w, device=DEV, seed=W.default_seed(name) + 97)
     depth = 4
@@ -115,7 +134,9 @@ def test_chain_round_step_equals_batched(gpu_lib, schedule, name, over):
     cap = 1 << max(6, (4 * n - 1).bit_length())
     pay = torch.arange(n * depth, dtype=torch.int32, device=DEV).reshape(n, depth)
     results = {}
-    for order in ((CHAIN, CHAIN), (BATCHED, BATCHED), (CHAIN, BATCHED), (BATCHED, CHAIN)):
+    for order in (("batched", "batched"), ("step", "step"), ("chain", "chain"),
+                  ("step", "batched"), ("batched", "step"), ("chain", "step"),
+                  ("step_g40", "chain")):
         cache = gpu_lib.SpecCache(cap, depth)
         outs = []
         for rep, sched in enumerate(order):
@@ -124,10 +145,10 @@ def test_chain_round_step_equals_batched(gpu_lib, schedule, name, over):
         assert cache.error() == 0
         cache.close()
         results[order] = outs
-    ref = results[(BATCHED, BATCHED)]
+    ref = results[("batched", "batched")]
     for order, outs in results.items():
         for r in range(2):
-            _same(outs[r], ref[r], KEYS + FORK_KEYS + ("hit", "tok_out"))
+            _same(outs[r], ref[r], KEYS + FORK_KEYS + ("hit", "tok_out"), order)
     # against the dict cache: the second call's entries replace the first's
     out = ref[1]
     c = oracle.SpecCacheOracle(depth)
@@ -145,7 +166,7 @@ def test_chain_round_step_equals_batched(gpu_lib, schedule, name, over):
     assert np.array_equal(to_np(out["tok_out"]), tout)
 
 
-def test_chain_degenerate_rows(gpu_lib, schedule):
+def test_degenerate_rows_every_schedule(gpu_lib, schedule):
     """Rows the draw treats specially, through both schedules and the oracle:
     near-equal target and draft rows rejected at position 0 (every element's
     sign is ambiguous, so the split overflows and the residual is summed
@@ -173,12 +194,14 @@ def test_chain_degenerate_rows(gpu_lib, schedule):
     inp = {"Z": Z.to(DEV), "D": D.contiguous().to(DEV), "x": x.to(DEV), "T": T.to(DEV),
            "u_acc": u_acc.to(DEV), "u_smp": u_smp.to(DEV)}
     w = W.workload("tiny", B=B, k=k, V=V, f=0)
-    schedule(CHAIN)
-    a = _verify(gpu_lib, w, inp)
-    schedule(BATCHED)
-    b = _verify(gpu_lib, w, inp)
-    _same(a, b, KEYS)
-    assert a["err"] == b["err"]
+    outs = {}
+    for sched in SCHEDULES:
+        schedule(sched)
+        outs[sched] = _verify(gpu_lib, w, inp)
+    a = outs["batched"]
+    for sched, o in outs.items():
+        _same(o, a, KEYS, sched)
+        assert o["err"] == a["err"], sched
     assert a["err"] == (gpu_lib.DEVERR_BAD_TEMPERATURE | gpu_lib.DEVERR_BAD_TOKEN |
                         gpu_lib.DEVERR_BAD_LOGITS)
     acc = to_np(a["accept_len"])
@@ -202,12 +225,12 @@ def _capture(fn):
     return graph
 
 
-@pytest.mark.parametrize("temp", ["1.0", "0"])
-def test_chain_round_step_graph_replay(gpu_lib, schedule, temp):
-    """The B = 1 round step (one statistics pass, then the cluster kernel
-    with the cache clear, insert and lookup) captured once and replayed with
-    new inputs: each replay against the oracle and the dict cache."""
-    schedule(-1)  # the default schedule: B = 1 takes the cluster kernel
+@pytest.mark.parametrize("sched,temp", [("step", "1.0"), ("step", "0"), ("chain", "1.0")])
+def test_round_step_graph_replay(gpu_lib, schedule, sched, temp):
+    """The B = 1 round step (verify, forks, cache clear, insert and lookup)
+    captured once as a CUDA graph and replayed with new inputs: each replay
+    against the oracle and the dict cache."""
+    schedule(sched)
     w = W.workload("ssd_fork")
     depth = 7
     static = W.make_inputs(w, device=DEV, seed=400, temp=temp)
@@ -246,3 +269,29 @@ def test_chain_round_step_graph_replay(gpu_lib, schedule, temp):
     assert rep.sampled_mismatch == 0
     assert cache.error() == 0
     cache.close()
+
+
+def test_step_barrier_timeout_is_reported(gpu_lib, schedule):
+    """A grid barrier whose wait cannot end: the workspace's first arrival
+    sub-counter is planted at a value the count never reaches, so no CTA
+    completes the first barrier.  Every wait gives up after its time limit,
+    the call reports SSD_DEVERR_TIMEOUT, the kernel's exit puts the barrier
+    words back to zero, and the next call on the same workspace is right."""
+    schedule("step")
+    w = W.workload("tiny", B=2, V=4096, temp="1.0")
+    inp = W.make_inputs(w, device=DEV, seed=8)
+    ws = gpu_lib.new_workspace(gpu_lib.workspace_bytes(w.B, w.k, w.V, w.f), DEV)
+    base = (-ws.data_ptr()) % 256          # the binding aligns the workspace to 256 bytes
+    bar = ws[base + 256: base + 260]       # sub-counter 0 of the barrier words
+    bar.copy_(torch.tensor([0x00, 0x00, 0x00, 0x40], dtype=torch.uint8, device=DEV))
+    args = (inp["Z"], inp["D"], inp["x"], inp["T"], inp["u_acc"], inp["u_smp"], w.f, inp["mask"])
+    gpu_lib.ssd_verify_fork(*args, ws=ws)
+    torch.cuda.synchronize()
+    assert gpu_lib.get_device_error(ws, clear=True) & gpu_lib.DEVERR_TIMEOUT
+    assert int(bar.sum()) == 0
+    out = gpu_lib.ssd_verify_fork(*args, ws=ws)
+    torch.cuda.synchronize()
+    assert gpu_lib.get_device_error(ws, clear=True) == 0
+    ref = oracle_rows(inp, np.arange(w.B))
+    rep = compare_verify(inp, out, np.arange(w.B), ref, Report())
+    assert not rep.failures, rep.failures[:3]
