@@ -28,9 +28,27 @@ constexpr double kInvFixMass = 1.0 / 4398046511104.0;
 // Logit element types.  bf16 is the upper half of a binary32, so widening is
 // a 16-bit shift.
 // ---------------------------------------------------------------------------
+// Loads in flight per thread of the streaming pass (vectors issued before
+// the first is used) and the resident CTAs per SM its register budget is
+// cut for, per element type.
+#ifndef SSD_STATS_UNROLL_F32
+#define SSD_STATS_UNROLL_F32 4
+#endif
+#ifndef SSD_STATS_UNROLL_BF16
+#define SSD_STATS_UNROLL_BF16 4
+#endif
+#ifndef SSD_STATS_BLOCKS_F32
+#define SSD_STATS_BLOCKS_F32 6
+#endif
+#ifndef SSD_STATS_BLOCKS_BF16
+#define SSD_STATS_BLOCKS_BF16 6
+#endif
+
 struct F32Tag {
   using Elem = float;
   static constexpr int kVec = 4;  // elements per 16-byte vector
+  static constexpr int kUnroll = SSD_STATS_UNROLL_F32;
+  static constexpr int kBlocks = SSD_STATS_BLOCKS_F32;
   using Raw = float4;
   __device__ __forceinline__ static float load1(const Elem* p) { return __ldg(p); }
   __device__ __forceinline__ static Raw loadraw(const Elem* p) {
@@ -60,6 +78,8 @@ struct F32Tag {
 struct BF16Tag {
   using Elem = uint16_t;
   static constexpr int kVec = 8;
+  static constexpr int kUnroll = SSD_STATS_UNROLL_BF16;
+  static constexpr int kBlocks = SSD_STATS_BLOCKS_BF16;
   using Raw = uint4;
   __device__ __forceinline__ static Raw loadraw(const Elem* p) {
     uint4 v;

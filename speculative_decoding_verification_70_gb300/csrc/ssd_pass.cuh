@@ -2,7 +2,8 @@
 // the online-softmax statistics (maximum, lowest argmax, NaN flag, sum of
 // 2^((z - m) c); Milakov & Gimelshein 2018), the certified top-f of the
 // chunk for the forked recovery (masked tokens skipped) and, for the
-// drafter's own sampling, the best Gumbel-perturbed logit.  Shared by the
+// drafter's own sampling, the best Gumbel-perturbed logit; and one CTA's
+// whole unit of the verify statistics (stats_unit).  Shared by the
 // statistics kernels (ssd_stats.cu) and the small-batch step kernel
 // (ssd_step.cu).
 #pragma once
@@ -337,7 +338,7 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
                             StatsSmem& sm, TopfScratch* ts, const GumbelArgs* ga = nullptr,
                             GumbelPart* out_g = nullptr) {
   constexpr int kV = VEC ? Tag::kVec : 1;
-  constexpr int U = 4;
+  constexpr int U = Tag::kUnroll;
   const int tid = threadIdx.x;
   ScanState st;
   scan_init(st);
@@ -395,4 +396,59 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
   if constexpr (TOPF) topf_select<Tag, VEC>(p, st, row, lo, hi, sm.mask, out_top, n_slots, *ts);
 }
 
+// Statistics of chunks c .. c + G - 1 of logit row r of batch row b (the
+// work of one CTA of the statistics kernel; G = p.G): one partial record for
+// the group in slot c, identity records in the group's other slots, and for
+// a draft row below Pdf its top-f list.  Uniform over the CTA; holds
+// barriers.
+template <typename Tag, bool VEC>
+__device__ __forceinline__ void stats_unit(const StatsParams& p, int b, int r, int c, StatsSmem& sm,
+                                           TopfScratch& ts, float2* s_c) {
+  using Elem = typename Tag::Elem;
+  const int lo = c * p.CH, hi = min(p.V, lo + p.G * p.CH);
+  const int n_slots = min(p.G, p.C - c);
+  const Elem* row;
+  bool need_stats, need_top = false;
+  int j = 0;
+  if (r < p.Pz) {
+    row = static_cast<const Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(r) * p.V;
+    need_stats = true;
+  } else {
+    j = r - p.Pz;
+    row = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db + static_cast<int64_t>(j) * p.V;
+    need_stats = j < p.Pds;
+    need_top = p.f > 0 && j < p.Pdf;
+    if (!need_stats && !need_top) return;
+  }
+  const float T = p.T ? p.T[b] : 0.f;
+  const bool do_exp = need_stats && T > 0.f;  // uniform over the CTA
+  float cf = 0.f;
+  if (do_exp) cf = cta_temp_coeff(T, s_c).x;
+  PartStat* out_part = p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C + c;
+  if (threadIdx.x > 0 && threadIdx.x < n_slots) {
+    PartStat id;
+    id.m = -INFINITY;
+    id.s = 0.f;
+    id.idx = kIdxNone;
+    id.flags = 0;
+    out_part[threadIdx.x] = id;
+  }
+  if (need_top) {
+    if (threadIdx.x < p.M)
+      sm.mask[threadIdx.x] = p.mask[(static_cast<int64_t>(b) * p.Pdf + j) * p.M + threadIdx.x];
+    __syncthreads();
+    TopEntry* out_top = p.topk + ((static_cast<int64_t>(b) * p.Pdf + j) * p.C + c) * p.f;
+    if (do_exp)
+      stats_chunk<Tag, VEC, true, true>(p, row, lo, hi, cf, out_part, out_top, n_slots, sm, &ts);
+    else
+      stats_chunk<Tag, VEC, false, true>(p, row, lo, hi, cf, out_part, out_top, n_slots, sm, &ts);
+    return;
+  }
+  if (do_exp)
+    stats_chunk<Tag, VEC, true, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm, nullptr);
+  else
+    stats_chunk<Tag, VEC, false, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm, nullptr);
+}
+
 }  // namespace ssd
+

@@ -31,10 +31,10 @@ namespace ssd {
 // grid: (C, rows of this launch, B).  Resident CTAs per SM requested from
 // the register allocator: enough 16-byte loads in flight to saturate HBM.
 #ifndef SSD_TOPF_MIN_BLOCKS
-#define SSD_TOPF_MIN_BLOCKS 6
+#define SSD_TOPF_MIN_BLOCKS Tag::kBlocks
 #endif
 template <typename Tag, bool VEC, bool HAS_TOPF>
-__global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : 6)
+__global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : Tag::kBlocks)
     stats_kernel(StatsParams p) {
   using Elem = typename Tag::Elem;
   // A CTA of the plain variant covers p.G consecutive chunks: one reduction

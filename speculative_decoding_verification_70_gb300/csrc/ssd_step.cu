@@ -138,59 +138,6 @@ struct StepSmem {
   int flag;
 };
 
-// Statistics of chunks c .. c + G - 1 of row r of batch row b (the work of
-// one CTA of the statistics kernel): one record for the group in slot c,
-// identity records in the group's other slots.
-template <typename Tag, bool VEC>
-__device__ void stats_unit(const StatsParams& p, int b, int r, int c, StepSmem& sm) {
-  using Elem = typename Tag::Elem;
-  const int lo = c * p.CH, hi = min(p.V, lo + p.G * p.CH);
-  const int n_slots = min(p.G, p.C - c);
-  const Elem* row;
-  bool need_stats, need_top = false;
-  int j = 0;
-  if (r < p.Pz) {
-    row = static_cast<const Elem*>(p.Z) + static_cast<int64_t>(b) * p.zb + static_cast<int64_t>(r) * p.V;
-    need_stats = true;
-  } else {
-    j = r - p.Pz;
-    row = static_cast<const Elem*>(p.D) + static_cast<int64_t>(b) * p.db + static_cast<int64_t>(j) * p.V;
-    need_stats = j < p.Pds;
-    need_top = p.f > 0 && j < p.Pdf;
-    if (!need_stats && !need_top) return;
-  }
-  const float T = p.T[b];
-  const bool do_exp = need_stats && T > 0.f;  // uniform over the CTA
-  float cf = 0.f;
-  if (do_exp) cf = cta_temp_coeff(T, &sm.c2).x;
-  PartStat* out_part = p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C + c;
-  if (threadIdx.x > 0 && threadIdx.x < n_slots) {
-    PartStat id;
-    id.m = -INFINITY;
-    id.s = 0.f;
-    id.idx = kIdxNone;
-    id.flags = 0;
-    out_part[threadIdx.x] = id;
-  }
-  if (need_top) {
-    if (threadIdx.x < p.M)
-      sm.u.p1.st.mask[threadIdx.x] = p.mask[(static_cast<int64_t>(b) * p.Pdf + j) * p.M + threadIdx.x];
-    __syncthreads();
-    TopEntry* out_top = p.topk + ((static_cast<int64_t>(b) * p.Pdf + j) * p.C + c) * p.f;
-    if (do_exp)
-      stats_chunk<Tag, VEC, true, true>(p, row, lo, hi, cf, out_part, out_top, n_slots,
-                                        sm.u.p1.st, &sm.u.p1.ts);
-    else
-      stats_chunk<Tag, VEC, false, true>(p, row, lo, hi, cf, out_part, out_top, n_slots,
-                                         sm.u.p1.st, &sm.u.p1.ts);
-    return;
-  }
-  if (do_exp)
-    stats_chunk<Tag, VEC, true, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm.u.p1.st, nullptr);
-  else
-    stats_chunk<Tag, VEC, false, false>(p, row, lo, hi, cf, out_part, nullptr, 0, sm.u.p1.st, nullptr);
-}
-
 __device__ __forceinline__ float step_logit(const void* base, int dtype, int64_t i) {
   if (dtype == 1)
     return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(base) + i)) << 16);
@@ -253,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, kStepMinBlocks) step_kernel(StepPara
   for (int u = blockIdx.x; u < q.units; u += G) {
     const int c = (u % ngroups) * sp.G, rr = u / ngroups;
     __syncthreads();  // the previous unit's scratch
-    stats_unit<Tag, VEC>(sp, rr / sp.R, rr % sp.R, c, sm);
+    stats_unit<Tag, VEC>(sp, rr / sp.R, rr % sp.R, c, sm.u.p1.st, sm.u.p1.ts, &sm.c2);
   }
   bool ok = grid_barrier(q.bar, p.err, &sm.flag);
 
