@@ -171,6 +171,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
   const int b = blockIdx.x / cs;
   const int k = p.k, Pz = p.Pz;
 
+  // the cluster barrier's first phase: arrive now, wait before the first
+  // access to another CTA's shared memory (every CTA of the cluster has
+  // then started)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
   // inputs the statistics pass does not write, fetched before waiting for
   // it: the temperature (thread 0 turns it into log2(e)/T while the rest
   // loads the exp2 table) and what acceptance reads besides the statistics
@@ -196,6 +201,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
   const float2 c2 = cta_temp_coeff(greedy || t_bad ? 1.f : T, &sm.c2);  // holds a barrier
   const float c_hi = (greedy || t_bad) ? 0.f : c2.x, c_lo = (greedy || t_bad) ? 0.f : c2.y;
   pdl_wait();  // the statistics pass has completed and its partials are visible
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
   // 1. row merges: cluster-wide warp gw merges row gw (and its forks)
   const int gw = rank * kChainWarps + warp;

@@ -55,8 +55,12 @@ namespace cg = cooperative_groups;
 struct TreeSmem {
   float2 tab[64];
   float2 c2;
-  float2 slot[2];                            // this CTA's pass sum (by pass parity)
-  long long ctot;                            // this CTA's fixed-point total (the draw)
+  // every CTA's pass sum (by pass parity), fixed-point total and last
+  // positive index (the draw), pushed by that CTA into every CTA of the
+  // cluster before a cluster barrier: remote stores, then local reads
+  float2 slot[2][SSD_TREE_MAX_CLUSTER];
+  long long ctot[SSD_TREE_MAX_CLUSTER];
+  int clast_all[SSD_TREE_MAX_CLUSTER];
   int clast;                                 // this CTA's last positive index
   int res;                                   // rank 0: the drawn token (-1: none)
   int par[kMaxTreeNodes], tok[kMaxTreeNodes];
@@ -242,18 +246,23 @@ __device__ __forceinline__ void tree_pass(const typename Tag::Elem* zr,
   }
 }
 
-// Cluster total of the CTAs' sums (h, l): publish, cluster barrier, add the
-// cs sums in rank order (every CTA gets the same total).  Slots alternate by
-// pass parity, so a slot is rewritten only after the next barrier.
+// Cluster total of the CTAs' sums (h, l; every thread holds its CTA's):
+// threads 0 .. cs-1 push the sum into slot [parity][rank] of every CTA,
+// cluster barrier, then every CTA adds the cs local copies in rank order
+// (the same bits everywhere).  Slots alternate by pass parity, so a CTA
+// rewrites another's slot only after the barrier that follows that CTA's
+// reads.
 __device__ __forceinline__ void cluster_total(cg::cluster_group& cl, TreeSmem& sm, int& parity,
                                               float h, float l, float& th, float& tl) {
-  if (threadIdx.x == 0) sm.slot[parity] = make_float2(h, l);
+  const int cs = static_cast<int>(cl.num_blocks());
+  const int rank = static_cast<int>(cl.block_rank());
+  if (static_cast<int>(threadIdx.x) < cs)
+    *cl.map_shared_rank(&sm.slot[parity][rank], static_cast<int>(threadIdx.x)) = make_float2(h, l);
   cl.sync();
   th = 0.f;
   tl = 0.f;
-  const int cs = static_cast<int>(cl.num_blocks());
   for (int r = 0; r < cs; ++r) {
-    const float2 v = *cl.map_shared_rank(&sm.slot[parity], r);
+    const float2 v = sm.slot[parity][r];
     df_acc(th, tl, v.x, v.y);
   }
   parity ^= 1;
@@ -268,6 +277,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x / cs, N = p.N;
   const bool lead = rank == 0 && tid == 0;   // writes the outputs
+  // the cluster barrier's first phase: arrive now, wait before the first
+  // store into another CTA's shared memory (every CTA has then started)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   load_exp2_table(sm.tab);
   if (tid < N) {
     sm.par[tid] = p.parent[static_cast<int64_t>(b) * N + tid];
@@ -330,6 +342,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
       p.accept_len[b] = (!t_bad && sm.bad) ? -2 : -1;
       atomicOr(p.err, t_bad ? 0x1 : (sm.bad ? 0x4 : 0x2));
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     return;  // every CTA of the cluster leaves here (same data, same test)
   }
   if (greedy) {  // first child carrying the argmax, then the argmax
@@ -351,7 +364,8 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
       }
       p.accept_len[b] = depth;
     }
-    return;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    return;  // every CTA of the cluster leaves here (T is the row's)
   }
 
   // every child's e_z(x) and e_d(x) at its parent's rows, gathered in
@@ -392,6 +406,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   const bool use_cache = p.cache_stride > 0;
   float4* cache = use_cache ? p.cache + static_cast<int64_t>(b) * p.cache_stride + g : nullptr;
   int cached = -1;                          // the node whose exponentials the cache holds
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   for (;;) {
     while (c < N && sm.par[c] != cur) ++c;
     if (c >= N) break;  // the children of cur are exhausted
@@ -486,13 +501,18 @@ __global__ void __launch_bounds__(kTreeThreads) tree_walk_kernel(TreeParams p) {
   if (tid == 0) sm.clast = -1;
   __syncthreads();
   if (last >= 0) atomicMax(&sm.clast, last);
-  if (tid == 0) sm.ctot = cta_total;
+  __syncthreads();
+  if (tid < cs) {  // this CTA's total and last positive index into every CTA
+    TreeSmem* dst = cl.map_shared_rank(&sm, tid);
+    dst->ctot[rank] = cta_total;
+    dst->clast_all[rank] = sm.clast;
+  }
   cl.sync();
   long long before = 0;                     // the fixed-point totals of lower ranks
   int clast = -1;
   for (int r = 0; r < cs; ++r) {
-    if (r < rank) before += *cl.map_shared_rank(&sm.ctot, r);
-    clast = max(clast, *cl.map_shared_rank(&sm.clast, r));
+    if (r < rank) before += sm.ctot[r];
+    clast = max(clast, sm.clast_all[r]);
   }
   const long long incl = before + incl_cta;
   const float u = p.u_smp[b];
