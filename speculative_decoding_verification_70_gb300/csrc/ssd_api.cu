@@ -414,12 +414,13 @@ SliceParams slice_params(const VerifyCall& c, bool fork, const WsLayout& L, int 
   memset(&rp, 0, sizeof rp);
   rp.Z = Zb; rp.zb = c.zb; rp.Pz = sp.Pz;
   rp.D = Db; rp.db = c.db;
-  rp.V = c.V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = c.k;
+  rp.V = c.V; rp.C = L.dch.C; rp.CH = L.dch.CH; rp.E = L.dch.E; rp.R = L.R; rp.k = c.k;
   rp.T = c.T + b0; rp.u_smp = c.u_smp ? c.u_smp + b0 : nullptr;
   rp.rowstat = rowstat; rp.bstate = bstate;
-  rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm)) + static_cast<size_t>(b0) * C * 2;
-  rp.rthr = reinterpret_cast<long long*>(wsp(c.ws, L.rthr)) + static_cast<size_t>(b0) * C * 3 * kDrawThreads;
-  rp.racc = reinterpret_cast<long long*>(wsp(c.ws, L.racc)) + static_cast<size_t>(b0) * C * 2;
+  const size_t Cd = static_cast<size_t>(L.dch.C);
+  rp.rnorm = reinterpret_cast<long long*>(wsp(c.ws, L.rnorm)) + static_cast<size_t>(b0) * Cd * 2;
+  rp.rthr = reinterpret_cast<long long*>(wsp(c.ws, L.rthr)) + static_cast<size_t>(b0) * Cd * 3 * kDrawThreads;
+  rp.racc = reinterpret_cast<long long*>(wsp(c.ws, L.racc)) + static_cast<size_t>(b0) * Cd * 2;
   rp.amb_cnt = reinterpret_cast<int*>(wsp(c.ws, L.amb_cnt)) + b0;
   rp.amb_cap = amb_cap(c.V);
   rp.amb_idx = reinterpret_cast<int*>(wsp(c.ws, L.amb_idx)) + static_cast<size_t>(b0) * rp.amb_cap;
@@ -1102,7 +1103,7 @@ ssd_status ssd_sample_residual(const void* Z, int64_t z_bstride, const void* D, 
   memset(&rp, 0, sizeof rp);
   rp.Z = Z; rp.zb = z_bstride; rp.Pz = k + 1;
   rp.D = D; rp.db = d_bstride;
-  rp.V = V; rp.C = L.ch.C; rp.CH = L.ch.CH; rp.E = L.ch.E; rp.R = L.R; rp.k = k;
+  rp.V = V; rp.C = L.dch.C; rp.CH = L.dch.CH; rp.E = L.dch.E; rp.R = L.R; rp.k = k;
   rp.T = T; rp.u_smp = u_smp;
   rp.rowstat = pp.rowstat; rp.bstate = pp.bstate;
   rp.rnorm = reinterpret_cast<long long*>(wsp(ws, L.rnorm));

@@ -93,7 +93,8 @@ struct WsLayout {
   size_t err, part, topk, rowstat, bstate, rnorm, rthr, racc, amb_cnt, amb_idx, gpart, total;
   size_t srows, scta, sbar;   // the step kernel (batches of at most kStepMaxB rows)
   int B, R, Pf, f;
-  Chunking ch;
+  Chunking ch;    // the statistics pass
+  Chunking dch;   // the draw's passes
 };
 
 struct StatsParams {
@@ -479,6 +480,33 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Chunking of the draw's passes (norm pass, select): the statistics' chunks,
+// or more when B batch rows would give the norm pass too few CTAs to fill
+// the GPU (it aims at ~2432 CTAs, 16 per SM, like the statistics policy);
+// chunks of at least 2048 elements and at most 256 per row (the select runs
+// one chunk per thread).  At B = 64, V = 151936: 38 chunks of 4000 instead of
+// the statistics' 10 of 15200.  The per-thread sums of the norm pass take
+// 24 bytes per E elements of every row.
+inline Chunking make_draw_chunking(int B, int V, const Chunking& st) {
+  // batches of at most 16 rows draw in the cluster kernel by default; their
+  // batched draw (when selected) keeps the statistics' chunks, and so does
+  // their workspace
+  if (B <= 16) return st;
+  long long want = (2432 + (B > 0 ? B : 1) - 1) / (B > 0 ? B : 1);
+  const long long cap = (V + 2047) / 2048;
+  if (want > cap) want = cap;
+  if (want > 256) want = 256;
+  if (want <= st.C) return st;
+  Chunking d;
+  long long CH = (V + want - 1) / want;
+  CH = (CH + 7) / 8 * 8;
+  d.C = static_cast<int>((V + CH - 1) / CH);
+  d.CH = static_cast<int>(CH);
+  long long E = (CH + 255) / 256;
+  d.E = static_cast<int>((E + 7) / 8 * 8);
+  return d;
+}
+
 // Every workspace layout starts with the same header: the device error word
 // at offset 0 and the step kernel's barrier words at kWsStepBar.  No other
 // region of any layout overlaps the header, so the barrier words, zero when
@@ -506,9 +534,11 @@ inline WsLayout make_layout(int B, int k, int V, int f, int esize = 4) {
   L.part = off;                     off = align256(off + sizeof(PartStat) * B * L.R * C);
   L.rowstat = off;                  off = align256(off + sizeof(RowStat) * B * L.R);
   L.bstate = off;                   off = align256(off + sizeof(BState) * B);
-  L.rnorm = off;                    off = align256(off + sizeof(long long) * 2 * B * C);
-  L.rthr = off;                     off = align256(off + sizeof(long long) * 3 * kDrawThreads * B * C);
-  L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * C);
+  L.dch = make_draw_chunking(B, V, L.ch);
+  const size_t Cd = static_cast<size_t>(L.dch.C);
+  L.rnorm = off;                    off = align256(off + sizeof(long long) * 2 * B * Cd);
+  L.rthr = off;                     off = align256(off + sizeof(long long) * 3 * kDrawThreads * B * Cd);
+  L.racc = off;                     off = align256(off + sizeof(long long) * 2 * B * Cd);
   L.amb_cnt = off;                  off = align256(off + sizeof(int) * B);
   L.amb_idx = off;                  off = align256(off + sizeof(int) * B * amb_cap(V));
   L.gpart = off;                    off = align256(off + sizeof(GumbelPart) * B * L.Pf * C);
@@ -576,6 +606,7 @@ inline WsLayout make_softmax_layout(int rows, int V, int esize = 4) {
   L.Pf = 0;
   L.f = 0;
   L.ch = make_chunking(rows, 1, V, esize);
+  L.dch = L.ch;
   const size_t C = static_cast<size_t>(L.ch.C);
   size_t off = 0;
   L.err = off;                      off = kWsHeader;
