@@ -235,10 +235,22 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
       merge_topf_row(p.topk + (static_cast<int64_t>(b) * p.Pdf + j) * p.C * p.f, p.C, p.f, keep,
                      (st.flags & 1) != 0, p.fork_tok + o, p.fork_logit + o, sm.heads[warp]);
       if (lane == 0 && (st.flags & 1)) atomicOr(p.err, 0x2);
-      if (lane == 0 && cp.cache_on) __threadfence();  // the forks, before the cluster's insert reads them
+      if (cp.cache_on && greedy) {
+        // a greedy row draws nothing for the insert to hide behind: its
+        // forks go into the cache now, by the warp that merged them
+        __syncwarp();
+        const unsigned long long seq = (__ldcg(cp.cache.calls) + 1ull) << 32;
+        unsigned long long key;
+        if (lane < p.f && make_key(b, j, p.fork_tok[o + lane], key))
+          cache_insert_unique(cp.cache, key, seq | static_cast<unsigned long long>(o + lane),
+                              cp.payload + (o + lane) * cp.cache.depth);
+        __threadfence();
+      } else if (lane == 0 && cp.cache_on) {
+        __threadfence();  // the forks, before the cluster's insert reads them
+      }
     }
   }
-  cl.sync();  // every row's statistics in every CTA; the forks in global memory
+  cl.sync();  // every row's statistics in every CTA; the forks (greedy: in the cache) in global memory
 
 
   // 2. acceptance at each draft position (lane i of warp kAccWarp, in every CTA)
@@ -487,7 +499,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
     }
     cl.sync();  // the token is in rank 0's shared memory
     if (rank == 0 && tid == 0) p.out_tok[static_cast<int64_t>(b) * (k + 1) + n] = sm.res;
-  } else {
+  } else if (!greedy) {  // (a greedy row's forks went in with the merges)
     if (cp.cache_on && warp > 0) chain_insert(cp, b, rank, cs);
     cl.sync();  // the insert precedes the lookup (rank 0)
   }
