@@ -198,8 +198,14 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
   }
   const bool t_bad = isnan(T) || T < 0.f;
   const bool greedy = !(T > 0.f);
-  const float2 c2 = cta_temp_coeff(greedy || t_bad ? 1.f : T, &sm.c2);  // holds a barrier
-  const float c_hi = (greedy || t_bad) ? 0.f : c2.x, c_lo = (greedy || t_bad) ? 0.f : c2.y;
+  float c_hi = 0.f, c_lo = 0.f;
+  if (greedy || t_bad) {  // no exponentials: no coefficient (uniform over the cluster)
+    __syncthreads();
+  } else {
+    const float2 c2 = cta_temp_coeff(T, &sm.c2);  // holds a barrier
+    c_hi = c2.x;
+    c_lo = c2.y;
+  }
   pdl_wait();  // the statistics pass has completed and its partials are visible
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
