@@ -209,51 +209,61 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(ChainParams cp)
   pdl_wait();  // the statistics pass has completed and its partials are visible
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 
-  // 1. row merges: cluster-wide warp gw merges row gw (and its forks)
+  // 1. row merges: cluster-wide warp u < R merges row u; warp R + j merges
+  // the top-f lists of fork row j (in parallel with that row's own merge:
+  // it needs only the row's NaN flag, an OR over the partial records)
   const int gw = rank * kChainWarps + warp;
-  for (int r = gw; r < p.R; r += cs * kChainWarps) {
-    const bool is_target = r < Pz;
-    const int j = r - Pz;
-    const bool need_stats = is_target || j < p.Pds;
-    RowStat st;
-    float h, l;
-    merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c_hi, c_lo,
-              need_stats && !greedy && !t_bad, sm.tab, st, h, l);
-    // lane 0's values into every CTA: the CTAs take their decisions from
-    // these copies, so they must be the same bits
-    st.m = __shfl_sync(kFull, st.m, 0);
-    st.argmax = __shfl_sync(kFull, st.argmax, 0);
-    st.flags = __shfl_sync(kFull, st.flags, 0);
-    h = __shfl_sync(kFull, h, 0);
-    l = __shfl_sync(kFull, l, 0);
-    if (lane < cs) {
-      ChainSmem* dst = cl.map_shared_rank(&sm, lane);
-      dst->m[r] = st.m;
-      dst->sh[r] = h;
-      dst->sl[r] = l;
-      dst->am[r] = st.argmax;
-      dst->fl[r] = st.flags;
-    }
-    if (lane == 0) p.rowstat[static_cast<int64_t>(b) * p.Rp + r] = st;
-    if (!is_target && j < p.Pdf && p.fork_tok) {
-      const int64_t o = (static_cast<int64_t>(b) * p.Pdf + j) * p.f;
-      const int keep = p.fanout ? min(max(__ldg(p.fanout + j), 0), p.f) : p.f;
-      merge_topf_row(p.topk + (static_cast<int64_t>(b) * p.Pdf + j) * p.C * p.f, p.C, p.f, keep,
-                     (st.flags & 1) != 0, p.fork_tok + o, p.fork_logit + o, sm.heads[warp]);
-      if (lane == 0 && (st.flags & 1)) atomicOr(p.err, 0x2);
-      if (cp.cache_on && greedy) {
-        // a greedy row draws nothing for the insert to hide behind: its
-        // forks go into the cache now, by the warp that merged them
-        __syncwarp();
-        const unsigned long long seq = (__ldcg(cp.cache.calls) + 1ull) << 32;
-        unsigned long long key;
-        if (lane < p.f && make_key(b, j, p.fork_tok[o + lane], key))
-          cache_insert_unique(cp.cache, key, seq | static_cast<unsigned long long>(o + lane),
-                              cp.payload + (o + lane) * cp.cache.depth);
-        __threadfence();
-      } else if (lane == 0 && cp.cache_on) {
-        __threadfence();  // the forks, before the cluster's insert reads them
+  const int n_fork = p.fork_tok ? p.Pdf : 0;
+  for (int u = gw; u < p.R + n_fork; u += cs * kChainWarps) {
+    if (u < p.R) {
+      const int r = u;
+      const bool is_target = r < Pz;
+      const int j = r - Pz;
+      const bool need_stats = is_target || j < p.Pds;
+      RowStat st;
+      float h, l;
+      merge_row(p.part + (static_cast<int64_t>(b) * p.Rp + r) * p.C, p.C, c_hi, c_lo,
+                need_stats && !greedy && !t_bad, sm.tab, st, h, l);
+      // lane 0's values into every CTA: the CTAs take their decisions from
+      // these copies, so they must be the same bits
+      st.m = __shfl_sync(kFull, st.m, 0);
+      st.argmax = __shfl_sync(kFull, st.argmax, 0);
+      st.flags = __shfl_sync(kFull, st.flags, 0);
+      h = __shfl_sync(kFull, h, 0);
+      l = __shfl_sync(kFull, l, 0);
+      if (lane < cs) {
+        ChainSmem* dst = cl.map_shared_rank(&sm, lane);
+        dst->m[r] = st.m;
+        dst->sh[r] = h;
+        dst->sl[r] = l;
+        dst->am[r] = st.argmax;
+        dst->fl[r] = st.flags;
       }
+      if (lane == 0) p.rowstat[static_cast<int64_t>(b) * p.Rp + r] = st;
+      continue;
+    }
+    const int j = u - p.R;
+    const PartStat* parts = p.part + (static_cast<int64_t>(b) * p.Rp + Pz + j) * p.C;
+    int nan = 0;
+    for (int q = lane; q < p.C; q += 32) nan |= parts[q].flags & 1;
+    nan = __any_sync(kFull, nan != 0);
+    const int64_t o = (static_cast<int64_t>(b) * p.Pdf + j) * p.f;
+    const int keep = p.fanout ? min(max(__ldg(p.fanout + j), 0), p.f) : p.f;
+    merge_topf_row(p.topk + (static_cast<int64_t>(b) * p.Pdf + j) * p.C * p.f, p.C, p.f, keep,
+                   nan != 0, p.fork_tok + o, p.fork_logit + o, sm.heads[warp]);
+    if (lane == 0 && nan) atomicOr(p.err, 0x2);
+    if (cp.cache_on && greedy) {
+      // a greedy row draws nothing for the insert to hide behind: its
+      // forks go into the cache now, by the warp that merged them
+      __syncwarp();
+      const unsigned long long seq = (__ldcg(cp.cache.calls) + 1ull) << 32;
+      unsigned long long key;
+      if (lane < p.f && make_key(b, j, p.fork_tok[o + lane], key))
+        cache_insert_unique(cp.cache, key, seq | static_cast<unsigned long long>(o + lane),
+                            cp.payload + (o + lane) * cp.cache.depth);
+      __threadfence();
+    } else if (lane == 0 && cp.cache_on) {
+      __threadfence();  // the forks, before the cluster's insert reads them
     }
   }
   cl.sync();  // every row's statistics in every CTA; the forks (greedy: in the cache) in global memory
