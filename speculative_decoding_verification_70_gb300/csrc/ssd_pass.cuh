@@ -65,9 +65,13 @@ __device__ __forceinline__ float lg2_fast(float x) {
 // two perturbed logits tie that closely.
 __device__ __forceinline__ float gumbel_key(float z, float invT, uint32_t w) {
   const uint32_t m = w >> 9;
-  const float v = (static_cast<float>(8388607u - m) + 0.5f) * 1.1920928955078125e-7f;  // 1 - u
+  // u = (m + 1/2) 2^-23 and v = 1 - u without an integer-to-float
+  // conversion (a quarter-rate instruction): 1 + m 2^-23 is the float with
+  // mantissa m, and subtracting 1 - 2^-24 from it is exact (the operands are
+  // within a factor 2), as is 1 - u; the values are those of the definition
   constexpr float kLn2 = 0.693147180559945309f;
-  const float u = (static_cast<float>(m) + 0.5f) * 1.1920928955078125e-7f;
+  const float u = __uint_as_float(0x3f800000u | m) - __uint_as_float(0x3f7fffffu);
+  const float v = 1.0f - u;
   float s = fmaf(v, 0.2f, 0.25f);
   s = fmaf(v, s, 0.333333333f);
   s = fmaf(v, s, 0.5f);
@@ -345,6 +349,10 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
   float gy = -INFINITY;
   int gi = kIdxNone;
   const int v0 = lo / kV, v1 = (hi + kV - 1) / kV;
+  // the branch-free maximum update (index resolved after the pass) where
+  // the per-element work is heavier than a long fp32 stream's: bf16
+  // vectors and the Gumbel pass
+  constexpr bool kDefer = kV > 1 && (GUMBEL || kV == 8);
   for (int vb = v0 + tid; vb < v1; vb += kThreads * U) {
     typename Tag::Raw raw[U];
     float sc[U];
@@ -360,15 +368,26 @@ __device__ void stats_chunk(const StatsParams& p, const typename Tag::Elem* row,
     for (int u = 0; u < U; ++u) {
       const int vi = vb + u * kThreads;
       if (vi < v1) {
-        float z[8];
-        if (VEC) Tag::unpackraw(raw[u], z);
-        else z[0] = sc[u];
-        float m = z[0];
+        if constexpr (VEC && !GUMBEL && kV == 8) {
+          scan_bf16<DO_EXP, TOPF>(st, raw[u], vi * kV, c);
+        } else {
+          float z[8];
+          if (VEC) Tag::unpackraw(raw[u], z);
+          else z[0] = sc[u];
+          float m = z[0];
 #pragma unroll
-        for (int e = 1; e < kV; ++e) m = max_nan(m, z[e]);
-        scan_vector<DO_EXP, TOPF>(st, z, kV, m, vi * kV, c);
-        if constexpr (GUMBEL) gumbel_vector<kV>(*ga, z, vi * kV, gy, gi);
+          for (int e = 1; e < kV; ++e) m = max_nan(m, z[e]);
+          scan_vector<DO_EXP, TOPF, kDefer>(st, z, kV, m, vi * kV, c);
+          if constexpr (GUMBEL) gumbel_vector<kV>(*ga, z, vi * kV, gy, gi);
+        }
       }
+    }
+  }
+  if constexpr (kDefer) {  // the argmax's place inside its vector (an L2 hit)
+    if (st.idx != kIdxNone && !st.nan) {
+      float z[8];
+      Tag::unpackraw(Tag::loadraw(row + st.idx), z);
+      scan_resolve(st, z, kV);
     }
   }
   if constexpr (GUMBEL) {

@@ -52,7 +52,8 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 struct ScanState {
   float m;    // running maximum
   float s;    // running sum of 2^((z - m) c) (with sb: two lanes of a packed pair)
-  int idx;    // lowest index attaining m
+  int idx;    // lowest index attaining m (during the pass: the first index of
+              // the first vector attaining m; scan_resolve makes it exact)
   int nan;    // a NaN was seen
   float m2;   // second largest value -- kept only for top-f rows
   float sb;   // second lane of the running sum (pairs of elements)
@@ -70,9 +71,6 @@ __device__ __forceinline__ void scan_init(ScanState& st) {
 // The running sum: both lanes.
 __device__ __forceinline__ float scan_sum(const ScanState& st) { return st.s + st.sb; }
 
-// Max / argmax / NaN / (optionally) the online exponential sum over one
-// vector of n logits starting at index base_idx.  vm is the vector maximum
-// with NaN propagation (NaN iff the vector holds a NaN).
 // Second largest of the first n values of z (n = 1, 4 or 8), branch-free.
 __device__ __forceinline__ float second_max(const float (&z)[8], int n) {
   if (n == 1) return -INFINITY;
@@ -88,10 +86,36 @@ __device__ __forceinline__ float second_max(const float (&z)[8], int n) {
   return fmaxf(fminf(m4, n4), fmaxf(s4, t4));
 }
 
-// With SECOND the thread also keeps m2, the second largest value among its
-// elements (m2 <- max(m2, min(vector max, old max), second max of the
-// vector), exact for values, no branch).
-template <bool DO_EXP, bool SECOND = false>
+// The running maximum's update by one vector (maximum vm, first index
+// base_idx), without a branch: the warps' lanes meet new maxima at different
+// vectors, and a divergent branch would be taken by the whole warp on most
+// vectors of a short pass.  The sum is rescaled by f = 2^((m - m') c) only
+// when the maximum grows (f = 1 exactly otherwise, so the bits are those of
+// a branch around the rescale).  The position inside the vector is found
+// once, at the end (scan_resolve).
+template <bool DO_EXP>
+__device__ __forceinline__ void scan_max(ScanState& st, float vm, int base_idx, float c) {
+  const bool take = vm > st.m || st.idx == kIdxNone;
+  const float nm = take ? vm : st.m;
+  if (DO_EXP) {
+    const float f = (st.m == nm) ? 1.f : ex2_fast((st.m - nm) * c);
+    const f32x2 s2 = mul2(pk2(st.s, st.sb), pk2(f, f));
+    up2(s2, st.s, st.sb);
+  }
+  st.idx = take ? base_idx : st.idx;
+  st.m = nm;
+}
+
+// Max / argmax / NaN / (optionally) the online exponential sum over one
+// vector of n logits starting at index base_idx.  vm is the vector maximum
+// with NaN propagation (NaN iff the vector holds a NaN).  With SECOND the
+// thread also keeps m2, the second largest value among its elements
+// (m2 <- max(m2, min(vector max, old max), second max of the vector), exact
+// for values, no branch).  DEFER: the branch-free update of scan_max, the
+// index resolved by scan_resolve at the end; otherwise a branch taken when
+// the maximum grows finds the index at once (a long pass over fp32 rows,
+// where the extra exponential per vector would cost more than the branch).
+template <bool DO_EXP, bool SECOND = false, bool DEFER = false>
 __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], int n,
                                             float vm, int base_idx, float c) {
   if (vm != vm) {  // a NaN in the vector: the row is invalid
@@ -99,14 +123,16 @@ __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], 
     return;
   }
   if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(fminf(vm, st.m), second_max(z, n)));
-  if (vm > st.m || st.idx == kIdxNone) {
+  if (DEFER) {
+    scan_max<DO_EXP>(st, vm, base_idx, c);
+  } else if (vm > st.m || st.idx == kIdxNone) {
     int e_star = n - 1;
 #pragma unroll
     for (int e = 7; e >= 0; --e)
       if (e < n && z[e] == vm) e_star = e;
     if (DO_EXP) {
       // rescale the running sum to the new maximum
-      float f = (st.m == vm) ? 1.f : ex2_fast((st.m - vm) * c);
+      const float f = (st.m == vm) ? 1.f : ex2_fast((st.m - vm) * c);
       st.s = st.s * f;
       st.sb = st.sb * f;
     }
@@ -131,6 +157,92 @@ __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], 
         }
       up2(s2, st.s, st.sb);
     }
+  }
+}
+
+// The end of a thread's pass: st.idx names the first vector attaining st.m
+// (n logits z, as loaded again); the lowest element of it equal to st.m
+// makes the index exact.
+__device__ __forceinline__ void scan_resolve(ScanState& st, const float (&z)[8], int n) {
+  int e_star = n - 1;
+#pragma unroll
+  for (int e = 7; e >= 0; --e)
+    if (e < n && z[e] == st.m) e_star = e;
+  st.idx += e_star;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 vectors straight from the loaded words (eight logits in four 32-bit
+// words, element 2j in the low half of word j): the vector maximum (and, for
+// top-f rows, the second largest value) from bf16x2 maxima and minima --
+// exact, as bf16 values compare exactly -- and the exponentials on the
+// widened pairs.  Every float result is bit-identical to widening the eight
+// logits first and running scan_vector on them: the same operations on the
+// same values, the same lanes (even elements to s, odd ones to sb) and the
+// same order of the sums.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned bf2_max_nan(unsigned a, unsigned b) {
+  unsigned r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned bf2_max(unsigned a, unsigned b) {
+  unsigned r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned bf2_min(unsigned a, unsigned b) {
+  unsigned r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float bf_lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
+// both halves of w widened to binary32, as one packed pair (low half first)
+__device__ __forceinline__ f32x2 bf2_widen(unsigned w) {
+  f32x2 r;
+  asm("{\n\t.reg .b32 l, h;\n\tshl.b32 l, %1, 16;\n\tand.b32 h, %1, 0xffff0000;\n\t"
+      "mov.b64 %0, {l, h};\n\t}"
+      : "=l"(r)
+      : "r"(w));
+  return r;
+}
+
+template <bool DO_EXP, bool SECOND = false>
+__device__ __forceinline__ void scan_bf16(ScanState& st, const uint4& w, int base_idx, float c) {
+  float vm, v2 = -INFINITY;
+  if (SECOND) {
+    // per lane (even / odd elements) the largest and second largest of four,
+    // then the two lanes combined: the second largest of the eight values
+    const unsigned h01 = bf2_max_nan(w.x, w.y), l01 = bf2_min(w.x, w.y);
+    const unsigned h23 = bf2_max_nan(w.z, w.w), l23 = bf2_min(w.z, w.w);
+    const unsigned h = bf2_max_nan(h01, h23);
+    const unsigned s = bf2_max(bf2_min(h01, h23), bf2_max(l01, l23));
+    const float h0 = bf_lo(h), h1 = bf_hi(h);
+    vm = max_nan(h0, h1);
+    v2 = fmaxf(fminf(h0, h1), fmaxf(bf_lo(s), bf_hi(s)));
+  } else {
+    const unsigned h = bf2_max_nan(bf2_max_nan(w.x, w.y), bf2_max_nan(w.z, w.w));
+    vm = max_nan(bf_lo(h), bf_hi(h));
+  }
+  if (vm != vm) {  // a NaN in the vector: the row is invalid
+    st.nan = 1;
+    return;
+  }
+  if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(fminf(vm, st.m), v2));
+  scan_max<DO_EXP>(st, vm, base_idx, c);
+  if (DO_EXP) {
+    const float base = (st.m == -INFINITY) ? 0.f : st.m;
+    const f32x2 b2 = pk2(base, base), c2 = pk2(c, c);
+    f32x2 s2 = pk2(st.s, st.sb);
+    const unsigned ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x0, x1;
+      up2(mul2(sub2(bf2_widen(ws[j]), b2), c2), x0, x1);
+      s2 = add2(s2, pk2(ex2_fast(x0), ex2_fast(x1)));
+    }
+    up2(s2, st.s, st.sb);
   }
 }
 
