@@ -808,6 +808,10 @@ ssd_status ssd_draft_sample(const void* D, int64_t d_bstride, ssd_dtype dtype, i
   sp.err = reinterpret_cast<int*>(wsp(ws, L.err));
   sp.seed_lo = static_cast<uint32_t>(seed);
   sp.seed_hi = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {  // Philox4x32's key schedule: the Weyl increments
+    sp.rk0[r] = sp.seed_lo + static_cast<uint32_t>(r) * 0x9E3779B9u;
+    sp.rk1[r] = sp.seed_hi + static_cast<uint32_t>(r) * 0xBB67AE85u;
+  }
   sp.offset = offset;
   sp.Pf = L.Pf;
   sp.G = 1;

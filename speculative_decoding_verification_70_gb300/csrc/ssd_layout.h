@@ -119,6 +119,7 @@ struct StatsParams {
   // draft-side sampling (draft_kernel only)
   GumbelPart* gpart;   // [B][Pf][C]
   uint32_t seed_lo, seed_hi, offset;
+  uint32_t rk0[10], rk1[10];  // the generator's round keys (key schedule of the seed)
   int Pf;              // row pitch of gpart[] and topk[] (k + 1)
   // token trees: draft row j is read only if node j has a child (null: all)
   const int32_t* tree_parent;  // [B][tree_N]

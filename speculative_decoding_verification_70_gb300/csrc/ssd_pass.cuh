@@ -33,20 +33,26 @@ struct StatsSmem {
 // and u = (w >> 9 + 1/2) / 2^23 (23 bits: u and 1 - u are exact floats).
 // ---------------------------------------------------------------------------
 struct GumbelArgs {
-  uint32_t k0, k1, row, b, offset;
+  const uint32_t* rk0;  // round keys: key word 0 of rounds 0..9
+  const uint32_t* rk1;  // key word 1
+  uint32_t row, b, offset;
   float invT;
 };
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Ten rounds of Philox4x32 on counter c with precomputed round keys (the
+// seed's key schedule, formed once on the host): per round two 32x32->64
+// products, the high halves XORed with the other counter words and the
+// round key.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const uint32_t* rk0,
+                                               const uint32_t* rk1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += 0x9E3779B9u;
-      k1 += 0xBB67AE85u;
-    }
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    unsigned long long p0, p1;
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+    asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+    const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+    const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
+    c = make_uint4(hi1 ^ c.y ^ rk0[r], lo1, hi0 ^ c.w ^ rk1[r], lo0);
   }
   return c;
 }
@@ -88,7 +94,7 @@ __device__ __forceinline__ void gumbel_vector(const GumbelArgs& g, const float (
                                               float& gy, int& gi) {
   if (KV == 1) {
     const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(base) >> 2, g.row, g.b, g.offset),
-                                  g.k0, g.k1);
+                                  g.rk0, g.rk1);
     const int q = base & 3;
     const uint32_t word = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
     const float y = gumbel_key(z[0], g.invT, word);
@@ -100,7 +106,7 @@ __device__ __forceinline__ void gumbel_vector(const GumbelArgs& g, const float (
 #pragma unroll
     for (int h = 0; h < KV / 4; ++h) {
       const uint4 w = philox4x32_10(
-          make_uint4((static_cast<uint32_t>(base) >> 2) + h, g.row, g.b, g.offset), g.k0, g.k1);
+          make_uint4((static_cast<uint32_t>(base) >> 2) + h, g.row, g.b, g.offset), g.rk0, g.rk1);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {

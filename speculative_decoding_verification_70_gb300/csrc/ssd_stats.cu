@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, HAS_TOPF ? SSD_TOPF_MIN_BLOCKS : Tag
 // Gumbel-perturbed logit (T > 0 rows) and, with HAS_TOPF, a top-(f+1) list
 // (the forks with the drafted token masked are taken from it at the merge).
 template <typename Tag, bool VEC, bool HAS_TOPF>
-__global__ void __launch_bounds__(kThreads, SSD_TOPF_MIN_BLOCKS) draft_kernel(StatsParams p) {
+__global__ void __launch_bounds__(kThreads, SSD_TOPF_MIN_BLOCKS) draft_kernel(const __grid_constant__ StatsParams p) {
   using Elem = typename Tag::Elem;
   const int G = p.G;
   const int c = blockIdx.x * G, i = blockIdx.y + p.r0, b = blockIdx.z + p.b0;
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, SSD_TOPF_MIN_BLOCKS) draft_kernel(St
     }
   }
   GumbelArgs ga;
-  ga.k0 = p.seed_lo;
-  ga.k1 = p.seed_hi;
+  ga.rk0 = p.rk0;
+  ga.rk1 = p.rk1;
   ga.row = static_cast<uint32_t>(i);
   ga.b = static_cast<uint32_t>(b);
   ga.offset = p.offset;
