@@ -284,15 +284,14 @@ __device__ __forceinline__ void exp2_df2(f32x2 xh, f32x2 xl, const float2* tab, 
   lo = pk2(ok0 ? l0 : 0.f, ok1 ? l1 : 0.f);
 }
 
-// comp_acc for two lanes.
+// comp_acc for two lanes, with TwoSum in place of the ordered Fast2Sum: for
+// non-negative values both give the exact error of acc + vh, so every lane
+// is bit-identical to comp_acc, without the per-lane max / min and the
+// repacking they need.
 __device__ __forceinline__ void comp_acc2(f32x2& acc, f32x2& comp, f32x2 vh, f32x2 vl) {
-  float a0, a1, v0, v1;
-  up2(acc, a0, a1);
-  up2(vh, v0, v1);
-  const f32x2 big = pk2(fmaxf(a0, v0), fmaxf(a1, v1));
-  const f32x2 small = pk2(fminf(a0, v0), fminf(a1, v1));
-  const f32x2 t = add2(big, small);
-  comp = add2(comp, add2(add2(sub2(big, t), small), vl));
+  f32x2 t, err;
+  two_sum2(acc, vh, t, err);
+  comp = add2(comp, add2(err, vl));
   acc = t;
 }
 
