@@ -319,7 +319,18 @@ struct DevStreams {
   std::mutex mu;
   bool ready = false;
   bool failed = false;
+  // s1: target-row statistics; s2: draft-row (top-f) statistics, at the
+  // device's greatest priority so that its CTAs are dispatched first when
+  // both streams wait on the same fork event (the longer top-f CTAs first,
+  // the plain ones filling the last wave: at B = 512 the pass took 693 us
+  // in that order and 758 us in the other, which equal priorities left to
+  // chance from one call to the next)
   cudaStream_t s1 = nullptr, s2 = nullptr;
+  // the cache insert beside the draw, at the device's greatest priority: the
+  // norm pass fills every SM, and a side stream of equal priority got its
+  // CTAs only as the norm pass drained, so the select (which waits for the
+  // insert) started ~25 us after the norm pass at B = 512
+  cudaStream_t s3 = nullptr;
   cudaEvent_t ev[3 + 2 * kMaxSlices] = {};  // fork, per-slice joins, cache step
 };
 DevStreams g_streams[kMaxDevs];
@@ -333,8 +344,11 @@ DevStreams* device_streams() {
   std::lock_guard<std::mutex> lk(d.mu);
   if (d.ready) return &d;
   if (d.failed) return nullptr;
-  bool ok = cudaStreamCreateWithFlags(&d.s1, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&d.s2, cudaStreamNonBlocking) == cudaSuccess;
+  int least = 0, greatest = 0;
+  bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&d.s1, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&d.s2, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&d.s3, cudaStreamNonBlocking, greatest) == cudaSuccess;
   for (auto& e : d.ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     d.failed = true;
@@ -653,7 +667,7 @@ ssd_status run_verify(const VerifyCall& c, bool fork) {
     if (e == cudaSuccess) e = cudaStreamWaitEvent(c.stream, ds->ev[2 + 2 * i], 0);
     pass.end();
     if (e == cudaSuccess)
-      e = enqueue_tail(c, q, b1 - b0, vec, c.stream, i == S - 1, ds->s2, ds->ev[1 + 2 * kMaxSlices],
+      e = enqueue_tail(c, q, b1 - b0, vec, c.stream, i == S - 1, ds->s3, ds->ev[1 + 2 * kMaxSlices],
                        ds->ev[2 + 2 * kMaxSlices]);
   }
   return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
