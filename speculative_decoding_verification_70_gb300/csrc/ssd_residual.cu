@@ -268,6 +268,50 @@ __device__ int select_in_chunk(const typename Tag::Elem* zr, const typename Tag:
                                       df_to_fix(h, l, scale), sm, s_pick);
 }
 
+// The exact residual weights (2^60 fixed point) of the ambiguous-sign
+// elements amb[0..n) that lie in [lo, hi), each handed to add(i, w).  A long
+// list is taken in batches of K entries per thread, so that a batch's index
+// loads, then its logit loads, are in flight together (a row with a few
+// thousand entries otherwise pays two dependent global-memory latencies per
+// entry and thread); a list of at most one entry per thread takes K = 1.
+template <int K, typename Tag, typename Add>
+__device__ __forceinline__ void for_ambiguous_k(const int* amb, int n, int lo, int hi,
+                                                const typename Tag::Elem* zr,
+                                                const typename Tag::Elem* dr, const RowCtx& cx,
+                                                const float2* tab, Add&& add) {
+  for (int q0 = threadIdx.x; q0 < n; q0 += K * kThreads) {
+    int idx[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      const int q = q0 + j * kThreads;
+      const int i = q < n ? amb[q] : -1;
+      idx[j] = (i >= lo && i < hi) ? i : -1;
+    }
+    float z[K], d[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      z[j] = idx[j] >= 0 ? Tag::load1(zr + idx[j]) : 0.f;
+      d[j] = idx[j] >= 0 ? Tag::load1(dr + idx[j]) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      if (idx[j] < 0) continue;
+      float wh, wl;
+      weight<Q_RESID>(idx[j], z[j], d[j], cx, tab, wh, wl);
+      add(idx[j], df_to_fix(wh, wl, kFixResidual));
+    }
+  }
+}
+
+template <typename Tag, typename Add>
+__device__ __forceinline__ void for_ambiguous(const int* amb, int n, int lo, int hi,
+                                              const typename Tag::Elem* zr,
+                                              const typename Tag::Elem* dr, const RowCtx& cx,
+                                              const float2* tab, Add&& add) {
+  if (n > kThreads) for_ambiguous_k<8, Tag>(amb, n, lo, hi, zr, dr, cx, tab, add);
+  else for_ambiguous_k<1, Tag>(amb, n, lo, hi, zr, dr, cx, tab, add);
+}
+
 // grid B.  One CTA per batch row; every chunk-level step runs one chunk per
 // thread (C <= kThreads): the chunk weights are formed in parallel, an int64
 // block scan places the target, and one 128-bit product gives
@@ -338,13 +382,10 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
     const bool split = resid_row && n_amb <= p.amb_cap;
     const int* amb = p.amb_idx + static_cast<int64_t>(b) * p.amb_cap;
     if (split) {
-      for (int q = tid; q < n_amb; q += kThreads) {
-        const int i = amb[q];
-        float wh, wl;
-        weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
+      for_ambiguous<Tag>(amb, n_amb, 0, p.V, zr, dr, cx, tab, [&](int i, long long w) {
         atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[i / p.CH]),
-                  static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
-      }
+                  static_cast<unsigned long long>(w));
+      });
       __syncthreads();
     }
     // chunk weights in the units of the thread level: residual mass in
@@ -398,15 +439,10 @@ __global__ void __launch_bounds__(kThreads) residual_select_kernel(ResidualParam
       // per-thread sign-split masses plus each thread's ambiguous elements
       s_amb[tid] = 0;
       __syncthreads();
-      for (int r = tid; r < n_amb; r += kThreads) {
-        const int i = amb[r];
-        if (i >= clo && i < chi) {
-          float wh, wl;
-          weight<Q_RESID>(i, Tag::load1(zr + i), Tag::load1(dr + i), cx, tab, wh, wl);
-          atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[(i - clo) / p.E]),
-                    static_cast<unsigned long long>(df_to_fix(wh, wl, kFixResidual)));
-        }
-      }
+      for_ambiguous<Tag>(amb, n_amb, clo, chi, zr, dr, cx, tab, [&](int i, long long w) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&s_amb[(i - clo) / p.E]),
+                  static_cast<unsigned long long>(w));
+      });
       __syncthreads();
       const long long w =
           split_mass(own[kDrawThreads], own[2 * kDrawThreads], s_acc[0], s_acc[1]) + s_amb[tid];
