@@ -38,6 +38,7 @@ CACHE_DEPTH = 7
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stats_pass_mixed512.md")
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["speculative_decoding_verification_70_gb300/csrc/ssd_stats.cu",
+                  "speculative_decoding_verification_70_gb300/csrc/ssd_pass.cuh",
                   "speculative_decoding_verification_70_gb300/csrc/ssd_scan.cuh",
                   "speculative_decoding_verification_70_gb300/csrc/ssd_device.cuh",
                   "speculative_decoding_verification_70_gb300/csrc/ssd_layout.h"]
