@@ -293,9 +293,12 @@ __device__ __forceinline__ float logit_at(const void* base, int dtype, int64_t i
 
 // grid: B.  Verification (and, when fork_tok != null, the forked top-f).
 // NW warps per CTA: 8 for large batches; 16 at small B, where the CTA's
-// row merges are the critical path (one round for 2(k+1) <= 16 rows).
+// row merges are the critical path (one round for 2(k+1) <= 16 rows).  With
+// 8 warps (B > 152) four CTAs fit an SM (64 registers), so 512 rows take one
+// wave (measured at B = 512: 18.2 against 22.1 us per launch with the
+// unconstrained 112 registers and two CTAs per SM).
 template <int NW>
-__global__ void __launch_bounds__(NW * 32) finalize_kernel(FinalizeParams p) {
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 4 : 1) finalize_kernel(FinalizeParams p) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float2 tab[64];
