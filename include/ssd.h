@@ -512,7 +512,9 @@ SSD_API int ssd_spec_cache_depth(const ssd_spec_cache *cache);
  * device time.  Entries with launches == 0 are phases that span several
  * launches: "stats_pass" is the statistics pass of a batched verify, whose
  * target-row and draft-row kernels run concurrently on two internal streams,
- * from the fork to the join on the caller's stream.  Events are created at
+ * from the fork to the join on the caller's stream; "stats_span" is the same
+ * pass without the fork and join: from the earlier of its two launches'
+ * begin events to the later of their end events.  Events are created at
  * begin and destroyed at end.
  */
 typedef struct {

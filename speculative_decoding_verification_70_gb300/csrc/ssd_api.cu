@@ -1444,6 +1444,41 @@ ssd_status ssd_profile_end(ssd_profile_entry* out, int cap, int* n_out) {
     ms[r.kernel] += t;
     timed[r.kernel] += 1;
   }
+  // "stats_span": for each statistics-pass phase (fork to join on the
+  // caller's stream), the span of its two launches on the internal streams,
+  // from the earlier of their begin events to the later of their end events
+  // (the kernels' own time, without the fork and join)
+  auto find_id = [&](const char* nm) {
+    for (size_t i = 0; i < g_prof.names.size(); ++i)
+      if (strcmp(g_prof.names[i], nm) == 0) return static_cast<int>(i);
+    return -1;
+  };
+  const int id_pass = find_id("stats_pass"), id_t = find_id("stats_topf"), id_p = find_id("stats");
+  if (id_pass >= 0 && id_t >= 0 && id_p >= 0) {
+    const int id_span = g_prof.kernel_id("stats_span");
+    ms.resize(g_prof.names.size(), 0.0);
+    timed.resize(g_prof.names.size(), 0);
+    const size_t nr = g_prof.recs.size();
+    for (size_t i = 0; i < nr; ++i) {
+      if (g_prof.recs[i].kernel != id_pass) continue;
+      const ProfRecord* rt = nullptr;
+      const ProfRecord* rp = nullptr;
+      for (size_t j = i + 1; j < nr && g_prof.recs[j].kernel != id_pass; ++j) {
+        if (g_prof.recs[j].kernel == id_t && !rt) rt = &g_prof.recs[j];
+        if (g_prof.recs[j].kernel == id_p && !rp) rp = &g_prof.recs[j];
+      }
+      if (!rt || !rp) continue;
+      const cudaEvent_t ref = g_prof.recs[i].a;
+      float bt = 0.f, bp = 0.f, et = 0.f, ep = 0.f;
+      if (cudaEventElapsedTime(&bt, ref, rt->a) != cudaSuccess ||
+          cudaEventElapsedTime(&bp, ref, rp->a) != cudaSuccess ||
+          cudaEventElapsedTime(&et, ref, rt->b) != cudaSuccess ||
+          cudaEventElapsedTime(&ep, ref, rp->b) != cudaSuccess)
+        continue;
+      ms[id_span] += static_cast<double>(et > ep ? et : ep) - (bt < bp ? bt : bp);
+      timed[id_span] += 1;
+    }
+  }
   int n = 0;
   for (size_t i = 0; i < g_prof.names.size() && out && n < cap; ++i, ++n) {
     memset(&out[n], 0, sizeof out[n]);
