@@ -457,10 +457,14 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
   if (C < c0) C = c0;
   if (C > 256) C = 256;
   if (C < 1) C = 1;
-  // a grid a little above one wave of the statistics kernel (6 CTAs per SM
-  // on 152 SMs) is cut to one wave: the few CTAs of a second wave would
-  // cost a whole CTA latency (e.g. B = 1, 16 rows: 57 chunks, not 63)
-  if (rows * C > 912 && rows * C < 1824 && 912 / rows >= c0) C = 912 / rows;
+  // a grid below two waves of the statistics kernel (6 CTAs per SM on 152
+  // SMs) is cut to half a wave, three CTAs per SM: there the CTAs' fixed
+  // costs (set-up, block reduction, top-f selection) and the sharing of an
+  // SM by six CTAs set the pass's time (B = 1, ssd_fork's 16 rows: 28
+  // chunks per row, 448 CTAs; the step as a graph 17.9 / 32.3 us at T = 0 /
+  // 1 against 18.0 / 32.6 us with the one-wave cut's 57 chunks; llama_sd
+  // 22.3 against 22.9 us at T = 1)
+  if (rows * C < 1824 && 456 / rows >= c0) C = 456 / rows;
   long long CH = (V + C - 1) / C;
   const int ov = g_split.chunk.load(std::memory_order_relaxed);
   if (ov > 0) {
