@@ -439,9 +439,13 @@ inline int split_group(int policy, int C) {
 }
 
 // Chunking policy: chunks of at most 32 KB (so that one chunk fits a
-// shared-memory stage); for small batches more chunks so the grid fills the
-// GPU (at least ~16 CTAs per SM on 152 SMs), but no chunk below 2048
-// elements.  esize is the logit element size; sizing with esize = 4 gives
+// shared-memory stage); for small batches more chunks, enough for about one
+// wave of the statistics kernel (912 CTAs: 6 per SM on 152 SMs), but no
+// chunk below 2048 elements.  Aiming at 2432 CTAs (16 per SM) gave small
+// CTAs whose fixed costs set the time: the verify + fork + cache step with
+// one-wave chunks takes 36.8 / 40.8 / 62.9 us at B = 2 / 4 / 8 (ssd_fork
+// rows) against 41.0 / 45.3 / 65.7, and 41.1 / 74.0 us at B = 4 / 16
+// (qwen_b64 rows) against 46.3 / 76.3.  esize is the logit element size; sizing with esize = 4 gives
 // the most chunks, which is what the workspace is sized for.  An override
 // of the chunk length is clamped to [ceil(V / 256), 32 KB of elements] (at
 // most 256 chunks: the draw's select runs one chunk per thread; at most
@@ -451,7 +455,7 @@ inline Chunking make_chunking(int B, int rows_per_b, int V, int esize) {
   long long rows = static_cast<long long>(B) * (rows_per_b > 0 ? rows_per_b : 1);
   const long long max_ch = kMaxChunkBytes / esize;
   long long c0 = (V + max_ch - 1) / max_ch;
-  long long want = (2432 + rows - 1) / rows;
+  long long want = (912 + rows - 1) / rows;
   long long cap = (V + 2047) / 2048;
   long long C = want < cap ? want : cap;
   if (C < c0) C = c0;
