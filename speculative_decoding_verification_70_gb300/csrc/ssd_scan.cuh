@@ -122,10 +122,15 @@ __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], 
     st.nan = 1;
     return;
   }
-  if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(fminf(vm, st.m), second_max(z, n)));
   if (DEFER) {
+    if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(fminf(vm, st.m), second_max(z, n)));
     scan_max<DO_EXP>(st, vm, base_idx, c);
   } else if (vm > st.m || st.idx == kIdxNone) {
+    // a new maximum: the old one and the vector's second value can be
+    // second; on the (common) other path the vector's own maximum bounds
+    // all its elements, so the second-largest network runs only here --
+    // the same m2 as taking min(vm, m) and the vector's second value always
+    if (SECOND) st.m2 = fmaxf(st.m2, fmaxf(st.m, second_max(z, n)));
     int e_star = n - 1;
 #pragma unroll
     for (int e = 7; e >= 0; --e)
@@ -138,6 +143,8 @@ __device__ __forceinline__ void scan_vector(ScanState& st, const float (&z)[8], 
     }
     st.m = vm;
     st.idx = base_idx + e_star;
+  } else if (SECOND) {
+    st.m2 = fmaxf(st.m2, vm);  // vm <= m
   }
   if (DO_EXP) {
     float base = (st.m == -INFINITY) ? 0.f : st.m;
