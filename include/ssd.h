@@ -102,9 +102,10 @@ SSD_API int ssd_version(void);
  * the error-word reads, which say so).  The verify calls (all but
  * ssd_verify_noalloc) run the target-row and draft-row statistics on two
  * internal streams forked from and joined back to the caller's stream by
- * events, and the SSD round step inserts the forks into the cache on the
- * second one beside the draw; the streams and events are created on the
- * first such call on a device.  Calls can therefore be captured into a CUDA
+ * events (the draft-row stream at the device's greatest priority), and the
+ * SSD round step inserts the forks into the cache on a third one, also at
+ * the greatest priority, beside the draw; the streams and events are
+ * created on the first such call on a device.  Calls can therefore be captured into a CUDA
  * graph (make one verify call on the device before capturing).  B may exceed
  * 65535: kernels launch in grids of 65535 batch rows.
  */
