@@ -111,7 +111,9 @@ __device__ __forceinline__ void scan_max(ScanState& st, float vm, int base_idx, 
 // with NaN propagation (NaN iff the vector holds a NaN).  With SECOND the
 // thread also keeps m2, the second largest value among its elements
 // (m2 <- max(m2, min(vector max, old max), second max of the vector), exact
-// for values, no branch).  DEFER: the branch-free update of scan_max, the
+// for values; without DEFER the vector's second value is formed only when
+// the maximum grows, the vector maximum bounding it otherwise).  DEFER: the
+// branch-free update of scan_max, the
 // index resolved by scan_resolve at the end; otherwise a branch taken when
 // the maximum grows finds the index at once (a long pass over fp32 rows,
 // where the extra exponential per vector would cost more than the branch).
